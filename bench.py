@@ -1,0 +1,360 @@
+#!/usr/bin/env python
+"""Throughput of the speculative-tree hot path: verified trees/s and logit GB/s.
+
+One step = spec_tree_build (support selection + dual-identity expansion of
+every draft row, then top-R ranking) + spec_tree_verify over one batch of
+trees whose draft and target logits are resident in HBM.  Prints one JSON
+line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs one process per GPU under torchrun: each rank owns its own batch of
+trees (weak scaling); the only collectives are the barrier around the timed
+region and the max over ranks of its duration.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified trees/sec and logit GB/s (fraction of GB300 HBM peak) at 128K vocab"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama3_b64")
+    ap.add_argument("--batch", type=int, default=None, help="override trees per GPU")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload(args):
+    from dynamic_tree_speculative_gb300 import workloads as WL
+    wl = WL.BENCH_WORKLOAD if args.workload == "llama3_b64" else WL.WORKLOADS[args.workload]
+    if args.batch:
+        wl = wl.with_(B=args.batch)
+    return wl
+
+
+def describe(wl) -> str:
+    return (f"{wl.name}: V={wl.V} {wl.dtype} logits, {wl.B} trees per GPU, K={wl.K}, m={wl.m}, W={wl.W}, "
+            f"depth {wl.depth}, R={wl.R}, T={wl.temperature}, builder {wl.builder}, top-{wl.support} support")
+
+
+def config_of(wl, n_gpus):
+    return {"workload": describe(wl), "trees_per_gpu": wl.B, "global_batch": wl.B * n_gpus, "vocab": wl.V,
+            "K": wl.K, "m": wl.m, "W": wl.W, "depth": wl.depth, "R": wl.R, "temperature": wl.temperature,
+            "builder": wl.builder, "support": wl.support, "zipf_a": wl.zipf_a, "sigma_draft": wl.sigma_draft,
+            "parallelism": f"trees sharded over {n_gpus} GPU(s), no collective on the data path",
+            "l2": "inputs larger than L2: every step streams all draft rows and the accepted target rows"}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks ---
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the GPU works."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "20", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": "nvidia-smi unavailable"}
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"error": "no samples"}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[6 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "interval_ms": 20,
+                "window": "warm-up + timed steps"}
+
+
+# ------------------------------------------------------------ CPU oracle ---
+
+def oracle_trees(wl, seed, tree_ids, budget_s, warm=0):
+    """Build + verify trees of the workload through the float64 oracle; returns (trees, seconds)."""
+    import numpy as np
+    import torch
+    from dynamic_tree_speculative_gb300 import workloads as WL
+    from oracle import spec_tree_oracle as O
+    op = O.Params(K=wl.K, m=wl.m, W=wl.W, depth=wl.depth, R=wl.R, temperature=wl.temperature,
+                  support=wl.support, builder=wl.builder, lam=wl.lam, beta=wl.beta, gamma=wl.gamma,
+                  delta=wl.delta, rho=wl.rho, eta=wl.eta, alpha=wl.alpha)
+    n_rows = wl.n_exp
+    u_probe = WL.build_uniforms(wl, seed, n_rows)
+    uv, ub = WL.verify_uniforms(wl, seed)
+    done, spent = 0, 0.0
+    for i, b in enumerate(tree_ids):
+        draft, latent = WL.draft_logits(wl, seed, n_rows=n_rows, trees=[b])
+        rows = WL.to_numpy_f64(draft[0])
+        t0 = time.perf_counter()
+        tree = O.build(rows, u_probe[b].numpy().astype(np.float64), op)
+        t1 = time.perf_counter()
+        exp_row = torch.full((1, wl.R + 1), -1, dtype=torch.int32)
+        exp_row[0, :tree.n_nodes] = torch.from_numpy(tree.exp_row.astype(np.int32))
+        target = WL.to_numpy_f64(WL.target_logits(wl, seed, latent, exp_row, trees=[b])[0])
+        t2 = time.perf_counter()
+        O.verify(tree, target, uv[b].numpy(), float(ub[b]), op)
+        t3 = time.perf_counter()
+        if i >= warm:
+            done += 1
+            spent += (t1 - t0) + (t3 - t2)
+        if budget_s is not None and spent >= budget_s:
+            break
+    return done, spent
+
+
+def run_reference(args):
+    """The CPU oracle, as it stands, on the host cores: one tree of the workload per step."""
+    from dynamic_tree_speculative_gb300 import ranks as R
+    info = R.rank_info()
+    if not info.is_root:
+        return 0
+    wl = workload(args)
+    ids = [i % wl.B for i in range(args.warmup + args.steps)]
+    done, spent = oracle_trees(wl, args.seed, ids, None, warm=args.warmup)
+    value = done / spent
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "trees/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * spent / done,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl, args.gpus),
+            "cpu_baseline": {"value": value, "unit": "trees/s", "cores": 1, "kind": "oracle",
+                             "sample": f"one tree of the workload per step ({done} trees, build + verify)"},
+            "e2e": {"value": value, "unit": "trees/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# -------------------------------------------------------------- our arm ---
+
+def select_expand_traffic(V):
+    """DRAM bytes per select_expand launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "select_expand_traffic.json")
+    src = os.path.join(ROOT, "dynamic_tree_speculative_gb300", "csrc", "select_expand.cu")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if d.get("source_sha256") != h:
+            return None
+        return d
+    except Exception:
+        return None
+
+
+def run_ours(args):
+    import torch
+    from dynamic_tree_speculative_gb300 import binding as B
+    from dynamic_tree_speculative_gb300 import ranks as R
+    from dynamic_tree_speculative_gb300 import workloads as WL
+
+    info = R.rank_info()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device(f"cuda:{info.local_rank}")
+    torch.cuda.set_device(dev)
+    R.init(info, "nccl")
+    wl = workload(args)
+    seed = R.rank_seed(args.seed, info.rank)
+    params = B.Params.from_workload(wl)
+    cparams = params.c()
+    n_rows = B.rows_needed(params)
+    V = wl.V
+
+    draft, latent = WL.draft_logits(wl, seed, n_rows=n_rows, device=dev)
+    u_probe = WL.build_uniforms(wl, seed, n_rows, device=dev)
+    uv, ub = WL.verify_uniforms(wl, seed, device=dev)
+    tree = B.TreeBuffers(params, wl.B, device=dev)
+    out = B.VerifyOutputs(params, wl.B, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    B.spec_tree_build(cparams, V, draft, u_probe, tree, status)
+    torch.cuda.synchronize()
+    target = WL.target_logits(wl, seed, latent, tree.node_exp_row, device=dev)
+    del latent
+    torch.cuda.empty_cache()
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        B.spec_tree_select_expand(cparams, V, draft, u_probe, tree, status, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        B.spec_tree_rank(cparams, V, tree, status, stream)
+        B.spec_tree_verify(cparams, V, target, tree, uv, ub, out.accept_len, out.out_tok, out.out_node, None,
+                           status, stream)
+
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else info.local_rank)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    R.barrier(info, dev)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for k in range(K):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    R.barrier(info, dev)
+    clk = clocks.stop()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    k1_s = statistics.mean(a.elapsed_time(b) for a, b in evs) / 1e3
+    st = int(status.item())
+
+    acc = out.accept_len.cpu()
+    trees_rate = R.whole_job_rate(wl.B * K, elapsed, info, dev)
+    slowest = R.max_over_ranks(elapsed, info, dev)
+    S = min(wl.support, V)
+    es = 2 if wl.dtype == "bf16" else 4
+    draft_bytes = wl.B * n_rows * V * es
+    sup_bytes = wl.B * n_rows * (S * 12 + 12)
+    target_bytes = int((acc.long() + 1).sum()) * V * es
+    step_bytes = draft_bytes + sup_bytes + target_bytes
+    logit_gbs = R.sum_over_ranks(step_bytes * K, info, dev) / slowest / 1e9
+    hbm, peak_kind = peaks()
+    k1_bytes = draft_bytes + sup_bytes + wl.B * n_rows * 4
+    achieved = k1_bytes / k1_s / 1e9
+    trf = select_expand_traffic(V)
+
+    result = {
+        "metric": METRIC, "value": trees_rate, "unit": "trees/s", "n_gpus": info.world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": 1e3 * slowest / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic", "config": config_of(wl, info.world),
+        "logit_gbs": logit_gbs, "logit_frac_of_peak": logit_gbs / (hbm * info.world),
+        "peak_kind": peak_kind, "status": st,
+        "accept_len_mean": float(acc.float().mean()),
+        "roofline": {"kernel": "select_expand", "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_kind": f"{peak_kind} copy bandwidth (burst)",
+                     "traffic": None if trf is None else trf["dram_bytes_per_launch_scaled"],
+                     "algorithmic_bytes_per_launch": k1_bytes, "avg_launch_ms": 1e3 * k1_s},
+        "gpu_launches": 3 * K, "clocks": clk,
+    }
+
+    if info.is_root and info.world == 1 and not args.no_cpu_baseline:
+        done, spent = oracle_trees(wl, seed, list(range(wl.B)), args.cpu_seconds)
+        result["cpu_baseline"] = {"value": done / spent, "unit": "trees/s", "cores": 1, "kind": "oracle",
+                                  "sample": f"{done} trees of this workload (build + verify), float64 numpy, "
+                                            "one thread"}
+
+    if not args.no_e2e:
+        result["e2e"] = e2e(args, wl, cparams, draft, target, u_probe, uv, ub, tree, out, status, info, dev, K)
+    if info.is_root:
+        print(json.dumps(result), flush=True)
+    if info.world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e(args, wl, cparams, draft, target, u_probe, uv, ub, tree, out, status, info, dev, K):
+    """Same metric through the public API with inputs in pinned host memory and results read back."""
+    import torch
+    from dynamic_tree_speculative_gb300 import binding as B
+    from dynamic_tree_speculative_gb300 import ranks as R
+    hosts = [x.cpu().pin_memory() for x in (draft, target, u_probe, uv, ub)]
+    devs = [draft, target, u_probe, uv, ub]
+    res_h = [torch.empty(out.accept_len.shape, dtype=torch.int32).pin_memory(),
+             torch.empty(out.out_tok.shape, dtype=torch.int32).pin_memory()]
+    stream = torch.cuda.current_stream()
+    V = wl.V
+
+    def step():
+        for d, h in zip(devs, hosts):
+            d.copy_(h, non_blocking=True)
+        B.spec_tree_build(cparams, V, draft, u_probe, tree, status, stream)
+        B.spec_tree_verify(cparams, V, target, tree, uv, ub, out.accept_len, out.out_tok, out.out_node, None,
+                           status, stream)
+        res_h[0].copy_(out.accept_len, non_blocking=True)
+        res_h[1].copy_(out.out_tok, non_blocking=True)
+
+    for _ in range(min(args.warmup, 2)):
+        step()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    R.barrier(info, dev)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(K):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    R.barrier(info, dev)
+    el = R.max_over_ranks(a.elapsed_time(b) / 1e3, info, dev)
+    h2d = sum(h.numel() * h.element_size() for h in hosts)
+    d2h = sum(h.numel() * h.element_size() for h in res_h)
+    return {"value": R.sum_over_ranks(wl.B * K, info, dev) / el, "unit": "trees/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+            "path": "pinned host -> HBM copies, spec_tree_build, spec_tree_verify, results -> host"}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

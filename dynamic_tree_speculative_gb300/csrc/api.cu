@@ -1,0 +1,208 @@
+// Host side of the C ABI (include/spec_tree.h): argument checks and launches.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "spec_tree.h"
+#include "st_kernels.h"
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+
+int num_sms_of_current_device() {
+  static int cache[MAX_DEVICES] = {0};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+int support_size(const spec_tree_params* p, int V) {
+  const int s = p->support == 0 ? SPEC_TREE_MAX_SUPPORT : p->support;
+  return s < V ? s : V;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+int elem_size(int dtype) { return dtype == SPEC_TREE_BF16 ? 2 : (dtype == SPEC_TREE_F32 ? 4 : 0); }
+
+int check_rows(int dtype, const void* logits, int64_t row_stride, int V) {
+  const int es = elem_size(dtype);
+  if (es == 0) return SPEC_TREE_E_LAYOUT;
+  if (logits == nullptr) return SPEC_TREE_E_PARAM;
+  if (row_stride < V) return SPEC_TREE_E_PARAM;
+  if (!aligned16(logits) || (row_stride * es) % 16 != 0) return SPEC_TREE_E_LAYOUT;
+  return SPEC_TREE_OK;
+}
+
+int check_tree(const spec_tree_params* p, const spec_tree_t* t, int V, bool need_nodes, bool need_sup) {
+  if (t == nullptr) return SPEC_TREE_E_PARAM;
+  const int S = support_size(p, V);
+  if (need_sup && (t->sup_id == nullptr || t->sup_q == nullptr || t->sup_qT == nullptr || t->sup_z == nullptr ||
+                   t->sup_zT == nullptr || t->probe_pos == nullptr || t->sup_stride < S))
+    return SPEC_TREE_E_PARAM;
+  if (need_nodes && (t->node_token == nullptr || t->node_parent == nullptr || t->node_depth == nullptr ||
+                     t->node_kind == nullptr || t->node_slot == nullptr || t->node_exp_row == nullptr ||
+                     t->node_score == nullptr || t->n_nodes == nullptr || t->max_nodes < p->R + 1 ||
+                     t->max_nodes > SPEC_TREE_MAX_NODES))
+    return SPEC_TREE_E_PARAM;
+  if (t->n_rows < spec_tree_rows_needed(p)) return SPEC_TREE_E_PARAM;
+  return SPEC_TREE_OK;
+}
+
+cudaStream_t as_stream(spec_tree_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+int spec_tree_rows_needed(const spec_tree_params* p) {
+  if (p == nullptr) return 0;
+  if (p->builder == SPEC_TREE_BUILDER_SMART) return p->R + 1;
+  return 1 + (p->depth - 1) * p->W;
+}
+
+int spec_tree_check_params(const spec_tree_params* p, int V) {
+  if (p == nullptr) return SPEC_TREE_E_PARAM;
+  if (V < 1 || V >= (1 << 24)) return SPEC_TREE_E_PARAM;
+  if (p->support < 0 || p->support > SPEC_TREE_MAX_SUPPORT) return SPEC_TREE_E_PARAM;
+  const int S = support_size(p, V);
+  if (p->K < 1 || p->K > S || p->m < 0 || p->m >= p->K) return SPEC_TREE_E_PARAM;
+  if (p->depth < 1 || p->depth > 255 || p->R < 1 || p->R + 1 > SPEC_TREE_MAX_NODES) return SPEC_TREE_E_PARAM;
+  if (!(p->temperature > 0.0f) || !isfinite(p->temperature)) return SPEC_TREE_E_PARAM;
+  if (p->builder == SPEC_TREE_BUILDER_TOPR) {
+    if (p->W < 1 || p->W > 4095 || p->W > SPEC_TREE_MAX_NODES) return SPEC_TREE_E_PARAM;
+    const int64_t ncand = p->K + static_cast<int64_t>(p->depth - 1) * p->W * p->K;
+    if (ncand > SPEC_TREE_MAX_CAND) return SPEC_TREE_E_PARAM;
+  } else if (p->builder == SPEC_TREE_BUILDER_SMART) {
+    if (static_cast<int64_t>(p->K) * (p->R + 1) > SPEC_TREE_MAX_CAND) return SPEC_TREE_E_PARAM;
+    const float c[7] = {p->lambda, p->beta, p->gamma, p->delta, p->rho, p->eta, p->alpha};
+    for (float x : c)
+      if (!isfinite(x)) return SPEC_TREE_E_PARAM;
+    if (p->lambda < 0.0f || p->gamma < 0.0f || p->delta < 0.0f || p->rho < 1.0f || !(p->alpha > 0.0f))
+      return SPEC_TREE_E_PARAM;
+  } else {
+    return SPEC_TREE_E_PARAM;
+  }
+  return SPEC_TREE_OK;
+}
+
+int spec_tree_select_expand(const spec_tree_params* p, int B, int V, int dtype, const void* draft_logits,
+                            int64_t row_stride, const float* u_probe, const spec_tree_t* tree, uint32_t* status,
+                            spec_tree_stream_t stream) {
+  int rc = spec_tree_check_params(p, V);
+  if (rc) return rc;
+  if (B < 0 || u_probe == nullptr) return SPEC_TREE_E_PARAM;
+  if ((rc = check_rows(dtype, draft_logits, row_stride, V))) return rc;
+  if ((rc = check_tree(p, tree, V, false, true))) return rc;
+  const int needed = spec_tree_rows_needed(p);
+  st::SelLaunch L;
+  L.logits = draft_logits;
+  L.row_stride = row_stride;
+  L.n_rows = tree->n_rows;
+  L.rows_used = needed < tree->n_rows ? needed : tree->n_rows;
+  L.B = B;
+  L.V = V;
+  L.S = support_size(p, V);
+  L.m = p->m;
+  L.temperature = p->temperature;
+  L.u_probe = u_probe;
+  L.sup_id = tree->sup_id;
+  L.sup_q = tree->sup_q;
+  L.sup_qT = tree->sup_qT;
+  L.sup_z = tree->sup_z;
+  L.sup_zT = tree->sup_zT;
+  L.probe_pos = tree->probe_pos;
+  L.sup_stride = tree->sup_stride;
+  L.status = status;
+  L.num_sms = num_sms_of_current_device();
+  L.ctas_per_sm = 2;
+  if (L.num_sms <= 0) return SPEC_TREE_E_CUDA;
+  return st::launch_select_expand(dtype, L, as_stream(stream)) == cudaSuccess ? SPEC_TREE_OK : SPEC_TREE_E_CUDA;
+}
+
+int spec_tree_rank(const spec_tree_params* p, int B, int V, const spec_tree_t* tree, uint32_t* status,
+                   spec_tree_stream_t stream) {
+  int rc = spec_tree_check_params(p, V);
+  if (rc) return rc;
+  if (B < 0) return SPEC_TREE_E_PARAM;
+  if ((rc = check_tree(p, tree, V, true, true))) return rc;
+  st::RankLaunch L;
+  L.p = *p;
+  L.B = B;
+  L.S = support_size(p, V);
+  const int needed = spec_tree_rows_needed(p);
+  L.rows_avail = needed < tree->n_rows ? needed : tree->n_rows;
+  L.tree = *tree;
+  L.status = status;
+  const cudaError_t err = p->builder == SPEC_TREE_BUILDER_SMART ? st::launch_rank_smart(L, as_stream(stream))
+                                                                 : st::launch_rank_topr(L, as_stream(stream));
+  return err == cudaSuccess ? SPEC_TREE_OK : SPEC_TREE_E_CUDA;
+}
+
+int spec_tree_build(const spec_tree_params* p, int B, int V, int dtype, const void* draft_logits,
+                    int64_t row_stride, const float* u_probe, const spec_tree_t* tree, uint32_t* status,
+                    spec_tree_stream_t stream) {
+  int rc = spec_tree_check_params(p, V);
+  if (rc) return rc;
+  if ((rc = check_tree(p, tree, V, true, true))) return rc;
+  if ((rc = spec_tree_select_expand(p, B, V, dtype, draft_logits, row_stride, u_probe, tree, status, stream)))
+    return rc;
+  return spec_tree_rank(p, B, V, tree, status, stream);
+}
+
+int spec_tree_verify(const spec_tree_params* p, int B, int V, int dtype, const void* target_logits,
+                     int64_t row_stride, const spec_tree_t* tree, const float* u_verify, const float* u_bonus,
+                     int32_t* accept_len, int32_t* out_tok, int32_t* out_node, uint32_t* margins, uint32_t* status,
+                     spec_tree_stream_t stream) {
+  int rc = spec_tree_check_params(p, V);
+  if (rc) return rc;
+  if (B < 0 || u_verify == nullptr || u_bonus == nullptr || accept_len == nullptr || out_tok == nullptr ||
+      out_node == nullptr)
+    return SPEC_TREE_E_PARAM;
+  if ((rc = check_rows(dtype, target_logits, row_stride, V))) return rc;
+  if ((rc = check_tree(p, tree, V, true, true))) return rc;
+  st::VerifyLaunch L;
+  L.p = *p;
+  L.B = B;
+  L.V = V;
+  L.S = support_size(p, V);
+  L.dtype = dtype;
+  L.target = target_logits;
+  L.row_stride = row_stride;
+  L.tree = *tree;
+  L.u_verify = u_verify;
+  L.u_bonus = u_bonus;
+  L.accept_len = accept_len;
+  L.out_tok = out_tok;
+  L.out_node = out_node;
+  L.margins = margins;
+  L.status = status;
+  return st::launch_verify(L, as_stream(stream)) == cudaSuccess ? SPEC_TREE_OK : SPEC_TREE_E_CUDA;
+}
+
+const char* spec_tree_strerror(int code) {
+  switch (code) {
+    case SPEC_TREE_OK:
+      return "ok";
+    case SPEC_TREE_E_PARAM:
+      return "invalid parameter or null pointer";
+    case SPEC_TREE_E_LAYOUT:
+      return "unsupported dtype or rows not 16-byte aligned";
+    case SPEC_TREE_E_CUDA:
+      return "CUDA launch failed";
+    default:
+      return "unknown error";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+// Launch descriptors shared by the host API and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "spec_tree.h"
+
+namespace st {
+
+struct SelLaunch {
+  const void* logits;
+  int64_t row_stride;  // elements
+  int64_t n_rows;      // rows per tree in memory
+  int64_t rows_used;   // rows per tree to process
+  int B, V, S, m;
+  float temperature;
+  const float* u_probe;
+  int32_t* sup_id;
+  float* sup_q;
+  float* sup_qT;
+  float* sup_z;
+  float* sup_zT;
+  int32_t* probe_pos;
+  int sup_stride;
+  uint32_t* status;
+  int num_sms;
+  int ctas_per_sm;
+};
+
+struct RankLaunch {
+  spec_tree_params p;
+  int B, S;
+  int64_t rows_avail;  // rows per tree that were expanded
+  spec_tree_t tree;
+  uint32_t* status;
+};
+
+struct VerifyLaunch {
+  spec_tree_params p;
+  int B, V, S, dtype;
+  const void* target;
+  int64_t row_stride;  // elements
+  spec_tree_t tree;
+  const float* u_verify;
+  const float* u_bonus;
+  int32_t* accept_len;
+  int32_t* out_tok;
+  int32_t* out_node;
+  uint32_t* margins;
+  uint32_t* status;
+};
+
+size_t select_expand_smem_bytes();
+cudaError_t launch_select_expand(int dtype, const SelLaunch& L, cudaStream_t stream);
+cudaError_t launch_rank_topr(const RankLaunch& L, cudaStream_t stream);
+cudaError_t launch_rank_smart(const RankLaunch& L, cudaStream_t stream);
+cudaError_t launch_verify(const VerifyLaunch& L, cudaStream_t stream);
+
+}  // namespace st

@@ -124,22 +124,25 @@ def cast_rows(x: torch.Tensor, dtype: str) -> torch.Tensor:
 
 
 def draft_logits(wl: Workload, seed: int, n_rows: Optional[int] = None, device="cpu",
-                 row_stride: Optional[int] = None):
+                 row_stride: Optional[int] = None, trees: Optional[Sequence[int]] = None):
     """Draft logits [B][n_rows][row_stride] (storage dtype) and latent rows [B][n_rows][V] fp32.
 
-    Padding columns (row_stride > V) are filled with -inf; they are never read
-    by a caller that passes V correctly.
+    Tree b's rows are keyed by (seed, b), so any subset `trees` of the batch
+    can be generated alone (the result then has len(trees) trees).  Padding
+    columns (row_stride > V) are filled with -inf; they are never read by a
+    caller that passes V correctly.
     """
     n_rows = n_rows or wl.n_exp
     stride = row_stride or wl.V
-    lat = torch.empty((wl.B, n_rows, wl.V), dtype=torch.float32, device=device)
-    drf = torch.full((wl.B, n_rows, stride), float("-inf"),
+    ids = list(range(wl.B)) if trees is None else list(trees)
+    lat = torch.empty((len(ids), n_rows, wl.V), dtype=torch.float32, device=device)
+    drf = torch.full((len(ids), n_rows, stride), float("-inf"),
                      dtype=torch.bfloat16 if wl.dtype == "bf16" else torch.float32, device=device)
-    for b in range(wl.B):
-        lat[b] = latent_rows((seed, "tree", b), n_rows, wl.V, wl.zipf_a, wl.noise_sd, device)
+    for i, b in enumerate(ids):
+        lat[i] = latent_rows((seed, "tree", b), n_rows, wl.V, wl.zipf_a, wl.noise_sd, device)
         g = _gen(("draftnoise", seed, b), device)
         noise = torch.randn((n_rows, wl.V), generator=g, device=device) * wl.sigma_draft
-        drf[b, :, :wl.V] = cast_rows(lat[b] + noise, wl.dtype)
+        drf[i, :, :wl.V] = cast_rows(lat[i] + noise, wl.dtype)
     return drf, lat
 
 
@@ -158,25 +161,28 @@ def verify_uniforms(wl: Workload, seed: int, device="cpu"):
 
 
 def target_logits(wl: Workload, seed: int, latent: torch.Tensor, node_exp_row: torch.Tensor,
-                  n_nodes: torch.Tensor, device="cpu", row_stride: Optional[int] = None):
+                  n_nodes=None, device="cpu", row_stride: Optional[int] = None,
+                  trees: Optional[Sequence[int]] = None):
     """Target logits [B][R+1][row_stride] for a built tree.
 
-    node_exp_row[b][i] >= 0 gives the latent slot of an expanded node; other
+    node_exp_row[i][j] >= 0 gives the latent slot of an expanded node; other
     nodes (and unused entries) get a fresh latent row keyed by (tree, node).
+    `trees` names the batch indices of the rows of `latent` / `node_exp_row`.
     """
     stride = row_stride or wl.V
     max_nodes = node_exp_row.shape[1]
-    out = torch.full((wl.B, max_nodes, stride), float("-inf"),
+    ids = list(range(node_exp_row.shape[0])) if trees is None else list(trees)
+    out = torch.full((len(ids), max_nodes, stride), float("-inf"),
                      dtype=torch.bfloat16 if wl.dtype == "bf16" else torch.float32, device=device)
     exp_row = node_exp_row.to("cpu")
-    for b in range(wl.B):
-        fresh = latent_rows((seed, "fresh", b), max_nodes, wl.V, wl.zipf_a, wl.noise_sd, device)
-        rows = fresh.clone()
-        for i in range(max_nodes):
-            e = int(exp_row[b, i])
-            if e >= 0:
-                rows[i] = latent[b, e].to(device)
-        out[b, :, :wl.V] = cast_rows(rows, wl.dtype)
+    for i, b in enumerate(ids):
+        rows = latent_rows((seed, "fresh", b), max_nodes, wl.V, wl.zipf_a, wl.noise_sd, device)
+        sel = [(j, int(exp_row[i, j])) for j in range(max_nodes) if int(exp_row[i, j]) >= 0]
+        if sel:
+            dst = torch.tensor([j for j, _ in sel], device=device)
+            src = torch.tensor([e for _, e in sel], device=latent.device)
+            rows[dst] = latent[i].index_select(0, src).to(device)
+        out[i, :, :wl.V] = cast_rows(rows, wl.dtype)
     return out
 
 

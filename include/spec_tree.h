@@ -1,0 +1,225 @@
+/*
+ * spec_tree.h -- C ABI of the GB300 (sm_103a) hot path of stochastic
+ * dynamic-tree speculative decoding.
+ *
+ * Sources of the operations (papernotes.org pages):
+ *   "RheoSampling: Resolving the One-Hot Dilemma in Stochastic Dynamic-Tree
+ *    Speculative Decoding" (NeurIPS 2026 notes), Method:
+ *     - Key design 1: top-128 truncation of the draft logits before the softmax;
+ *     - Key design 2: dual-identity expansion (top-m deterministic children, one
+ *       probe from the renormalised tail with proxy probability min{q(x_m), z},
+ *       fillers) and the Local Ranking Preservation lemma;
+ *     - overall framework / flowchart: cumulative path scores, global top-R pruning;
+ *     - Key design 3: optimal-transport verification (probe first, residual
+ *       norm(max(0, p - q~)), recursive rejection, bonus token);
+ *     - training-strategy paragraph: build/prune on untempered draft
+ *       probabilities, sample the probe and verify at temperature T.
+ *   "SMART: When is it Actually Worth Expanding a Speculative Tree?" (ECCV 2026
+ *    notes), Method / Key designs 1-3: the marginal keep rule with the cost
+ *    models lambda*|T| + beta and gamma*(exp(delta*|T|^rho) - 1) + eta.
+ *
+ * General contract of every entry point:
+ *   - Pointers named "device" are device pointers owned by the caller; the
+ *     library allocates nothing, keeps no state between calls and never
+ *     synchronises the host.  Every call is asynchronous on `stream`
+ *     (0 = the legacy default stream).
+ *   - Return value: SPEC_TREE_OK (0) or a negative SPEC_TREE_E_* code.
+ *     Argument errors are detected on the host before any launch, so nothing
+ *     has been enqueued when a call returns SPEC_TREE_E_PARAM or
+ *     SPEC_TREE_E_LAYOUT.  SPEC_TREE_E_CUDA reports a failed launch.
+ *   - Anomalies only the device can see (a NaN or +inf logit, an empty
+ *     residual after rounding, a bounded wait that gave up) are OR-ed into the
+ *     caller's device word `status` (SPEC_TREE_S_* bits).  Kernels never trap
+ *     and every wait is bounded.  The caller zeroes `status` when it wants a
+ *     fresh reading.
+ *   - Logit rows are row-major with `row_stride` elements between rows; a
+ *     row starts on a 16-byte boundary (base pointer 16-byte aligned and
+ *     row_stride * element size a multiple of 16), else SPEC_TREE_E_LAYOUT.
+ *     V need not be a multiple of 8.
+ */
+#ifndef SPEC_TREE_H
+#define SPEC_TREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA runtime header. */
+typedef struct CUstream_st* spec_tree_stream_t;
+
+/* element types of logit rows */
+#define SPEC_TREE_BF16 0
+#define SPEC_TREE_F32 1
+
+/* tree builders */
+#define SPEC_TREE_BUILDER_TOPR 0  /* expand-then-rerank, frontier top-W, global top-R */
+#define SPEC_TREE_BUILDER_SMART 1 /* SMART marginal keep rule, budget R */
+
+/* node kinds */
+#define SPEC_TREE_ROOT 0
+#define SPEC_TREE_DET 1
+#define SPEC_TREE_PROBE 2
+#define SPEC_TREE_FILL 3
+
+/* return codes */
+#define SPEC_TREE_OK 0
+#define SPEC_TREE_E_PARAM (-1)  /* bad parameter or null pointer */
+#define SPEC_TREE_E_LAYOUT (-3) /* unsupported dtype or misaligned rows */
+#define SPEC_TREE_E_CUDA (-4)   /* a kernel launch failed */
+
+/* device status bits */
+#define SPEC_TREE_S_NONFINITE_DRAFT 1u   /* NaN or +inf in a draft row read */
+#define SPEC_TREE_S_NONFINITE_TARGET 2u  /* NaN or +inf in a target row read */
+#define SPEC_TREE_S_RESIDUAL_EMPTY 4u    /* residual mass <= 0 after rounding; bonus drawn from p */
+#define SPEC_TREE_S_OVERFLOW 8u          /* internal candidate buffer overflow (not expected) */
+#define SPEC_TREE_S_TIMEOUT 16u          /* a bounded wait on a bulk copy gave up */
+#define SPEC_TREE_S_ROWS 32u             /* a tree wanted more draft rows than n_rows */
+
+/* Limits of this build. */
+#define SPEC_TREE_MAX_SUPPORT 128
+#define SPEC_TREE_MAX_CAND 2048 /* K + (depth-1)*W*K for the top-R builder; K*R for SMART */
+#define SPEC_TREE_MAX_NODES 512 /* R + 1 */
+
+/*
+ * Parameters of the method.
+ *   K        children (slots) per expanded node, 1 <= K <= support.
+ *   m        deterministic children (top-m), 0 <= m < K.
+ *   W        frontier width: nodes expanded per layer (top-R builder).
+ *   depth    D >= 1: layers of draft nodes.
+ *   R        pruned tree size in draft nodes, root excluded (top-R builder);
+ *            node budget (SMART).  Node arrays hold R + 1 entries.
+ *   support  |S| = min(support, V); 0 means 128.  1 <= support <= 128.
+ *   temperature T > 0: probe sampling and verification use q_T and
+ *            p = softmax(t / T); ranking uses untempered q.
+ *   builder  SPEC_TREE_BUILDER_TOPR or SPEC_TREE_BUILDER_SMART.
+ *   lambda, beta, gamma, delta, rho, eta, alpha: SMART cost model (units of
+ *            one target decoding step) and discount; ignored by top-R.
+ */
+typedef struct spec_tree_params {
+  int32_t K, m, W, depth, R, support;
+  float temperature;
+  int32_t builder;
+  float lambda, beta, gamma, delta, rho, eta, alpha;
+} spec_tree_params;
+
+/*
+ * Tree buffers (all device pointers, caller-owned).  B trees; `n_rows` draft
+ * rows and `max_nodes` (= R + 1) node entries per tree.
+ *
+ * Node arrays [B][max_nodes], canonical order: node 0 is the root, then depth
+ * ascending, then ranking key (score descending, creation index ascending).
+ * Entries at index >= n_nodes[b] hold token/parent/exp_row = -1, score 0.
+ *   node_token   token id (root: -1)
+ *   node_parent  index of the parent node (root: -1)
+ *   node_depth   0 for the root
+ *   node_kind    SPEC_TREE_ROOT/DET/PROBE/FILL
+ *   node_slot    sibling slot (DET 0..m-1, PROBE m, FILL after; root -1)
+ *   node_exp_row draft row the node was expanded from, -1 if not expanded
+ *   node_score   cumulative path score (the probe contributes its proxy)
+ *   n_nodes      [B] node count including the root
+ * Support arrays, per draft row [B][n_rows] (support ranks 0..|S|-1):
+ *   sup_id [.][S] token ids by (logit desc, id asc); sup_q / sup_qT [.][S]
+ *   untempered / tempered truncated softmax; sup_z / sup_zT tail masses over
+ *   ranks m..|S|-1; probe_pos rank of the probe in S (-1: no probe).
+ *   `sup_stride` is the per-row capacity of sup_id/sup_q/sup_qT (>= |S|).
+ */
+typedef struct spec_tree_t {
+  int32_t* node_token;
+  int32_t* node_parent;
+  int32_t* node_depth;
+  int32_t* node_kind;
+  int32_t* node_slot;
+  int32_t* node_exp_row;
+  float* node_score;
+  int32_t* n_nodes;
+  int32_t* sup_id;
+  float* sup_q;
+  float* sup_qT;
+  float* sup_z;
+  float* sup_zT;
+  int32_t* probe_pos;
+  int32_t n_rows;
+  int32_t max_nodes;
+  int32_t sup_stride;
+} spec_tree_t;
+
+/* Draft rows one tree consumes: 1 + (depth-1)*W (top-R), at most R + 1 (SMART). */
+int spec_tree_rows_needed(const spec_tree_params* p);
+
+/* Host-only check of the parameters against vocabulary size V (no CUDA call). */
+int spec_tree_check_params(const spec_tree_params* p, int V);
+
+/*
+ * Support selection and dual-identity expansion of every draft row
+ * (RheoSampling Key designs 1-2).  For each tree b and row e < rows, where
+ * rows = min(tree->n_rows, spec_tree_rows_needed(p)):
+ *   S = top-|S| token ids of draft row (b, e) by (logit desc, id asc);
+ *   q, q_T = softmax over S of l and of l / T (untempered / tempered);
+ *   z, z_T = their sums over ranks m..|S|-1 (the tail);
+ *   probe = first tail rank k, in rank order, with
+ *           u_probe[b][e] * z_T < sum_{j=m..k} q_T(j)   (none if z_T == 0).
+ * draft_logits: device [B][tree->n_rows][row_stride] of dtype (bf16 or f32).
+ * u_probe:      device [B][tree->n_rows] float, U[0,1).
+ * Writes the sup_* arrays and probe_pos of `tree`.
+ */
+int spec_tree_select_expand(const spec_tree_params* p, int B, int V, int dtype,
+                            const void* draft_logits, int64_t row_stride,
+                            const float* u_probe, const spec_tree_t* tree,
+                            uint32_t* status, spec_tree_stream_t stream);
+
+/*
+ * Tree building from the expanded rows (RheoSampling overall framework:
+ * path scores, frontier top-W per layer, global top-R; or SMART Key design 3
+ * keep rule).  Reads the sup_* arrays written by spec_tree_select_expand and
+ * writes the node arrays and n_nodes.  Child scores are fl(parent x q) in
+ * float32 (parent x proxy for the probe); the ranking key never involves a
+ * token id, so a probe's survival does not depend on its identity.
+ */
+int spec_tree_rank(const spec_tree_params* p, int B, int V, const spec_tree_t* tree,
+                   uint32_t* status, spec_tree_stream_t stream);
+
+/* spec_tree_select_expand followed by spec_tree_rank on the same stream. */
+int spec_tree_build(const spec_tree_params* p, int B, int V, int dtype,
+                    const void* draft_logits, int64_t row_stride,
+                    const float* u_probe, const spec_tree_t* tree,
+                    uint32_t* status, spec_tree_stream_t stream);
+
+/*
+ * Layer-by-layer verification of built trees (RheoSampling Key design 3).
+ * For each tree, from the root: p = softmax(t / T) over the full vocabulary
+ * of the current node's target row; the node's children are tested probe
+ * first (accept iff u < p(x_s) / q~_T(x_s)), then, under the residual
+ * w = max(0, p - q~_T) on the tail (w = p elsewhere, mass
+ * Zr = 1 - sum_tail min(p, q~_T)), each remaining child x in slot order
+ * (accept iff u < w(x) / Zr, else Zr -= w(x), w(x) = 0).  Without a probe
+ * child, w = p and Zr = 1.  The j-th decision at level l uses
+ * u_verify[b][l][j].  An accepted child becomes the node; when every child
+ * is rejected or the node has none, the bonus token is the first token in id
+ * order with u_bonus[b] * Zr < sum_{v' <= v} w(v').
+ *   target_logits: device [B][tree->max_nodes][row_stride]; row i is the
+ *                  target logits at node i.  Only rows on the accepted path
+ *                  are read.
+ *   u_verify: device [B][depth][K] float; u_bonus: device [B] float.
+ *   accept_len: device [B]; out_tok, out_node: device [B][depth + 1]
+ *   (accepted tokens then the bonus token; accepted node indices then -1;
+ *   unused entries -1).
+ *   margins: device uint32[2] or NULL; counts decisions whose float32 margin
+ *   is below 1e-6 in probability mass ([0] accept tests, [1] bonus draws).
+ */
+int spec_tree_verify(const spec_tree_params* p, int B, int V, int dtype,
+                     const void* target_logits, int64_t row_stride,
+                     const spec_tree_t* tree, const float* u_verify, const float* u_bonus,
+                     int32_t* accept_len, int32_t* out_tok, int32_t* out_node,
+                     uint32_t* margins, uint32_t* status, spec_tree_stream_t stream);
+
+/* Message for a return code (static string). */
+const char* spec_tree_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_TREE_H */

@@ -8,6 +8,19 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def _ensure_library():
+    """Build libspec_tree.so when it is missing or older than its sources (nvcc is needed)."""
+    from dynamic_tree_speculative_gb300 import build
+    srcs = [os.path.join(build.CSRC, f) for f in os.listdir(build.CSRC)]
+    srcs.append(os.path.join(build.INCLUDE, "spec_tree.h"))
+    if not os.path.exists(build.LIB) or max(os.path.getmtime(f) for f in srcs) > os.path.getmtime(build.LIB):
+        build.build()
+
+
+def pytest_sessionstart(session):
+    _ensure_library()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running CPU test")

@@ -1,0 +1,86 @@
+"""C-ABI library: loads, exports every declared symbol, host-side checks (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def binding():
+    from dynamic_tree_speculative_gb300 import binding as B
+    return B
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "spec_tree.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(spec_tree_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(binding):
+    names = _declared_functions()
+    assert len(names) >= 7
+    lib = ctypes.CDLL(binding.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(binding.EXPORTS) <= set(names)
+
+
+def test_rows_needed(binding):
+    P = binding.Params
+    assert binding.rows_needed(P(K=8, m=1, W=8, depth=8, R=60)) == 57
+    assert binding.rows_needed(P(K=6, m=1, W=6, depth=6, R=32)) == 31
+    assert binding.rows_needed(P(K=8, m=1, W=8, depth=8, R=60, builder=binding.BUILDER_SMART)) == 61
+
+
+@pytest.mark.parametrize("kw,V,ok", [
+    (dict(K=8, m=1, W=8, depth=8, R=60), 128256, True),
+    (dict(K=8, m=8, W=8, depth=8, R=60), 128256, False),    # m >= K
+    (dict(K=8, m=1, W=8, depth=8, R=60), 5, False),         # K > |S| = V
+    (dict(K=4, m=1, W=4, depth=3, R=8), 32, True),
+    (dict(K=8, m=1, W=8, depth=0, R=60), 1000, False),      # depth < 1
+    (dict(K=8, m=1, W=8, depth=8, R=0), 1000, False),       # R < 1
+    (dict(K=8, m=1, W=8, depth=8, R=60, temperature=0.0), 1000, False),
+    (dict(K=8, m=1, W=8, depth=8, R=60, support=129), 1000, False),
+    (dict(K=16, m=1, W=16, depth=9, R=60), 1000, False),    # candidates > 2048
+    (dict(K=8, m=1, W=8, depth=8, R=600), 1000, False),     # R + 1 > 512
+    (dict(K=2, m=0, W=1, depth=1, R=1), 2, True),
+])
+def test_param_checks(binding, kw, V, ok):
+    rc = binding.spec_tree_check_params(binding.Params(**kw), V)
+    assert (rc == binding.OK) == ok
+
+
+def test_bad_arguments_fail_before_any_launch(binding):
+    """Host checks return codes without touching CUDA (works with no GPU)."""
+    lib = binding._lib
+    p = binding.Params(K=8, m=1, W=8, depth=8, R=60).c()
+    t = binding.c_tree()
+    # null tree
+    assert lib.spec_tree_build(ctypes.byref(p), 1, 1000, binding.BF16, ctypes.c_void_p(16), 1000,
+                               ctypes.c_void_p(16), None, None, None) == binding.E_PARAM
+    # misaligned rows: row_stride * 2 bytes not a multiple of 16
+    for name, _ in binding.c_tree._fields_[:14]:
+        setattr(t, name, 256)
+    t.n_rows, t.max_nodes, t.sup_stride = 57, 61, 128
+    assert lib.spec_tree_select_expand(ctypes.byref(p), 1, 1001, binding.BF16, ctypes.c_void_p(256), 1001,
+                                       ctypes.c_void_p(256), ctypes.byref(t), None, None) == binding.E_LAYOUT
+    # unaligned base pointer
+    assert lib.spec_tree_select_expand(ctypes.byref(p), 1, 1000, binding.BF16, ctypes.c_void_p(258), 1008,
+                                       ctypes.c_void_p(256), ctypes.byref(t), None, None) == binding.E_LAYOUT
+    # unknown dtype
+    assert lib.spec_tree_select_expand(ctypes.byref(p), 1, 1000, 7, ctypes.c_void_p(256), 1008,
+                                       ctypes.c_void_p(256), ctypes.byref(t), None, None) == binding.E_LAYOUT
+    # too few rows per tree
+    t.n_rows = 56
+    assert lib.spec_tree_select_expand(ctypes.byref(p), 1, 1000, binding.BF16, ctypes.c_void_p(256), 1008,
+                                       ctypes.c_void_p(256), ctypes.byref(t), None, None) == binding.E_PARAM
+    # verify: null outputs
+    t.n_rows = 57
+    assert lib.spec_tree_verify(ctypes.byref(p), 1, 1000, binding.BF16, ctypes.c_void_p(256), 1008,
+                                ctypes.byref(t), ctypes.c_void_p(256), ctypes.c_void_p(256), None, None, None,
+                                None, None, None) == binding.E_PARAM
+    assert binding._lib.spec_tree_strerror(binding.E_LAYOUT).startswith(b"unsupported")

@@ -1,0 +1,185 @@
+"""CUDA path vs the CPU oracle, element by element, on seeded synthetic inputs.
+
+Every call goes through the C ABI (libspec_tree.so) via the ctypes binding.
+"""
+import numpy as np
+import pytest
+import torch
+
+from dynamic_tree_speculative_gb300 import workloads as WL
+
+pytestmark = pytest.mark.gpu
+
+import parity  # noqa: E402  (loads the native library; fails loudly if absent)
+
+
+def _report(name, out):
+    print(f"{name}: build exact {out['build_exact']} exempt {out['build_exempt']}; "
+          f"verify exact {out.get('verify_exact')} exempt {out.get('verify_exempt')}")
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_parity(seed):
+    wl = WL.WORKLOADS["tiny"].with_(B=256)
+    out = parity.run_parity(wl, seed)
+    _report("tiny", out)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_vicuna_parity(seed):
+    wl = WL.WORKLOADS["vicuna"].with_(B=4)
+    _report("vicuna", parity.run_parity(wl, seed))
+
+
+def test_llama3_parity():
+    """LLaMA-3-vocab workload at its own batch (8 trees, V = 128256), every tree."""
+    wl = WL.WORKLOADS["llama3"]
+    _report("llama3", parity.run_parity(wl, 3))
+
+
+def test_rl_large_batch_sampled():
+    """RL-rollout workload at full size (64 trees, V = 151936, T = 0.7); oracle on sampled trees."""
+    wl = WL.WORKLOADS["rl"]
+    _report("rl", parity.run_parity(wl, 4, sample=[0, 17, 40, 63]))
+
+
+def test_bench_workload_sampled():
+    """The timed workload (LLaMA-3 vocab, 64 trees) in the bench's launch configuration."""
+    wl = WL.BENCH_WORKLOAD
+    _report("bench", parity.run_parity(wl, 5, sample=[0, 31, 63]))
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_smart_parity(seed):
+    wl = WL.WORKLOADS["sweep_smart"].with_(B=6, V=32000)
+    _report("smart", parity.run_parity(wl, seed))
+
+
+def test_smart_parity_llama_vocab():
+    wl = WL.WORKLOADS["sweep_smart"].with_(B=4)
+    _report("smart128k", parity.run_parity(wl, 9))
+
+
+EDGE = {
+    "support_is_V": dict(V=100, K=8, m=1, W=4, depth=4, R=12),
+    "ragged_V": dict(V=1001, K=8, m=1, W=4, depth=4, R=20, stride=1008),
+    "tiny_V_no_vector": dict(V=5, K=2, m=1, W=2, depth=3, R=6, stride=8),
+    "f32_ragged": dict(V=4099, K=6, m=1, W=3, depth=3, R=10, dtype="f32", stride=4100),
+    "m0": dict(V=3000, K=4, m=0, W=4, depth=4, R=16),
+    "m2": dict(V=3000, K=6, m=2, W=3, depth=4, R=16),
+    "m3": dict(V=3000, K=6, m=3, W=3, depth=4, R=16),
+    "cold": dict(V=3000, K=6, m=1, W=3, depth=4, R=16, temperature=0.5),
+    "hot": dict(V=3000, K=6, m=1, W=3, depth=4, R=16, temperature=1.7),
+    "R1": dict(V=3000, K=4, m=1, W=2, depth=3, R=1),
+    "R_over_all": dict(V=3000, K=4, m=1, W=3, depth=4, R=200),
+    "depth1": dict(V=3000, K=8, m=1, W=8, depth=1, R=8),
+    "support_32": dict(V=3000, K=4, m=1, W=3, depth=3, R=10, support=32),
+    "wide": dict(V=9000, K=16, m=1, W=16, depth=3, R=100),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EDGE))
+def test_edge_cases(name):
+    kw = dict(EDGE[name])
+    stride = kw.pop("stride", None)
+    base = WL.WORKLOADS["vicuna"].with_(B=16)
+    wl = base.with_(**kw)
+    _report(name, parity.run_parity(wl, 11, row_stride=stride))
+
+
+def _parity_on_draft(wl, draft, seed=0):
+    case = parity.make_case(wl, seed)
+    case.draft = draft
+    case.latent = draft.float()
+    trees = parity.oracle_build(case, range(wl.B))
+    g = parity.run_gpu(case, None)
+    return parity.compare_build(g, trees, min(wl.support, wl.V))
+
+
+def test_heavy_ties_and_constant_rows():
+    """Integer-valued bf16 logits (massive ties) and a constant row: ids break ties ascending."""
+    wl = WL.WORKLOADS["vicuna"].with_(B=4, V=20000, depth=3, R=12, K=6, W=3)
+    n_rows = 1 + (wl.depth - 1) * wl.W
+    g = torch.Generator().manual_seed(5)
+    draft = torch.randint(-6, 3, (wl.B, n_rows, wl.V), generator=g).to(torch.bfloat16)
+    draft[1] = 0.25
+    draft[2, :, 5000:] = -3.0  # a long constant tail
+    ex, exm = _parity_on_draft(wl, draft)
+    assert ex + exm == wl.B
+
+
+def test_nan_row_sets_status_and_stays_in_bounds():
+    from dynamic_tree_speculative_gb300 import binding as B
+    wl = WL.WORKLOADS["vicuna"].with_(B=2, V=5000, depth=3, R=10, K=4, W=2)
+    case = parity.make_case(wl, 0)
+    case.draft[0, 1, 777] = float("nan")
+    g = parity.run_gpu(case, None)
+    assert g["status"] & B.S_NONFINITE_DRAFT
+    # the other tree is untouched by the bad row
+    trees = parity.oracle_build(case, [1])
+    assert parity.compare_build(g, trees, min(wl.support, wl.V))[0] == 1
+
+
+def test_probe_survival_independent_of_identity_gpu():
+    """Sweeping the root's probe uniform never moves the probe node (only tokens change)."""
+    wl = WL.WORKLOADS["vicuna"].with_(B=32, V=4000, depth=4, R=14, K=4, W=3)
+    case = parity.make_case(wl, 21)
+    case.u_probe[:, 0] = torch.linspace(0.0, 0.999, wl.B)
+    case.draft[:] = case.draft[0:1]          # same rows in every tree
+    case.u_probe[:, 1:] = case.u_probe[0:1, 1:]
+    g = parity.run_gpu(case, None)
+    sig = set()
+    for b in range(wl.B):
+        kinds = g["node_kind"][b]
+        parents = g["node_parent"][b]
+        probe_nodes = [i for i in range(len(kinds)) if kinds[i] == 2 and parents[i] == 0]
+        sig.add(tuple(probe_nodes))
+    assert len(sig) == 1, sig
+
+
+def test_gpu_losslessness_chi_square():
+    """Tiny workload on the GPU path, path-keyed targets: first emitted token ~ p(root)."""
+    from scipy.stats import chi2
+    from dynamic_tree_speculative_gb300 import binding as B
+    wl = WL.WORKLOADS["tiny"].with_(B=10000)
+    params = B.Params.from_workload(wl)
+    n_rows = B.rows_needed(params)
+    base, _ = WL.draft_logits(wl.with_(B=1), 77, n_rows=n_rows)
+    draft = base.expand(wl.B, -1, -1).contiguous()
+    u_probe = WL.uniforms(77, "p", (wl.B, n_rows))
+    uv, ub = WL.uniforms(77, "v", (wl.B, wl.depth, wl.K)), WL.uniforms(77, "b", (wl.B,))
+    dev = "cuda"
+    tree = B.TreeBuffers(params, wl.B, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    B.spec_tree_build(params, wl.V, draft.to(dev), u_probe.to(dev), tree, status)
+    tok = tree.node_token.cpu().numpy()
+    par = tree.node_parent.cpu().numpy()
+    nn = tree.n_nodes.cpu().numpy()
+    cache = {}
+    rows = torch.empty((wl.B, wl.R + 1, wl.V), dtype=torch.float32)
+    for b in range(wl.B):
+        for i in range(wl.R + 1):
+            path, j = [], i
+            while j > 0:
+                path.append(int(tok[b, j]))
+                j = par[b, j]
+            key = tuple(reversed(path)) if i < nn[b] else ("unused",)
+            if key not in cache:
+                cache[key] = WL.path_keyed_rows(123, [key if key != ("unused",) else (-7,)], wl.V, 1.2, 0.5)[0]
+            rows[b, i] = cache[key]
+    out = B.VerifyOutputs(params, wl.B, device=dev)
+    B.spec_tree_verify(params, wl.V, rows.to(dev), tree, uv.to(dev), ub.to(dev), out.accept_len, out.out_tok,
+                       out.out_node, out.margins, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    first = out.out_tok[:, 0].cpu().numpy()
+    p = torch.softmax(cache[()].double(), 0).numpy()
+    counts = np.bincount(first, minlength=wl.V)
+    exp = p * wl.B
+    keep = exp >= 5
+    stat = ((counts[keep] - exp[keep]) ** 2 / exp[keep]).sum()
+    rest_o, rest_e = counts[~keep].sum(), exp[~keep].sum()
+    if rest_e > 0:
+        stat += (rest_o - rest_e) ** 2 / rest_e
+    dof = keep.sum() + (1 if rest_e > 0 else 0) - 1
+    assert chi2.sf(stat, dof) > 1e-3
