@@ -33,6 +33,10 @@ struct RankShared {
   int32_t aux[SPEC_TREE_MAX_CAND];     // top-R: selected flag; SMART: layer order
   int32_t front[SPEC_TREE_MAX_NODES];  // current frontier / active list (candidate indices)
   int32_t front_next[SPEC_TREE_MAX_NODES];
+  // children of every expanded row, precomputed: entry row * K + slot
+  float ch_lp[SPEC_TREE_MAX_CAND];
+  int32_t ch_tok[SPEC_TREE_MAX_CAND];
+  int32_t ch_kind[SPEC_TREE_MAX_CAND];
   int nc;
   int nf;
   int n_kept;
@@ -72,26 +76,38 @@ __device__ __forceinline__ float child_of(const spec_tree_t& t, int64_t row, int
   return q[rank];
 }
 
-// Generate the K children of every node in s.front[0..nf) at `depth`,
-// appending candidates at s.nc.  Parent scores come from s.score (root: 1).
-__device__ void gen_layer(RankShared& s, const RankLaunch& L, int b, int depth, int nf, int base) {
+// Children of the first `rows` expanded rows of tree b into shared memory
+// (one parallel pass over global memory; the layer loop then reads smem only).
+__device__ void load_children(RankShared& s, const RankLaunch& L, int b, int rows) {
   const int K = L.p.K, m = L.p.m;
   const spec_tree_t& t = L.tree;
+  for (int idx = threadIdx.x; idx < rows * K; idx += RANK_THREADS) {
+    const int r = idx / K, slot = idx - r * K;
+    const int64_t row = static_cast<int64_t>(b) * t.n_rows + r;
+    int kind, rank;
+    s.ch_lp[idx] = child_of(t, row, m, slot, kind, rank);
+    s.ch_kind[idx] = kind;
+    s.ch_tok[idx] = t.sup_id[row * t.sup_stride + rank];
+  }
+}
+
+// Generate the K children of every node in s.front[0..nf) at `depth`,
+// appending candidates at `base`.  Parent scores come from s.score (root: 1).
+__device__ void gen_layer(RankShared& s, const RankLaunch& L, int depth, int nf, int base) {
+  const int K = L.p.K;
   for (int idx = threadIdx.x; idx < nf * K; idx += RANK_THREADS) {
     const int f = idx / K, slot = idx - f * K;
     const int pc = s.front[f];
     const int prow = pc < 0 ? 0 : s.exp_row[pc];
     const float pscore = pc < 0 ? 1.0f : s.score[pc];
-    const int64_t row = static_cast<int64_t>(b) * t.n_rows + prow;
-    int kind, rank;
-    const float lp = child_of(t, row, m, slot, kind, rank);
-    const float sc = pscore * lp;
+    const int ci = prow * K + slot;
+    const float sc = pscore * s.ch_lp[ci];
     const int c = base + idx;
     s.score[c] = sc;
     s.key[c] = rank_key(sc, depth, f, slot);
-    s.token[c] = t.sup_id[row * t.sup_stride + rank];
+    s.token[c] = s.ch_tok[ci];
     s.parent[c] = pc;
-    s.meta[c] = (depth << 16) | (kind << 12) | slot;
+    s.meta[c] = (depth << 16) | (s.ch_kind[ci] << 12) | slot;
     s.exp_row[c] = -1;
     s.pos[c] = -1;
   }
@@ -131,6 +147,7 @@ __global__ void __launch_bounds__(RANK_THREADS) rank_topr_kernel(RankLaunch L) {
   RankShared& s = *reinterpret_cast<RankShared*>(smem_raw);
   const int b = blockIdx.x, tid = threadIdx.x;
   const int K = L.p.K, W = L.p.W, D = L.p.depth, R = L.p.R;
+  load_children(s, L, b, static_cast<int>(L.rows_avail));
   if (tid == 0) {
     s.front[0] = -1;
     s.nf = 1;
@@ -139,7 +156,7 @@ __global__ void __launch_bounds__(RANK_THREADS) rank_topr_kernel(RankLaunch L) {
   __syncthreads();
   for (int d = 1; d <= D; ++d) {
     const int nf = s.nf, base = s.nc, ln = nf * K;
-    gen_layer(s, L, b, d, nf, base);
+    gen_layer(s, L, d, nf, base);
     __syncthreads();
     if (d < D) {
       // frontier of layer d: its top-W candidates, expanded from rows 1 + (d-1)*W + rank
@@ -210,6 +227,7 @@ __global__ void __launch_bounds__(RANK_THREADS) rank_smart_kernel(RankLaunch L) 
   const int K = L.p.K, D = L.p.depth, budget = L.p.R;
   // per-candidate scratch reused: exp_row doubles as "has a kept child" flag
   // for kept nodes via the high bit of meta (bit 30).
+  load_children(s, L, b, static_cast<int>(L.rows_avail));
   if (tid == 0) {
     s.front[0] = -1;
     s.nf = 1;
@@ -229,7 +247,7 @@ __global__ void __launch_bounds__(RANK_THREADS) rank_smart_kernel(RankLaunch L) 
       if (tid == 0) set_status(L.status, SPEC_TREE_S_ROWS);
       break;
     }
-    gen_layer(s, L, b, d, nf, base);
+    gen_layer(s, L, d, nf, base);
     __syncthreads();
     // order of the layer by key: aux[r] = candidate of rank r
     for (int i = tid; i < ln; i += RANK_THREADS) {

@@ -4,19 +4,30 @@
 // logits) and Key design 2 (top-m deterministic children, probe sampled from
 // the renormalised tempered tail, tail masses).
 //
-// One persistent CTA streams whole rows through a ring of shared-memory stages
-// filled by the TMA engine (cp.async.bulk, completion on mbarriers).  While a
-// row streams, a rising threshold keeps only elements that can still be in the
-// row's top-|S|: every 16-byte vector is first tested with three bf16x2 max
-// instructions against the threshold, and only vectors that pass are split
-// into elements and appended (warp-aggregated) to a candidate buffer.  When
-// the buffer grows past SEL_HIGH, an exact radix select over 64-bit
-// (order key, ~token id) composites cuts it back to the exact top-|S| of
-// everything seen so far, and the threshold becomes the key of its last
-// element (strict from then on: a later element with an equal key has a larger
-// id and loses the tie).  At the row end the same select gives the exact
-// support, which warp 0 turns into q, q_T, z, z_T and the probe while the next
-// row's chunks are already landing.
+// A persistent CTA owns rows; one producer warp streams every row twice
+// through a ring of shared-memory stages filled by the TMA engine
+// (cp.async.bulk, "full" mbarriers with transaction counts, "empty" mbarriers
+// released by the consumer warps), so the consumers never wait on a CTA-wide
+// barrier per chunk and the next row is already landing while a row's
+// selection runs.
+//
+//   pass 1 (HBM, kept in L2 with an evict-last hint): every consumer thread
+//     folds its elements into a running maximum (four bf16x2 max per 16-byte
+//     vector).  Thread maxima are distinct elements of the row, so if warp w's
+//     j-th largest thread maximum is b_w, with j * (consumer warps) >= |S|,
+//     then min_w b_w is a lower bound of the |S|-th largest logit.
+//   pass 2 (L2, evict-first): a vector's maximum is tested against the bound
+//     with packed bf16x2 compares; only vectors that reach it build an element
+//     mask (four more packed compares) and append their elements, with one
+//     shared atomic per lane, to a candidate buffer of 64-bit
+//     (order key, ~token id) composites -- typically ~250 per 128K-token row.
+//   select: an exact radix select over the composites gives the top-|S| by
+//     (logit desc, id asc); a rank count sorts them; warps 0..3 turn them into
+//     q, q_T, z, z_T and the probe (one support rank per thread).
+//
+// Rows whose candidates overflow the buffer (massive ties at the bound) are
+// redone by a robust path that streams the row from global memory in id
+// order, keeping the exact top-|S| of the prefix seen and a strict threshold.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -26,31 +37,46 @@
 
 namespace st {
 
-constexpr int SEL_THREADS = 512;
-constexpr int SEL_WARPS = SEL_THREADS / 32;
-constexpr int SEL_CHUNK = SEL_THREADS * 16;  // bytes per stage: one 16-byte vector per thread
-constexpr int SEL_STAGES = 6;
-constexpr int SEL_HIGH = 1024;               // select when the buffer holds more than this
-constexpr int SEL_CAP = SEL_HIGH + SEL_CHUNK / 2;  // + one chunk of bf16 elements
+constexpr int SX_CONS = 256;                     // consumer threads (8 warps)
+constexpr int SX_CWARPS = SX_CONS / 32;
+constexpr int SX_THREADS = SX_CONS + 32;         // + one producer warp
+constexpr int SX_VPT = 4;                        // 16-byte vectors per consumer thread per stage
+constexpr int SX_CHUNK = SX_CONS * 16 * SX_VPT;  // 16 KB per stage
+constexpr int SX_STAGES = 4;
+constexpr int SX_CAP = 4096;                     // candidate buffer (64-bit composites)
+constexpr int SX_FB_STEP = SX_CONS * 8;          // robust path: at most this many appends per step
+constexpr int SX_FB_HIGH = SX_CAP - SX_FB_STEP;
 
 struct SelShared {
-  alignas(128) uint8_t ring[SEL_STAGES][SEL_CHUNK];
-  uint64_t cand[SEL_CAP];
+  alignas(128) uint8_t ring[SX_STAGES][SX_CHUNK];
+  uint64_t cand[SX_CAP];
   uint64_t sel[SPEC_TREE_MAX_SUPPORT];
-  uint64_t full[SEL_STAGES];
+  uint64_t full[SX_STAGES];
+  uint64_t empty[SX_STAGES];
   uint32_t hist[256];
-  uint32_t warp_min[SEL_WARPS];
+  uint32_t warp_bound[SX_CWARPS];
   int count;
   int sel_count;
-  uint32_t thr_key;
-  int strict;
   int radix_bin;
   int radix_above;
   int radix_cnt;
+  uint32_t thr_key;
+  int strict;
   int timeout;
+  float epi_red[4][4];  // per-warp sums of the epilogue (warps 0..3)
+  float epi_scan[4];
+  int probe_first;
+  int probe_last;
 };
 
 size_t select_expand_smem_bytes() { return sizeof(SelShared); }
+
+// Barrier over the consumer warps only (the producer warp never joins).
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(SX_CONS) : "memory"); }
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 
 template <typename T>
 struct Elem;
@@ -67,7 +93,7 @@ struct Elem<float> {
   static constexpr int ES = 4;
 };
 
-// key of element j of a 16-byte vector, and whether it is NaN or +inf
+// Order key of element j of a 16-byte vector; flags NaN / +inf.
 template <typename T>
 __device__ __forceinline__ uint32_t elem_key(const uint4& v, int j, bool& nonfinite);
 
@@ -86,32 +112,71 @@ __device__ __forceinline__ uint32_t elem_key<float>(const uint4& v, int j, bool&
   return f32_key(bits);
 }
 
-// Upper bound of the keys in a vector; NaN maps to the largest key so that
-// a vector holding one always takes the element path (which reports it).
 template <typename T>
-__device__ __forceinline__ uint32_t vec_max_key(const uint4& v);
-
-template <>
-__device__ __forceinline__ uint32_t vec_max_key<__nv_bfloat16>(const uint4& v) {
-  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
-  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
-  const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
-  const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&v.w);
-  const __nv_bfloat162 mx = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
-  const __nv_bfloat16 h = __hmax_nan(mx.x, mx.y);
-  const uint32_t bits = __bfloat16_as_ushort(h);
-  if ((bits & 0x7fffu) > 0x7f80u) return 0xffffu;
-  return bf16_key(bits);
+__device__ __forceinline__ uint32_t scalar_key(const uint8_t* row, int v, bool& nonfinite) {
+  uint4 x = make_uint4(0, 0, 0, 0);
+  if (sizeof(T) == 2) x.x = reinterpret_cast<const uint16_t*>(row)[v];
+  else x.x = reinterpret_cast<const uint32_t*>(row)[v];
+  return elem_key<T>(x, 0, nonfinite);
 }
 
+// Running maximum of pass 1, as an order key (0 when the thread saw nothing).
+// bf16: packed bf16x2 max that propagates NaN (a thread that saw NaN reports
+// key 0, which only lowers the bound, and the row is flagged).  f32: keys.
+template <typename T>
+struct RunMax;
+
 template <>
-__device__ __forceinline__ uint32_t vec_max_key<float>(const uint4& v) {
-  uint32_t k = 0;
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+struct RunMax<__nv_bfloat16> {
+  __nv_bfloat162 m;
+  uint32_t extra;  // key of elements folded in one at a time
+  bool any;
+  __device__ void init() {
+    m = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+    extra = 0u;
+    any = false;
+  }
+  __device__ void add(const uint4& v) {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
+    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
+    const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&v.w);
+    m = __hmax2_nan(m, __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d)));
+    any = true;
+  }
+  __device__ void add_key(uint32_t key) {
+    extra = max(extra, key);
+    any = true;
+  }
+  __device__ uint32_t key(bool& nonfinite) const {
+    if (!any) return 0u;
+    const uint32_t lo = __bfloat16_as_ushort(m.x), hi = __bfloat16_as_ushort(m.y);
+    if (((lo & 0x7fffu) > 0x7f80u) || ((hi & 0x7fffu) > 0x7f80u)) {
+      nonfinite = true;
+      return 0u;
+    }
+    return max(extra, max(bf16_key(lo), bf16_key(hi)));
+  }
+};
+
+template <>
+struct RunMax<float> {
+  uint32_t k;
+  bool nf;
+  __device__ void init() {
+    k = 0u;
+    nf = false;
+  }
+  __device__ void add(const uint4& v) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) k = max(k, f32_is_nan(w[j]) ? 0xffffffffu : f32_key(w[j]));
-  return k;
-}
+    for (int j = 0; j < 4; ++j) k = max(k, elem_key<float>(v, j, nf));
+  }
+  __device__ void add_key(uint32_t key) { k = max(k, key); }
+  __device__ uint32_t key(bool& nonfinite) const {
+    if (nf) nonfinite = true;
+    return k;
+  }
+};
 
 template <typename T>
 __device__ __forceinline__ float key_value(uint32_t key);
@@ -124,8 +189,8 @@ __device__ __forceinline__ uint64_t make_comp(uint32_t key, uint32_t id) {
   return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~id);
 }
 
-// Warp-aggregated append of up to VEC accepted elements per lane.
-// `mask` bit j set: element j (key keys[j], id id0 + j) is appended.
+// Warp-aggregated append of the elements selected by `mask` (bit j: key
+// keys[j], id id0 + j).  All 32 lanes of the warp call it.
 template <int VEC>
 __device__ __forceinline__ void append_warp(SelShared& s, uint32_t mask, const uint32_t* keys, uint32_t id0,
                                             bool& overflow) {
@@ -146,38 +211,108 @@ __device__ __forceinline__ void append_warp(SelShared& s, uint32_t mask, const u
 #pragma unroll
   for (int j = 0; j < VEC; ++j) {
     if (mask & (1u << j)) {
-      if (pos < SEL_CAP) s.cand[pos] = make_comp(keys[j], id0 + j);
+      if (pos < SX_CAP) s.cand[pos] = make_comp(keys[j], id0 + j);
       else overflow = true;
       ++pos;
     }
   }
 }
 
-// Exact top-k of s.cand[0..n) (distinct composites), sorted descending into
-// s.cand[0..min(n,k)).  Sets count, and the strict threshold when n >= k.
-// Called by all threads of the CTA.
+// Pass-2 filter of one 16-byte vector: append every element whose key is at
+// least `bound` (per-lane shared atomics; only lanes with hits do any work).
+// bf16: packed bf16x2 compares against the bound's value, which order exactly
+// like the keys for every non-NaN element (NaN compares false and sorts last).
+template <typename T>
+struct Filter;
+
+template <>
+struct Filter<__nv_bfloat16> {
+  __nv_bfloat162 b2;
+  __device__ void init(uint32_t bound) {
+    const __nv_bfloat16 bv = __float2bfloat16_rn(bf16_key_value(bound));
+    b2 = __halves2bfloat162(bv, bv);
+  }
+  __device__ __forceinline__ void run(SelShared& s, const uint4& v, uint32_t id0, bool& overflow) const {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
+    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
+    const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&v.w);
+    __nv_bfloat162 mx = __hmax2(__hmax2(a, b), __hmax2(c, d));
+    mx = __hmax2(mx, __lowhigh2highlow(mx));
+    if (!__hbge2(mx, b2)) return;
+    const uint32_t m0 = __hge2_mask(a, b2), m1 = __hge2_mask(b, b2);
+    const uint32_t m2 = __hge2_mask(c, b2), m3 = __hge2_mask(d, b2);
+    const uint32_t mask = (m0 & 1u) | ((m0 >> 15) & 2u) | ((m1 & 1u) << 2) | ((m1 >> 13) & 8u) |
+                          ((m2 & 1u) << 4) | ((m2 >> 11) & 0x20u) | ((m3 & 1u) << 6) | ((m3 >> 9) & 0x80u);
+    int pos = atomicAdd(&s.count, __popc(mask));
+    bool nf = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (mask & (1u << j)) {
+        if (pos < SX_CAP) s.cand[pos] = make_comp(elem_key<__nv_bfloat16>(v, j, nf), id0 + j);
+        else overflow = true;
+        ++pos;
+      }
+    }
+  }
+};
+
+template <>
+struct Filter<float> {
+  uint32_t bound;
+  __device__ void init(uint32_t b) { bound = b; }
+  __device__ __forceinline__ void run(SelShared& s, const uint4& v, uint32_t id0, bool& overflow) const {
+    bool nf = false;
+    uint32_t keys[4], mask = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      keys[j] = elem_key<float>(v, j, nf);
+      if (keys[j] >= bound) mask |= 1u << j;
+    }
+    if (!mask) return;
+    int pos = atomicAdd(&s.count, __popc(mask));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (mask & (1u << j)) {
+        if (pos < SX_CAP) s.cand[pos] = make_comp(keys[j], id0 + j);
+        else overflow = true;
+        ++pos;
+      }
+    }
+  }
+};
+
+// j-th largest of the 32 lane values of a warp (binary search on key bits).
+template <int KEY_BITS>
+__device__ __forceinline__ uint32_t warp_kth_largest(uint32_t key, int j) {
+  uint32_t res = 0;
+#pragma unroll
+  for (int bit = KEY_BITS - 1; bit >= 0; --bit) {
+    const uint32_t cand = res | (1u << bit);
+    if (__popc(__ballot_sync(FULL, key >= cand)) >= j) res = cand;
+  }
+  return res;
+}
+
+// Exact top-k of s.cand[0..n) (distinct composites) sorted descending into
+// s.cand[0..min(n,k)); count = min(n,k); when n >= k the strict threshold
+// becomes the key of the k-th.  Consumer threads only.
 template <int KEY_BITS>
 __device__ void select_topk(SelShared& s, int n, int k) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (n > k) {
-    // digit positions: the key (bits 32..32+KEY_BITS-1), then ~id bits 23..0
-    // (bits 31..24 of ~id are all ones for ids below 2^24)
+    // digits: the key bytes, then bits 23..0 of ~id (bits 31..24 of ~id are
+    // all ones for ids below 2^24)
     constexpr int NKD = KEY_BITS / 8;
-    int shifts[NKD + 3];
-#pragma unroll
-    for (int i = 0; i < NKD; ++i) shifts[i] = 32 + KEY_BITS - 8 * (i + 1);
-    shifts[NKD] = 16;
-    shifts[NKD + 1] = 8;
-    shifts[NKD + 2] = 0;
     uint64_t prefix = 0, pmask = 0;
     int need = k;
-    const int n_round = (n + SEL_THREADS - 1) / SEL_THREADS * SEL_THREADS;
+    const int n_round = (n + SX_CONS - 1) / SX_CONS * SX_CONS;
 #pragma unroll 1
     for (int d = 0; d < NKD + 3; ++d) {
-      const int sh = shifts[d];
-      if (tid < 256) s.hist[tid] = 0;
-      __syncthreads();
-      for (int i = tid; i < n_round; i += SEL_THREADS) {
+      const int sh = d < NKD ? 32 + KEY_BITS - 8 * (d + 1) : 8 * (NKD + 2 - d);
+      s.hist[tid] = 0;
+      csync();
+      for (int i = tid; i < n_round; i += SX_CONS) {
         bool valid = i < n;
         const uint64_t c = valid ? s.cand[i] : 0ull;
         valid = valid && ((c & pmask) == prefix);
@@ -186,7 +321,7 @@ __device__ void select_topk(SelShared& s, int n, int k) {
         const unsigned peers = __match_any_sync(FULL, tag);
         if (valid && lane == __ffs(peers) - 1) atomicAdd(&s.hist[bin], static_cast<uint32_t>(__popc(peers)));
       }
-      __syncthreads();
+      csync();
       if (warp == 0) {
         uint32_t h[8], tot = 0;
 #pragma unroll
@@ -215,7 +350,7 @@ __device__ void select_topk(SelShared& s, int n, int k) {
           }
         }
       }
-      __syncthreads();
+      csync();
       const int bin = s.radix_bin, above = s.radix_above, cnt = s.radix_cnt;
       need -= above;
       prefix |= static_cast<uint64_t>(bin) << sh;
@@ -223,18 +358,18 @@ __device__ void select_topk(SelShared& s, int n, int k) {
       if (cnt == need) break;
     }
     if (tid == 0) s.sel_count = 0;
-    __syncthreads();
-    for (int i = tid; i < n; i += SEL_THREADS) {
+    csync();
+    for (int i = tid; i < n; i += SX_CONS) {
       const uint64_t c = s.cand[i];
       if ((c & pmask) >= prefix) {
         const int pos = atomicAdd(&s.sel_count, 1);
         if (pos < SPEC_TREE_MAX_SUPPORT) s.sel[pos] = c;
       }
     }
-    __syncthreads();
+    csync();
   } else {
-    for (int i = tid; i < n; i += SEL_THREADS) s.sel[i] = s.cand[i];
-    __syncthreads();
+    for (int i = tid; i < n; i += SX_CONS) s.sel[i] = s.cand[i];
+    csync();
   }
   const int kk = n < k ? n : k;
   uint64_t c = 0;
@@ -243,9 +378,9 @@ __device__ void select_topk(SelShared& s, int n, int k) {
     c = s.sel[tid];
     for (int j = 0; j < kk; ++j) r += (s.sel[j] > c);
   }
-  __syncthreads();
+  csync();
   if (tid < kk) s.cand[r] = c;
-  __syncthreads();
+  csync();
   if (tid == 0) {
     s.count = kk;
     if (n >= k) {
@@ -253,7 +388,7 @@ __device__ void select_topk(SelShared& s, int n, int k) {
       s.strict = 1;
     }
   }
-  __syncthreads();
+  csync();
 }
 
 struct SelArgs {
@@ -277,225 +412,274 @@ struct SelArgs {
   uint32_t* status;
 };
 
-// Softmaxes, tail masses and the probe of one row from its sorted support
-// (warp 0).  RheoSampling Key design 2; the probe is the first tail rank k
-// with u * z_T < sum_{j=m..k} q_T(j), computed on unnormalised weights.
+// Robust selection of a row straight from global memory, in id order: keep
+// the exact top-|S| of the prefix seen, then only elements strictly above
+// its last key (an equal key later in id order loses the tie).
 template <typename T>
-__device__ void expand_epilogue(const SelShared& s, const SelArgs& a, int64_t out_row, int n_sup) {
-  const int lane = threadIdx.x & 31;
-  float l[4];
-  uint32_t id[4];
-  bool valid[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int r = 4 * lane + j;
-    valid[j] = r < n_sup;
-    const uint64_t c = valid[j] ? s.cand[r] : 0ull;
-    l[j] = key_value<T>(static_cast<uint32_t>(c >> 32));
-    id[j] = ~static_cast<uint32_t>(c);
+__device__ void select_row_fallback(SelShared& s, const uint8_t* row, int V, int S, bool& nonfinite,
+                                    bool& overflow) {
+  using E = Elem<T>;
+  constexpr int VEC = E::VEC;
+  const int tid = threadIdx.x;
+  const int nvec = static_cast<int>((static_cast<int64_t>(V) * E::ES) / 16);
+  csync();
+  if (tid == 0) {
+    s.count = 0;
+    s.thr_key = 0;
+    s.strict = 0;
   }
-  const float lmax = __shfl_sync(FULL, l[0], 0);
-  if (lane == 0 && !(lmax < INFINITY)) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
-  // weights relative to the row maximum; float32 sums (<= 128 terms, pairwise
-  // across lanes) keep the relative error near 1e-7
-  float e[4], eT[4];
-  float se = 0.0f, seT = 0.0f, te = 0.0f, teT = 0.0f;
+  csync();
+  const int steps = (V + SX_CONS * VEC - 1) / (SX_CONS * VEC);
+  for (int step = 0; step < steps; ++step) {
+    const int vi = step * SX_CONS + tid;
+    const uint64_t lo = static_cast<uint64_t>(s.thr_key) + static_cast<uint64_t>(s.strict);
+    uint32_t keys[VEC];
+    uint32_t mask = 0;
+    const uint32_t id0 = static_cast<uint32_t>(vi) * VEC;
+    if (vi < nvec) {
+      const uint4 v = ldg_stream(row + static_cast<int64_t>(vi) * 16);
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int r = 4 * lane + j;
-    const float d = l[j] - lmax;
-    e[j] = valid[j] ? expf(d) : 0.0f;
-    eT[j] = valid[j] ? expf(d / a.temperature) : 0.0f;
-    se += e[j];
-    seT += eT[j];
-    if (r >= a.m) {
-      te += e[j];
-      teT += eT[j];
-    }
-  }
-  se = warp_sum(se);
-  seT = warp_sum(seT);
-  te = warp_sum(te);
-  teT = warp_sum(teT);
-  int32_t* sid = a.sup_id + out_row * a.sup_stride;
-  float* sq = a.sup_q + out_row * a.sup_stride;
-  float* sqT = a.sup_qT + out_row * a.sup_stride;
+      for (int j = 0; j < VEC; ++j) {
+        keys[j] = elem_key<T>(v, j, nonfinite);
+        if (keys[j] >= lo) mask |= 1u << j;
+      }
+    } else {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int r = 4 * lane + j;
-    if (valid[j]) {
-      sid[r] = static_cast<int32_t>(id[j]);
-      sq[r] = e[j] / se;
-      sqT[r] = eT[j] / seT;
-    }
-  }
-  int probe = -1;
-  if (a.m < n_sup && teT > 0.0f) {
-    const float target = a.u_probe[out_row] * teT;
-    float cum[4], acc = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (4 * lane + j >= a.m) acc += eT[j];
-      cum[j] = acc;
-    }
-    float incl = acc;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float t = __shfl_up_sync(FULL, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const float excl = incl - acc;
-    int mine = -1, last_pos = -1;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int r = 4 * lane + j;
-      if (r >= a.m && valid[j]) {
-        if (mine < 0 && target < excl + cum[j]) mine = r;
-        if (eT[j] > 0.0f) last_pos = r;
+      for (int j = 0; j < VEC; ++j) {
+        keys[j] = 0;
+        const int id = static_cast<int>(id0) + j;
+        if (id < V) {
+          keys[j] = scalar_key<T>(row, id, nonfinite);
+          if (keys[j] >= lo) mask |= 1u << j;
+        }
       }
     }
-    const unsigned hit = __ballot_sync(FULL, mine >= 0);
-    if (hit) {
-      probe = __shfl_sync(FULL, mine, __ffs(hit) - 1);
-    } else {
-      const unsigned pos = __ballot_sync(FULL, last_pos >= 0);
-      probe = __shfl_sync(FULL, last_pos, 31 - __clz(pos));
-    }
+    append_warp<VEC>(s, mask, keys, id0, overflow);
+    csync();
+    if (s.count > SX_FB_HIGH) select_topk<E::KEY_BITS>(s, s.count, S);
   }
+}
+
+// Softmaxes, tail masses and the probe of one row from its sorted support,
+// by consumer warps 0..3 (one support rank per thread).  RheoSampling Key
+// design 2; the probe is the first tail rank k with
+// u * z_T < sum_{j=m..k} q_T(j), computed on unnormalised weights.
+__device__ __forceinline__ void esync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+template <typename T>
+__device__ void expand_epilogue(SelShared& s, const SelArgs& a, int64_t out_row, int n_sup) {
+  const int r = threadIdx.x, lane = r & 31, w = r >> 5;
+  const bool valid = r < n_sup, tail = valid && r >= a.m;
+  const uint64_t c = valid ? s.cand[r] : 0ull;
+  const float l = key_value<T>(static_cast<uint32_t>(c >> 32));
+  const float lmax = key_value<T>(static_cast<uint32_t>(s.cand[0] >> 32));
+  if (r == 0 && !(lmax < INFINITY)) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
+  const float d = l - lmax;
+  const float e = valid ? expf(d) : 0.0f;
+  const float eT = valid ? expf(d / a.temperature) : 0.0f;
+  const float te = tail ? e : 0.0f, teT = tail ? eT : 0.0f;
+  // inclusive scan of the tail weights (rank order) within the warp
+  float incl = teT;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const float w_e = warp_sum(e), w_eT = warp_sum(eT), w_te = warp_sum(te);
+  if (lane == 31) s.epi_scan[w] = incl;
   if (lane == 0) {
-    a.sup_z[out_row] = te / se;
-    a.sup_zT[out_row] = teT / seT;
+    s.epi_red[w][0] = w_e;
+    s.epi_red[w][1] = w_eT;
+    s.epi_red[w][2] = w_te;
+  }
+  esync();
+  float se = 0.0f, seT = 0.0f, tz = 0.0f, tzT = 0.0f, before = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    se += s.epi_red[k][0];
+    seT += s.epi_red[k][1];
+    tz += s.epi_red[k][2];
+    tzT += s.epi_scan[k];
+    if (k < w) before += s.epi_scan[k];
+  }
+  if (valid) {
+    a.sup_id[out_row * a.sup_stride + r] = static_cast<int32_t>(~static_cast<uint32_t>(c));
+    a.sup_q[out_row * a.sup_stride + r] = e / se;
+    a.sup_qT[out_row * a.sup_stride + r] = eT / seT;
+  }
+  if (a.m < n_sup && tzT > 0.0f) {
+    const float target = a.u_probe[out_row] * tzT;
+    if (tail && target < before + incl) atomicMin(&s.probe_first, r);
+    if (tail && eT > 0.0f) atomicMax(&s.probe_last, r);
+  }
+  esync();
+  if (r == 0) {
+    int probe = -1;
+    if (a.m < n_sup && tzT > 0.0f) probe = s.probe_first < SPEC_TREE_MAX_SUPPORT ? s.probe_first : s.probe_last;
+    a.sup_z[out_row] = tz / se;
+    a.sup_zT[out_row] = tzT / seT;
     a.probe_pos[out_row] = probe;
+    s.probe_first = 1 << 30;
+    s.probe_last = -1;
   }
 }
 
 template <typename T>
-__global__ void __launch_bounds__(SEL_THREADS, 2) select_expand_kernel(SelArgs a) {
+__global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a) {
   using E = Elem<T>;
   constexpr int VEC = E::VEC;
-  constexpr int CHUNK_ELEMS = SEL_CHUNK / E::ES;
+  constexpr int CHUNK_ELEMS = SX_CHUNK / E::ES;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SelShared& s = *reinterpret_cast<SelShared*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   const int64_t row_bytes = static_cast<int64_t>(a.V) * E::ES;
   const int64_t tma_bytes = row_bytes & ~static_cast<int64_t>(15);
-  const int nch = static_cast<int>((tma_bytes + SEL_CHUNK - 1) / SEL_CHUNK);
-  const int tail_begin = static_cast<int>(tma_bytes / E::ES);
-  const int64_t my_rows =
-      a.total_rows > blockIdx.x ? (a.total_rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const int64_t my_chunks = my_rows * nch;
-
-  auto row_ptr = [&](int64_t lr) -> const uint8_t* {
-    const int64_t gr = blockIdx.x + lr * gridDim.x;
-    const int64_t b = gr / a.rows_used, e = gr % a.rows_used;
-    return a.logits + (b * a.n_rows + e) * a.row_bytes_stride;
-  };
-  const uint64_t policy = l2_evict_first_policy();
-  auto issue = [&](int64_t g) {
-    const int64_t lr = g / nch;
-    const int c = static_cast<int>(g % nch);
-    const int64_t off = static_cast<int64_t>(c) * SEL_CHUNK;
-    const uint32_t bytes = static_cast<uint32_t>(min64(SEL_CHUNK, tma_bytes - off));
-    const int st = static_cast<int>(g % SEL_STAGES);
-    mbar_expect_tx(&s.full[st], bytes);
-    bulk_g2s(s.ring[st], row_ptr(lr) + off, bytes, &s.full[st], policy);
-  };
+  const int nch = static_cast<int>((tma_bytes + SX_CHUNK - 1) / SX_CHUNK);
+  const int tail_begin = static_cast<int>(tma_bytes / 16) * VEC;
+  const int64_t my_rows = a.total_rows > blockIdx.x ? (a.total_rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
   if (tid == 0) {
-    for (int i = 0; i < SEL_STAGES; ++i) mbar_init(&s.full[i], 1);
+    for (int i = 0; i < SX_STAGES; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], SX_CWARPS);
+    }
     fence_mbar_init();
     s.timeout = 0;
-    for (int64_t g = 0; g < my_chunks && g < SEL_STAGES; ++g) issue(g);
+    s.probe_first = 1 << 30;
+    s.probe_last = -1;
   }
-  __syncthreads();
+  __syncthreads();  // the last CTA-wide barrier: the roles split below
 
-  bool nonfinite = false, overflow = false;
-  int64_t g = 0;
+  if (warp == SX_CWARPS) {
+    // ------------------------------------------------------------ producer ---
+    if (lane == 0 && nch > 0) {
+      const uint64_t keep = l2_evict_last_policy();
+      const uint64_t drop = l2_evict_first_policy();
+      int st = 0;
+      uint32_t phase = 0;
+      int64_t g = 0;
+      bool timed_out = false;
+      int64_t b = blockIdx.x / a.rows_used, e = blockIdx.x % a.rows_used;
+      for (int64_t lr = 0; lr < my_rows; ++lr) {
+        const uint8_t* row = a.logits + (b * a.n_rows + e) * a.row_bytes_stride;
+        for (int pass = 0; pass < 2; ++pass) {
+          for (int c = 0; c < nch; ++c, ++g) {
+            // stage reuse: wait until every consumer warp released its last use
+            if (g >= SX_STAGES && !mbar_wait(&s.empty[st], phase ^ 1u)) timed_out = true;
+            const int64_t off = static_cast<int64_t>(c) * SX_CHUNK;
+            const uint32_t bytes = static_cast<uint32_t>(min64(SX_CHUNK, tma_bytes - off));
+            mbar_expect_tx(&s.full[st], bytes);
+            bulk_g2s(s.ring[st], row + off, bytes, &s.full[st], pass == 0 ? keep : drop);
+            if (++st == SX_STAGES) {
+              st = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        e += gridDim.x;  // next row of this CTA, without dividing
+        while (e >= a.rows_used) {
+          e -= a.rows_used;
+          ++b;
+        }
+      }
+      if (timed_out) s.timeout = 1;
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers ---
+  bool nonfinite = false, overflow = false, p2over = false;
+  int st = 0;
+  uint32_t phase = 0;
+  int64_t b = blockIdx.x / a.rows_used, e = blockIdx.x % a.rows_used;
+  const int jth = (a.S + SX_CWARPS - 1) / SX_CWARPS;
   for (int64_t lr = 0; lr < my_rows; ++lr) {
-    const int64_t gr = blockIdx.x + lr * gridDim.x;
-    const int64_t out_row = (gr / a.rows_used) * a.n_rows + gr % a.rows_used;
-    if (tid == 0) {
-      s.count = 0;
-      s.thr_key = 0;
-      s.strict = 0;
-    }
-    __syncthreads();
-    for (int c = 0; c < nch; ++c, ++g) {
-      const int st = static_cast<int>(g % SEL_STAGES);
-      if (!mbar_wait(&s.full[st], static_cast<uint32_t>((g / SEL_STAGES) & 1))) s.timeout = 1;
-      const int64_t off = static_cast<int64_t>(c) * SEL_CHUNK;
-      const int nvec = static_cast<int>(min64(SEL_CHUNK, tma_bytes - off) / 16);
-      const bool have = tid < nvec;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (have) v = *reinterpret_cast<const uint4*>(s.ring[st] + tid * 16);
-      const uint32_t id0 = static_cast<uint32_t>(c) * CHUNK_ELEMS + tid * VEC;
-      uint64_t lo;
-      if (c == 0) {
-        // Warm start: 128 groups of 4 lanes; the smallest group maximum is a
-        // lower bound of the 128th largest key of the row (each group
-        // contributes a distinct element at least that large).
-        uint32_t gk = 0u;  // NaN keys are 0 here, so they only lower the bound
-        if (have) {
-          bool nf = false;
+    const int64_t out_row = b * a.n_rows + e;
+    const uint8_t* row = a.logits + out_row * a.row_bytes_stride;
+
+    // pass 1: running maximum of this thread's elements
+    RunMax<T> rm;
+    rm.init();
+    for (int c = 0; c < nch; ++c) {
+      if (!mbar_wait(&s.full[st], phase)) s.timeout = 1;
+      const int nvec = static_cast<int>(min64(SX_CHUNK, tma_bytes - static_cast<int64_t>(c) * SX_CHUNK) / 16);
+      uint4 v[SX_VPT];
 #pragma unroll
-          for (int j = 0; j < VEC; ++j) gk = max(gk, elem_key<T>(v, j, nf));
-        }
-        gk = max(gk, __shfl_xor_sync(FULL, gk, 1));
-        gk = max(gk, __shfl_xor_sync(FULL, gk, 2));
-        uint32_t wm = gk;
-        wm = min(wm, __shfl_xor_sync(FULL, wm, 4));
-        wm = min(wm, __shfl_xor_sync(FULL, wm, 8));
-        wm = min(wm, __shfl_xor_sync(FULL, wm, 16));
-        if (lane == 0) s.warp_min[warp] = wm;
-        __syncthreads();
-        uint32_t t0 = 0xffffffffu;
+      for (int k = 0; k < SX_VPT; ++k) {
+        const int vi = tid + k * SX_CONS;
+        v[k] = vi < nvec ? *reinterpret_cast<const uint4*>(s.ring[st] + vi * 16) : make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.empty[st]);
 #pragma unroll
-        for (int w = 0; w < SEL_WARPS; ++w) t0 = min(t0, s.warp_min[w]);
-        lo = t0;
-        if (tid == 0) s.thr_key = t0;  // still inclusive
-      } else {
-        lo = static_cast<uint64_t>(s.thr_key) + static_cast<uint64_t>(s.strict);
+      for (int k = 0; k < SX_VPT; ++k)
+        if (tid + k * SX_CONS < nvec) rm.add(v[k]);
+      if (++st == SX_STAGES) {
+        st = 0;
+        phase ^= 1u;
       }
-      uint32_t mask = 0;
-      uint32_t keys[VEC];
-      if (have && vec_max_key<T>(v) >= lo) {
+    }
+    const int tail_id = tail_begin + tid;  // elements past the last whole vector
+    uint32_t tail_key = 0;
+    if (tail_id < a.V) {
+      tail_key = scalar_key<T>(row, tail_id, nonfinite);
+      rm.add_key(tail_key);
+    }
+    // bound: min over consumer warps of the warp's jth-largest thread maximum
+    const uint32_t wb = warp_kth_largest<E::KEY_BITS>(rm.key(nonfinite), jth);
+    if (lane == 0) s.warp_bound[warp] = wb;
+    if (tid == 0) s.count = 0;
+    csync();
+    uint32_t bound = 0xffffffffu;
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-          keys[j] = elem_key<T>(v, j, nonfinite);
-          if (keys[j] >= lo) mask |= 1u << j;
-        }
+    for (int w = 0; w < SX_CWARPS; ++w) bound = min(bound, s.warp_bound[w]);
+    // a bound of key 0 (a thread maximum was NaN) has no value to compare
+    // against: such rows take the robust path below
+    const bool robust = bound == 0u;
+    Filter<T> flt;
+    flt.init(robust ? 0xffffffffu : bound);
+
+    // pass 2: candidates at or above the bound
+    for (int c = 0; c < nch; ++c) {
+      if (!mbar_wait(&s.full[st], phase)) s.timeout = 1;
+      const int nvec = static_cast<int>(min64(SX_CHUNK, tma_bytes - static_cast<int64_t>(c) * SX_CHUNK) / 16);
+      uint4 v[SX_VPT];
+#pragma unroll
+      for (int k = 0; k < SX_VPT; ++k) {
+        const int vi = tid + k * SX_CONS;
+        v[k] = vi < nvec ? *reinterpret_cast<const uint4*>(s.ring[st] + vi * 16) : make_uint4(0, 0, 0, 0);
       }
-      append_warp<VEC>(s, mask, keys, id0, overflow);
-      __syncthreads();
-      if (tid == 0 && g + SEL_STAGES < my_chunks) {
-        fence_proxy_async_smem();
-        issue(g + SEL_STAGES);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.empty[st]);
+#pragma unroll
+      for (int k = 0; k < SX_VPT; ++k) {
+        const int vi = tid + k * SX_CONS;
+        if (vi < nvec) flt.run(s, v[k], static_cast<uint32_t>(c * CHUNK_ELEMS + vi * VEC), p2over);
       }
-      if (s.timeout) break;
-      if (s.count > SEL_HIGH) select_topk<E::KEY_BITS>(s, s.count, a.S);
+      if (++st == SX_STAGES) {
+        st = 0;
+        phase ^= 1u;
+      }
     }
-    if (s.timeout) break;
-    // elements past the last whole 16-byte vector (V not a multiple of VEC)
-    if (warp == 0) {
-      const int t = tail_begin + lane;
-      uint32_t keys[1] = {0u};
-      uint32_t mask = 0;
-      if (t < a.V) {
-        const uint8_t* p = row_ptr(lr) + static_cast<int64_t>(t) * E::ES;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (E::ES == 2) v.x = *reinterpret_cast<const uint16_t*>(p);
-        else v.x = *reinterpret_cast<const uint32_t*>(p);
-        keys[0] = elem_key<T>(v, 0, nonfinite);
-        const uint64_t lo = nch == 0 ? 0ull : static_cast<uint64_t>(s.thr_key) + static_cast<uint64_t>(s.strict);
-        if (keys[0] >= lo) mask = 1u;
-      }
-      append_warp<1>(s, mask, keys, static_cast<uint32_t>(t), overflow);
+    if (tail_id < a.V && tail_key >= bound && !robust) {
+      const int pos = atomicAdd(&s.count, 1);
+      if (pos < SX_CAP) s.cand[pos] = make_comp(tail_key, static_cast<uint32_t>(tail_id));
     }
-    __syncthreads();
-    const int n = s.count;
+    csync();
+    int n = s.count;
+    if (n > SX_CAP || robust) {
+      // massive ties at the bound: redo the row in id order from global memory
+      select_row_fallback<T>(s, row, a.V, a.S, nonfinite, overflow);
+      n = s.count;
+    }
     select_topk<E::KEY_BITS>(s, n, a.S);
-    if (warp == 0) expand_epilogue<T>(s, a, out_row, n < a.S ? n : a.S);
+    if (warp < 4) expand_epilogue<T>(s, a, out_row, n < a.S ? n : a.S);
+    e += gridDim.x;
+    while (e >= a.rows_used) {
+      e -= a.rows_used;
+      ++b;
+    }
   }
   if (s.timeout && tid == 0) set_status(a.status, SPEC_TREE_S_TIMEOUT);
   if (nonfinite) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
@@ -529,12 +713,12 @@ cudaError_t launch_select_expand(int dtype, const SelLaunch& L, cudaStream_t str
     cudaError_t err = cudaFuncSetAttribute(select_expand_kernel<__nv_bfloat16>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    select_expand_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), SEL_THREADS, smem, stream>>>(a);
+    select_expand_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), SX_THREADS, smem, stream>>>(a);
   } else {
     cudaError_t err = cudaFuncSetAttribute(select_expand_kernel<float>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    select_expand_kernel<float><<<static_cast<unsigned>(grid), SEL_THREADS, smem, stream>>>(a);
+    select_expand_kernel<float><<<static_cast<unsigned>(grid), SX_THREADS, smem, stream>>>(a);
   }
   return cudaGetLastError();
 }

@@ -12,9 +12,11 @@ namespace st {
 constexpr unsigned FULL = 0xffffffffu;
 
 __host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
-// Upper bound on mbarrier polls before a wait gives up (each try_wait may
-// suspend the thread for a while, so this is far beyond any real latency).
-constexpr uint32_t WAIT_LIMIT = 1u << 24;
+// Bounded mbarrier waits: each poll may suspend the thread for up to
+// WAIT_SUSPEND_NS (it wakes as soon as the phase completes); after
+// WAIT_LIMIT polls (over a second) the wait gives up and reports a timeout.
+constexpr uint32_t WAIT_LIMIT = 1u << 16;
+constexpr uint32_t WAIT_SUSPEND_NS = 20000;
 
 // ------------------------------------------------------------- order keys ---
 // Order-preserving unsigned keys of float bit patterns: larger key <=> larger
@@ -74,16 +76,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t it = 0; it < WAIT_LIMIT; ++it) {
     uint32_t done;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
-        : "r"(addr), "r"(parity)
+        : "r"(addr), "r"(parity), "r"(WAIT_SUSPEND_NS)
         : "memory");
     if (done) return true;
   }
   return false;
 }
 
-// L2 policy for data read once (draft rows): evict first.
+// L2 policy for data read again soon: evict last.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// L2 policy for data read for the last time: evict first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));

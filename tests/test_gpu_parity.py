@@ -61,7 +61,7 @@ def test_smart_parity_llama_vocab():
 
 
 EDGE = {
-    "support_is_V": dict(V=100, K=8, m=1, W=4, depth=4, R=12),
+    "support_is_V": dict(V=100, K=8, m=1, W=4, depth=4, R=12, stride=104),
     "ragged_V": dict(V=1001, K=8, m=1, W=4, depth=4, R=20, stride=1008),
     "tiny_V_no_vector": dict(V=5, K=2, m=1, W=2, depth=3, R=6, stride=8),
     "f32_ragged": dict(V=4099, K=6, m=1, W=3, depth=3, R=10, dtype="f32", stride=4100),
