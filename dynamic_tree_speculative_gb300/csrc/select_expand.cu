@@ -44,19 +44,25 @@ constexpr int SX_VPT = 4;                        // 16-byte vectors per consumer
 constexpr int SX_CHUNK = SX_CONS * 16 * SX_VPT;  // 16 KB per stage
 constexpr int SX_STAGES = 4;
 constexpr int SX_CAP = 4096;                     // candidate buffer (64-bit composites)
+constexpr int SX_QCAP = 512;                     // pass-2 queue of vectors that reach the bound
 constexpr int SX_FB_STEP = SX_CONS * 8;          // robust path: at most this many appends per step
 constexpr int SX_FB_HIGH = SX_CAP - SX_FB_STEP;
 
 struct SelShared {
   alignas(128) uint8_t ring[SX_STAGES][SX_CHUNK];
   uint64_t cand[SX_CAP];
+  uint4 qvec[SX_QCAP];
+  uint32_t qid[SX_QCAP];
   uint64_t sel[SPEC_TREE_MAX_SUPPORT];
+  uint64_t tie[32];
   uint64_t full[SX_STAGES];
   uint64_t empty[SX_STAGES];
   uint32_t hist[256];
   uint32_t warp_bound[SX_CWARPS];
   int count;
+  int qcount;
   int sel_count;
+  int tie_count;
   int radix_bin;
   int radix_above;
   int radix_cnt;
@@ -218,10 +224,11 @@ __device__ __forceinline__ void append_warp(SelShared& s, uint32_t mask, const u
   }
 }
 
-// Pass-2 filter of one 16-byte vector: append every element whose key is at
-// least `bound` (per-lane shared atomics; only lanes with hits do any work).
-// bf16: packed bf16x2 compares against the bound's value, which order exactly
-// like the keys for every non-NaN element (NaN compares false and sorts last).
+// Pass-2 filter of 16-byte vectors against the bound: `pass` tells whether
+// any element reaches it; `emit` appends every element that does (one shared
+// atomic per lane).  bf16: packed bf16x2 compares against the bound's value,
+// which order exactly like the keys for every non-NaN element (NaN compares
+// false and sorts last).
 template <typename T>
 struct Filter;
 
@@ -232,14 +239,20 @@ struct Filter<__nv_bfloat16> {
     const __nv_bfloat16 bv = __float2bfloat16_rn(bf16_key_value(bound));
     b2 = __halves2bfloat162(bv, bv);
   }
-  __device__ __forceinline__ void run(SelShared& s, const uint4& v, uint32_t id0, bool& overflow) const {
+  __device__ __forceinline__ bool pass(const uint4& v) const {
     const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
     const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
     const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
     const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&v.w);
     __nv_bfloat162 mx = __hmax2(__hmax2(a, b), __hmax2(c, d));
     mx = __hmax2(mx, __lowhigh2highlow(mx));
-    if (!__hbge2(mx, b2)) return;
+    return __hbge2(mx, b2);
+  }
+  __device__ __forceinline__ void emit(SelShared& s, const uint4& v, uint32_t id0, bool& overflow) const {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
+    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
+    const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&v.w);
     const uint32_t m0 = __hge2_mask(a, b2), m1 = __hge2_mask(b, b2);
     const uint32_t m2 = __hge2_mask(c, b2), m3 = __hge2_mask(d, b2);
     const uint32_t mask = (m0 & 1u) | ((m0 >> 15) & 2u) | ((m1 & 1u) << 2) | ((m1 >> 13) & 8u) |
@@ -261,7 +274,14 @@ template <>
 struct Filter<float> {
   uint32_t bound;
   __device__ void init(uint32_t b) { bound = b; }
-  __device__ __forceinline__ void run(SelShared& s, const uint4& v, uint32_t id0, bool& overflow) const {
+  __device__ __forceinline__ bool pass(const uint4& v) const {
+    bool nf = false;
+    uint32_t k = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) k = max(k, elem_key<float>(v, j, nf));
+    return k >= bound;
+  }
+  __device__ __forceinline__ void emit(SelShared& s, const uint4& v, uint32_t id0, bool& overflow) const {
     bool nf = false;
     uint32_t keys[4], mask = 0;
 #pragma unroll
@@ -269,7 +289,6 @@ struct Filter<float> {
       keys[j] = elem_key<float>(v, j, nf);
       if (keys[j] >= bound) mask |= 1u << j;
     }
-    if (!mask) return;
     int pos = atomicAdd(&s.count, __popc(mask));
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -306,6 +325,7 @@ __device__ void select_topk(SelShared& s, int n, int k) {
     constexpr int NKD = KEY_BITS / 8;
     uint64_t prefix = 0, pmask = 0;
     int need = k;
+    bool tie_mode = false;
     const int n_round = (n + SX_CONS - 1) / SX_CONS * SX_CONS;
 #pragma unroll 1
     for (int d = 0; d < NKD + 3; ++d) {
@@ -356,12 +376,36 @@ __device__ void select_topk(SelShared& s, int n, int k) {
       prefix |= static_cast<uint64_t>(bin) << sh;
       pmask |= 0xffull << sh;
       if (cnt == need) break;
+      if (d == NKD - 1 && cnt <= 32) {
+        // a few candidates share the boundary key: one warp keeps the `need`
+        // smallest ids among them instead of three more radix passes
+        tie_mode = true;
+        break;
+      }
     }
-    if (tid == 0) s.sel_count = 0;
+    if (tid == 0) {
+      s.sel_count = 0;
+      s.tie_count = 0;
+    }
     csync();
     for (int i = tid; i < n; i += SX_CONS) {
       const uint64_t c = s.cand[i];
-      if ((c & pmask) >= prefix) {
+      const uint64_t m = c & pmask;
+      if (tie_mode ? m > prefix : m >= prefix) {
+        const int pos = atomicAdd(&s.sel_count, 1);
+        if (pos < SPEC_TREE_MAX_SUPPORT) s.sel[pos] = c;
+      } else if (tie_mode && m == prefix) {
+        const int pos = atomicAdd(&s.tie_count, 1);
+        if (pos < 32) s.tie[pos] = c;
+      }
+    }
+    csync();
+    if (tie_mode && warp == 0) {
+      const int nt = min(s.tie_count, 32);
+      const uint64_t c = lane < nt ? s.tie[lane] : 0ull;
+      int r = 0;
+      for (int j = 0; j < nt; ++j) r += s.tie[j] > c;
+      if (lane < nt && r < need) {
         const int pos = atomicAdd(&s.sel_count, 1);
         if (pos < SPEC_TREE_MAX_SUPPORT) s.sel[pos] = c;
       }
@@ -629,7 +673,10 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
     // bound: min over consumer warps of the warp's jth-largest thread maximum
     const uint32_t wb = warp_kth_largest<E::KEY_BITS>(rm.key(nonfinite), jth);
     if (lane == 0) s.warp_bound[warp] = wb;
-    if (tid == 0) s.count = 0;
+    if (tid == 0) {
+      s.count = 0;
+      s.qcount = 0;
+    }
     csync();
     uint32_t bound = 0xffffffffu;
 #pragma unroll
@@ -655,20 +702,34 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
 #pragma unroll
       for (int k = 0; k < SX_VPT; ++k) {
         const int vi = tid + k * SX_CONS;
-        if (vi < nvec) flt.run(s, v[k], static_cast<uint32_t>(c * CHUNK_ELEMS + vi * VEC), p2over);
+        if (vi < nvec && flt.pass(v[k])) {
+          // queue the vector; its elements are examined after the pass with
+          // every lane busy instead of one lane per warp
+          const int qp = atomicAdd(&s.qcount, 1);
+          if (qp < SX_QCAP) {
+            s.qvec[qp] = v[k];
+            s.qid[qp] = static_cast<uint32_t>(c * CHUNK_ELEMS + vi * VEC);
+          }
+        }
       }
       if (++st == SX_STAGES) {
         st = 0;
         phase ^= 1u;
       }
     }
-    if (tail_id < a.V && tail_key >= bound && !robust) {
-      const int pos = atomicAdd(&s.count, 1);
-      if (pos < SX_CAP) s.cand[pos] = make_comp(tail_key, static_cast<uint32_t>(tail_id));
+    csync();
+    const int qn = s.qcount;
+    const bool q_over = qn > SX_QCAP;
+    if (!q_over) {
+      for (int i = tid; i < qn; i += SX_CONS) flt.emit(s, s.qvec[i], s.qid[i], p2over);
+      if (tail_id < a.V && tail_key >= bound && !robust) {
+        const int pos = atomicAdd(&s.count, 1);
+        if (pos < SX_CAP) s.cand[pos] = make_comp(tail_key, static_cast<uint32_t>(tail_id));
+      }
     }
     csync();
     int n = s.count;
-    if (n > SX_CAP || robust) {
+    if (n > SX_CAP || robust || q_over) {
       // massive ties at the bound: redo the row in id order from global memory
       select_row_fallback<T>(s, row, a.V, a.S, nonfinite, overflow);
       n = s.count;
