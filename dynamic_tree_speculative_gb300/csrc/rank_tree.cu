@@ -20,7 +20,7 @@
 
 namespace st {
 
-constexpr int RANK_THREADS = 256;
+constexpr int RANK_THREADS = 512;
 
 struct RankShared {
   uint64_t key[SPEC_TREE_MAX_CAND];
@@ -30,7 +30,9 @@ struct RankShared {
   int32_t meta[SPEC_TREE_MAX_CAND];    // depth << 16 | kind << 12 | slot
   int32_t exp_row[SPEC_TREE_MAX_CAND];
   int32_t pos[SPEC_TREE_MAX_CAND];     // canonical node index, -1 = pruned
-  int32_t aux[SPEC_TREE_MAX_CAND];     // top-R: selected flag; SMART: layer order
+  int32_t aux[SPEC_TREE_MAX_CAND];     // SMART: layer order
+  uint64_t skey[SPEC_TREE_MAX_CAND];   // top-R: keys sorted descending
+  int32_t sidx[SPEC_TREE_MAX_CAND];    // top-R: candidate of each sorted key
   int32_t front[SPEC_TREE_MAX_NODES];  // current frontier / active list (candidate indices)
   int32_t front_next[SPEC_TREE_MAX_NODES];
   // children of every expanded row, precomputed: entry row * K + slot
@@ -182,25 +184,44 @@ __global__ void __launch_bounds__(RANK_THREADS) rank_topr_kernel(RankLaunch L) {
     __syncthreads();
   }
   const int nc = s.nc;
-  // global top-R, then canonical order (depth ascending, then key)
-  for (int i = tid; i < nc; i += RANK_THREADS) {
-    const uint64_t k = s.key[i];
-    int r = 0;
-    for (int j = 0; j < nc; ++j) r += s.key[j] > k;
-    s.aux[i] = r < R;
+  // global top-R: bitonic sort of all candidate keys, descending (keys are
+  // distinct; the zero padding sorts below every real key)
+  int n2 = 1;
+  while (n2 < nc) n2 <<= 1;
+  for (int i = tid; i < n2; i += RANK_THREADS) {
+    s.skey[i] = i < nc ? s.key[i] : 0ull;
+    s.sidx[i] = i < nc ? i : -1;
   }
   __syncthreads();
-  for (int i = tid; i < nc; i += RANK_THREADS) {
-    if (!s.aux[i]) continue;
-    const int di = s.meta[i] >> 16;
-    const uint64_t k = s.key[i];
-    int r = 1;
-    for (int j = 0; j < nc; ++j) {
-      if (!s.aux[j]) continue;
-      const int dj = s.meta[j] >> 16;
-      r += (dj < di) || (dj == di && s.key[j] > k);
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < n2; i += RANK_THREADS) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint64_t x = s.skey[i], y = s.skey[l];
+          if (((i & k) == 0) ? (x < y) : (x > y)) {
+            s.skey[i] = y;
+            s.skey[l] = x;
+            const int xi = s.sidx[i];
+            s.sidx[i] = s.sidx[l];
+            s.sidx[l] = xi;
+          }
+        }
+      }
+      __syncthreads();
     }
-    s.pos[i] = r;
+  }
+  // canonical order of the top R: depth ascending, then key (sorted order)
+  const int nsel = nc < R ? nc : R;
+  for (int r = tid; r < nsel; r += RANK_THREADS) {
+    const int ci = s.sidx[r];
+    const int di = s.meta[ci] >> 16;
+    int pos = 1;
+    for (int j = 0; j < nsel; ++j) {
+      const int dj = s.meta[s.sidx[j]] >> 16;
+      pos += (dj < di) || (dj == di && j < r);
+    }
+    s.pos[ci] = pos;
   }
   __syncthreads();
   write_nodes(s, L, b, 1 + (nc < R ? nc : R));

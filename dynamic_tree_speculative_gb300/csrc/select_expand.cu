@@ -43,9 +43,11 @@ constexpr int SX_THREADS = SX_CONS + 32;         // + one producer warp
 constexpr int SX_VPT = 4;                        // 16-byte vectors per consumer thread per stage
 constexpr int SX_CHUNK = SX_CONS * 16 * SX_VPT;  // 16 KB per stage
 constexpr int SX_STAGES = 4;
-constexpr int SX_CAP = 4096;                     // candidate buffer (64-bit composites)
-constexpr int SX_QCAP = 512;                     // pass-2 queue of vectors that reach the bound
-constexpr int SX_FB_STEP = SX_CONS * 8;          // robust path: at most this many appends per step
+constexpr int SX_FB_THREADS = 128;               // robust path: threads reading per step
+constexpr int SX_CAP = 512 + SX_FB_THREADS * 8;  // candidate buffer (64-bit composites)
+constexpr int SX_QCAP = 1024;                    // pass-2 queue of vectors that reach the bound
+constexpr int SX_QW = SX_QCAP / SX_CWARPS;       // queue slots owned by each consumer warp
+constexpr int SX_FB_STEP = SX_FB_THREADS * 8;    // robust path: at most this many appends per step
 constexpr int SX_FB_HIGH = SX_CAP - SX_FB_STEP;
 
 struct SelShared {
@@ -60,7 +62,7 @@ struct SelShared {
   uint32_t hist[256];
   uint32_t warp_bound[SX_CWARPS];
   int count;
-  int qcount;
+  int qn_warp[SX_CWARPS];
   int sel_count;
   int tie_count;
   int radix_bin;
@@ -150,6 +152,20 @@ struct RunMax<__nv_bfloat16> {
     m = __hmax2_nan(m, __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d)));
     any = true;
   }
+  // four vectors at once: a balanced tree of packed maxima
+  __device__ void add4(const uint4* v) {
+    __nv_bfloat162 x[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __nv_bfloat162* w = reinterpret_cast<const __nv_bfloat162*>(&v[q]);
+      x[2 * q] = __hmax2_nan(w[0], w[1]);
+      x[2 * q + 1] = __hmax2_nan(w[2], w[3]);
+    }
+    const __nv_bfloat162 y0 = __hmax2_nan(__hmax2_nan(x[0], x[1]), __hmax2_nan(x[2], x[3]));
+    const __nv_bfloat162 y1 = __hmax2_nan(__hmax2_nan(x[4], x[5]), __hmax2_nan(x[6], x[7]));
+    m = __hmax2_nan(m, __hmax2_nan(y0, y1));
+    any = true;
+  }
   __device__ void add_key(uint32_t key) {
     extra = max(extra, key);
     any = true;
@@ -176,6 +192,10 @@ struct RunMax<float> {
   __device__ void add(const uint4& v) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) k = max(k, elem_key<float>(v, j, nf));
+  }
+  __device__ void add4(const uint4* v) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) add(v[q]);
   }
   __device__ void add_key(uint32_t key) { k = max(k, key); }
   __device__ uint32_t key(bool& nonfinite) const {
@@ -239,6 +259,21 @@ struct Filter<__nv_bfloat16> {
     const __nv_bfloat16 bv = __float2bfloat16_rn(bf16_key_value(bound));
     b2 = __halves2bfloat162(bv, bv);
   }
+  // element-wise maximum of four vectors (NaN ignored)
+  __device__ static __forceinline__ uint4 merge4(const uint4* v) {
+    uint4 r;
+    uint32_t* o = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const __nv_bfloat162 x0 = reinterpret_cast<const __nv_bfloat162*>(&v[0])[w];
+      const __nv_bfloat162 x1 = reinterpret_cast<const __nv_bfloat162*>(&v[1])[w];
+      const __nv_bfloat162 x2 = reinterpret_cast<const __nv_bfloat162*>(&v[2])[w];
+      const __nv_bfloat162 x3 = reinterpret_cast<const __nv_bfloat162*>(&v[3])[w];
+      const __nv_bfloat162 mx = __hmax2(__hmax2(x0, x1), __hmax2(x2, x3));
+      o[w] = *reinterpret_cast<const uint32_t*>(&mx);
+    }
+    return r;
+  }
   __device__ __forceinline__ bool pass(const uint4& v) const {
     const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
     const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
@@ -274,6 +309,19 @@ template <>
 struct Filter<float> {
   uint32_t bound;
   __device__ void init(uint32_t b) { bound = b; }
+  // element-wise maximum of four vectors in key order
+  __device__ static __forceinline__ uint4 merge4(const uint4* v) {
+    uint4 r;
+    uint32_t* o = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t k = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) k = max(k, f32_key(reinterpret_cast<const uint32_t*>(&v[q])[w]));
+      o[w] = f32_from_key(k);
+    }
+    return r;
+  }
   __device__ __forceinline__ bool pass(const uint4& v) const {
     bool nf = false;
     uint32_t k = 0;
@@ -473,14 +521,17 @@ __device__ void select_row_fallback(SelShared& s, const uint8_t* row, int V, int
     s.strict = 0;
   }
   csync();
-  const int steps = (V + SX_CONS * VEC - 1) / (SX_CONS * VEC);
+  const int steps = (V + SX_FB_THREADS * VEC - 1) / (SX_FB_THREADS * VEC);
   for (int step = 0; step < steps; ++step) {
-    const int vi = step * SX_CONS + tid;
+    const int vi = tid < SX_FB_THREADS ? step * SX_FB_THREADS + tid : 0x7fffffff;
     const uint64_t lo = static_cast<uint64_t>(s.thr_key) + static_cast<uint64_t>(s.strict);
     uint32_t keys[VEC];
     uint32_t mask = 0;
     const uint32_t id0 = static_cast<uint32_t>(vi) * VEC;
-    if (vi < nvec) {
+    if (vi == 0x7fffffff) {
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) keys[j] = 0;
+    } else if (vi < nvec) {
       const uint4 v = ldg_stream(row + static_cast<int64_t>(vi) * 16);
 #pragma unroll
       for (int j = 0; j < VEC; ++j) {
@@ -581,6 +632,7 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
   const int64_t tma_bytes = row_bytes & ~static_cast<int64_t>(15);
   const int nch = static_cast<int>((tma_bytes + SX_CHUNK - 1) / SX_CHUNK);
   const int tail_begin = static_cast<int>(tma_bytes / 16) * VEC;
+  const int last_nvec = nch > 0 ? static_cast<int>((tma_bytes - static_cast<int64_t>(nch - 1) * SX_CHUNK) / 16) : 0;
   const int64_t my_rows = a.total_rows > blockIdx.x ? (a.total_rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
   if (tid == 0) {
@@ -647,18 +699,24 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
     rm.init();
     for (int c = 0; c < nch; ++c) {
       if (!mbar_wait(&s.full[st], phase)) s.timeout = 1;
-      const int nvec = static_cast<int>(min64(SX_CHUNK, tma_bytes - static_cast<int64_t>(c) * SX_CHUNK) / 16);
+      const uint4* src = reinterpret_cast<const uint4*>(s.ring[st]) + tid;
       uint4 v[SX_VPT];
+      if (c + 1 < nch) {  // full chunk
 #pragma unroll
-      for (int k = 0; k < SX_VPT; ++k) {
-        const int vi = tid + k * SX_CONS;
-        v[k] = vi < nvec ? *reinterpret_cast<const uint4*>(s.ring[st] + vi * 16) : make_uint4(0, 0, 0, 0);
+        for (int k = 0; k < SX_VPT; ++k) v[k] = src[k * SX_CONS];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.empty[st]);
+        rm.add4(v);
+      } else {
+#pragma unroll
+        for (int k = 0; k < SX_VPT; ++k)
+          v[k] = tid + k * SX_CONS < last_nvec ? src[k * SX_CONS] : make_uint4(0, 0, 0, 0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.empty[st]);
+#pragma unroll
+        for (int k = 0; k < SX_VPT; ++k)
+          if (tid + k * SX_CONS < last_nvec) rm.add(v[k]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.empty[st]);
-#pragma unroll
-      for (int k = 0; k < SX_VPT; ++k)
-        if (tid + k * SX_CONS < nvec) rm.add(v[k]);
       if (++st == SX_STAGES) {
         st = 0;
         phase ^= 1u;
@@ -673,10 +731,7 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
     // bound: min over consumer warps of the warp's jth-largest thread maximum
     const uint32_t wb = warp_kth_largest<E::KEY_BITS>(rm.key(nonfinite), jth);
     if (lane == 0) s.warp_bound[warp] = wb;
-    if (tid == 0) {
-      s.count = 0;
-      s.qcount = 0;
-    }
+    if (tid == 0) s.count = 0;
     csync();
     uint32_t bound = 0xffffffffu;
 #pragma unroll
@@ -687,28 +742,45 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
     Filter<T> flt;
     flt.init(robust ? 0xffffffffu : bound);
 
-    // pass 2: candidates at or above the bound
+    // pass 2: vectors that reach the bound go to this warp's queue slots
+    // (ballot-ranked, no atomics); their elements are examined after the
+    // pass with every lane busy instead of one lane per warp
+    uint32_t qn_w = 0;  // warp-uniform count of queued vectors
+    uint4* const wq = s.qvec + warp * SX_QW;
+    uint32_t* const wqid = s.qid + warp * SX_QW;
+    const unsigned lt_mask = (1u << lane) - 1u;
     for (int c = 0; c < nch; ++c) {
       if (!mbar_wait(&s.full[st], phase)) s.timeout = 1;
-      const int nvec = static_cast<int>(min64(SX_CHUNK, tma_bytes - static_cast<int64_t>(c) * SX_CHUNK) / 16);
+      const int nvec = c + 1 < nch ? SX_CHUNK / 16 : last_nvec;
+      const uint4* src = reinterpret_cast<const uint4*>(s.ring[st]) + tid;
       uint4 v[SX_VPT];
+      const bool full_chunk = c + 1 < nch;
+      if (full_chunk) {
 #pragma unroll
-      for (int k = 0; k < SX_VPT; ++k) {
-        const int vi = tid + k * SX_CONS;
-        v[k] = vi < nvec ? *reinterpret_cast<const uint4*>(s.ring[st] + vi * 16) : make_uint4(0, 0, 0, 0);
+        for (int k = 0; k < SX_VPT; ++k) v[k] = src[k * SX_CONS];
+      } else {
+#pragma unroll
+        for (int k = 0; k < SX_VPT; ++k) v[k] = tid + k * SX_CONS < nvec ? src[k * SX_CONS] : make_uint4(0, 0, 0, 0);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.empty[st]);
+      // one test for the thread's four vectors (their element-wise maximum)
+      // before testing them one by one
+      bool any = true;
+      if (tid + (SX_VPT - 1) * SX_CONS < nvec) any = flt.pass(Filter<T>::merge4(v));
+      if (__any_sync(FULL, any)) {
 #pragma unroll
-      for (int k = 0; k < SX_VPT; ++k) {
-        const int vi = tid + k * SX_CONS;
-        if (vi < nvec && flt.pass(v[k])) {
-          // queue the vector; its elements are examined after the pass with
-          // every lane busy instead of one lane per warp
-          const int qp = atomicAdd(&s.qcount, 1);
-          if (qp < SX_QCAP) {
-            s.qvec[qp] = v[k];
-            s.qid[qp] = static_cast<uint32_t>(c * CHUNK_ELEMS + vi * VEC);
+        for (int k = 0; k < SX_VPT; ++k) {
+          const int vi = tid + k * SX_CONS;
+          const bool hit = any && vi < nvec && flt.pass(v[k]);
+          const unsigned bal = __ballot_sync(FULL, hit);
+          if (bal) {
+            const uint32_t pos = qn_w + __popc(bal & lt_mask);
+            if (hit && pos < SX_QW) {
+              wq[pos] = v[k];
+              wqid[pos] = static_cast<uint32_t>(c * CHUNK_ELEMS + vi * VEC);
+            }
+            qn_w += __popc(bal);
           }
         }
       }
@@ -717,11 +789,25 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
         phase ^= 1u;
       }
     }
+    if (lane == 0) s.qn_warp[warp] = static_cast<int>(qn_w);
     csync();
-    const int qn = s.qcount;
-    const bool q_over = qn > SX_QCAP;
+    bool q_over = false;
+    int qtot = 0;
+#pragma unroll
+    for (int w = 0; w < SX_CWARPS; ++w) {
+      q_over = q_over || s.qn_warp[w] > SX_QW;
+      qtot += min(s.qn_warp[w], SX_QW);
+    }
     if (!q_over) {
-      for (int i = tid; i < qn; i += SX_CONS) flt.emit(s, s.qvec[i], s.qid[i], p2over);
+      for (int i = tid; i < qtot; i += SX_CONS) {
+        // flat index -> (warp region, slot)
+        int w = 0, rem = i;
+        while (rem >= s.qn_warp[w]) {
+          rem -= s.qn_warp[w];
+          ++w;
+        }
+        flt.emit(s, s.qvec[w * SX_QW + rem], s.qid[w * SX_QW + rem], p2over);
+      }
       if (tail_id < a.V && tail_key >= bound && !robust) {
         const int pos = atomicAdd(&s.count, 1);
         if (pos < SX_CAP) s.cand[pos] = make_comp(tail_key, static_cast<uint32_t>(tail_id));

@@ -8,12 +8,14 @@
 // p = softmax(t / T) over the whole vocabulary of the current node's target
 // row (training-strategy paragraph: verification runs at temperature T).
 //
-// Per level the CTA streams the node's target row once with 16-byte loads for
-// the online max / sum-exp, gathers p at the <= |S| support tokens of the
-// node's draft row (the tail and the children), and thread 0 takes the
-// decisions.  Only the final level streams its row a second time, in token-id
-// order, for the bonus inverse CDF (w differs from p only at support tokens,
-// which are patched from a small id-sorted list).
+// Per level the CTA streams the node's target row once with 16-byte loads;
+// warp w owns a contiguous slice of the row and keeps the slice's maximum and
+// sum of exp2((t - max) * log2(e) / T), so the row normaliser and the mass of
+// every slice come out of the same pass.  The <= |S| support tokens of the
+// node's draft row (the tail and the children) are gathered for exact p, the
+// residual is formed in parallel, and thread 0 takes the <= K decisions.  For
+// the bonus token the slice masses locate the slice that holds it, and only
+// that slice is read again and scanned in token-id order.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -31,29 +33,34 @@ constexpr double MASS_MARGIN = 1e-6;
 
 struct VerShared {
   int32_t node_parent[SPEC_TREE_MAX_NODES];
-  int32_t kids[SPEC_TREE_MAX_SUPPORT];  // children of the current node (node indices)
-  int nkids;
-  float p_sup[SPEC_TREE_MAX_SUPPORT];   // p at support ranks of the node's draft row
-  float qt_sup[SPEC_TREE_MAX_SUPPORT];  // q~_T at support ranks (0 off the tail)
-  float w_sup[SPEC_TREE_MAX_SUPPORT];   // residual at support ranks
-  int32_t corr_id[SPEC_TREE_MAX_SUPPORT];  // id-sorted tokens whose w differs from p
+  int32_t kid_by_slot[SPEC_TREE_MAX_SUPPORT];  // child node of each sibling slot, -1 if pruned
+  float p_sup[SPEC_TREE_MAX_SUPPORT];          // p at support ranks of the node's draft row
+  float w_sup[SPEC_TREE_MAX_SUPPORT];          // residual at support ranks
+  float slice_m[VER_WARPS];                    // slice maximum (logit)
+  float slice_s[VER_WARPS];                    // slice sum of exp2((t - slice_m) * c)
+  float slice_corr[VER_WARPS];                 // per slice: sum over corrected tokens of (p - w)
+  float red[VER_WARPS];
+  int32_t corr_tok[SPEC_TREE_MAX_SUPPORT];     // corrected tokens inside the bonus slice
   float corr_w[SPEC_TREE_MAX_SUPPORT];
-  int ncorr;
-  float red_m[VER_WARPS];
-  float red_s[VER_WARPS];
   float scan_w[VER_WARPS];
-  float scan_x[VER_WARPS];
-  float chunk_total;
-  float target_rel;
-  double running;
-  float M;       // max logit of the row
-  double Zp;     // sum of exp2((t - M) * log2e / T)
+  int ncorr;
+  float M;       // row maximum
+  double Zp;     // row sum of exp2((t - M) * c)
   double Zr;     // residual mass
   int accepted;  // accepted child node or -1
-  int residual;  // probe rejected: tail residual in force
   int bonus;
   int bonus_last;
+  int bonus_slice;
+  float bonus_target;  // target mass relative to the start of the bonus slice
 };
+
+// 2^x on the special-function unit (PTX ex2.approx.ftz: a few ulp; results
+// below 2^-126 flush to zero, which changes a row sum by at most 2^-126).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 template <typename T>
 struct VElem;
@@ -62,10 +69,19 @@ struct VElem<__nv_bfloat16> {
   static constexpr int VEC = 8, ES = 2;
   __device__ static float get(const uint4& v, int j) {
     const uint32_t w = (j < 2) ? v.x : (j < 4) ? v.y : (j < 6) ? v.z : v.w;
-    return __uint_as_float(((w >> (16 * (j & 1))) & 0xffffu) << 16);
+    return __uint_as_float((j & 1) ? (w & 0xffff0000u) : (w << 16));
   }
   __device__ static float load(const uint8_t* row, int v) {
     return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(row)[v]) << 16);
+  }
+  // maximum of the 8 elements, NaN-propagating
+  __device__ static float vmax(const uint4& v) {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
+    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
+    const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&v.w);
+    const __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+    return __bfloat162float(__hmax_nan(m.x, m.y));
   }
 };
 template <>
@@ -75,323 +91,227 @@ struct VElem<float> {
     return __uint_as_float((j == 0) ? v.x : (j == 1) ? v.y : (j == 2) ? v.z : v.w);
   }
   __device__ static float load(const uint8_t* row, int v) { return reinterpret_cast<const float*>(row)[v]; }
+  __device__ static float vmax(const uint4& v) {
+    const float a = __uint_as_float(v.x), b = __uint_as_float(v.y), c = __uint_as_float(v.z),
+                d = __uint_as_float(v.w);
+    const float m = fmaxf(fmaxf(a, b), fmaxf(c, d));
+    return (a != a || b != b || c != c || d != d) ? __int_as_float(0x7fffffff) : m;
+  }
 };
 
-// Block-wide max and sum-exp of one row: M = max t, Zp = sum exp2((t - M) * c),
-// c = log2(e) / T.  Online per thread (rescale when the running max grows),
-// compensated float32 accumulation per thread, float64 across threads.
+// Slice of warp w: vectors [w * per, min((w + 1) * per, nvec)); the scalar
+// tail (V not a multiple of the vector width) belongs to the last warp.
+struct Slice {
+  int v0, v1;
+  __device__ Slice(int w, int nvec) {
+    const int per = (nvec + VER_WARPS - 1) / VER_WARPS;
+    v0 = min(w * per, nvec);
+    v1 = min(v0 + per, nvec);
+  }
+};
+
+__device__ __forceinline__ int slice_of_token(int v, int nvec, int vec) {
+  const int per = (nvec + VER_WARPS - 1) / VER_WARPS;
+  if (v >= nvec * vec || per == 0) return VER_WARPS - 1;
+  return min((v / vec) / per, VER_WARPS - 1);
+}
+
+// Row statistics: per-slice maximum and sum of exp2((t - m) * c), the row
+// maximum M and Zp = sum exp2((t - M) * c), c = log2(e) / T.  Per lane:
+// online maximum with rescaling, compensated float32 sums of 8-element vector
+// sums; lanes combine in float32, slices in float64.
 template <typename T>
 __device__ void row_stats(VerShared& s, const uint8_t* row, int V, float c, bool& nonfinite) {
   using E = VElem<T>;
   constexpr int VEC = E::VEC;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nvec = static_cast<int>((static_cast<int64_t>(V) * E::ES) / 16);
+  const Slice sl(warp, nvec);
   float m_run = -INFINITY, s_run = 0.0f, comp = 0.0f;
-  auto consume = [&](const float* x, int n) {
-    float vmax = -INFINITY;
-    for (int j = 0; j < n; ++j) vmax = fmaxf(vmax, x[j]);
-    for (int j = 0; j < n; ++j)
-      if (!(x[j] == x[j]) || x[j] == INFINITY) nonfinite = true;
-    if (vmax == -INFINITY || !(vmax == vmax)) return;
-    if (vmax > m_run) {
-      const float f = exp2f((m_run - vmax) * c);
-      s_run *= f;
-      comp *= f;
-      m_run = vmax;
+  auto rescale = [&](float vm) {
+    const float f = ex2((m_run - vm) * c);
+    s_run *= f;
+    comp *= f;
+    m_run = vm;
+  };
+  auto consume = [&](const uint4& v) {
+    const float vm = E::vmax(v);
+    if (!(vm < INFINITY)) {  // NaN or +inf in the row
+      nonfinite = true;
+      return;
     }
+    if (vm == -INFINITY) return;
+    if (vm > m_run) rescale(vm);
     float vs = 0.0f;
-    for (int j = 0; j < n; ++j) vs += exp2f((x[j] - m_run) * c);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) vs += ex2((E::get(v, j) - m_run) * c);
     const float y = vs - comp;
     const float t = s_run + y;
     comp = (t - s_run) - y;
     s_run = t;
   };
   const uint4* rv = reinterpret_cast<const uint4*>(row);
-  int i = tid;
-  for (; i + 3 * VER_THREADS < nvec; i += 4 * VER_THREADS) {
+  int i = sl.v0 + lane;
+  for (; i + 96 < sl.v1; i += 128) {
     uint4 v[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = ldg_stream(rv + i + u * VER_THREADS);
+    for (int u = 0; u < 4; ++u) v[u] = ldg_stream(rv + i + 32 * u);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float x[VEC];
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) x[j] = E::get(v[u], j);
-      consume(x, VEC);
+    for (int u = 0; u < 4; ++u) consume(v[u]);
+  }
+  for (; i < sl.v1; i += 32) consume(ldg_stream(rv + i));
+  if (warp == VER_WARPS - 1) {
+    const int tk = nvec * VEC + lane;
+    if (tk < V) {
+      const float x = E::load(row, tk);
+      if (!(x < INFINITY)) nonfinite = true;
+      if (x > -INFINITY && x < INFINITY) {
+        if (x > m_run) rescale(x);
+        s_run += ex2((x - m_run) * c);
+      }
     }
   }
-  for (; i < nvec; i += VER_THREADS) {
-    const uint4 v = ldg_stream(rv + i);
-    float x[VEC];
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) x[j] = E::get(v, j);
-    consume(x, VEC);
-  }
-  const int tail = nvec * VEC + tid;
-  if (tail < V) {
-    float x[1] = {E::load(row, tail)};
-    consume(x, 1);
-  }
-  // block max
+  // combine lanes: slice maximum and sum relative to it
   float m = m_run;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
-  if (lane == 0) s.red_m[warp] = m;
-  __syncthreads();
-  float M = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < VER_WARPS; ++w) M = fmaxf(M, s.red_m[w]);
-  float part = (m_run == -INFINITY) ? 0.0f : s_run * exp2f((m_run - M) * c);
+  float part = (m_run == -INFINITY) ? 0.0f : (s_run - comp) * ex2((m_run - m) * c);
   part = warp_sum(part);
-  if (lane == 0) s.red_s[warp] = part;
+  if (lane == 0) {
+    s.slice_m[warp] = m;
+    s.slice_s[warp] = part;
+  }
   __syncthreads();
   if (tid == 0) {
+    float M = -INFINITY;
+    for (int w = 0; w < VER_WARPS; ++w) M = fmaxf(M, s.slice_m[w]);
     double z = 0.0;
-    for (int w = 0; w < VER_WARPS; ++w) z += s.red_s[w];
+    for (int w = 0; w < VER_WARPS; ++w)
+      if (s.slice_m[w] > -INFINITY) z += static_cast<double>(s.slice_s[w]) * ex2((s.slice_m[w] - M) * c);
     s.M = M;
     s.Zp = z;
   }
   __syncthreads();
 }
 
-// Bonus token: first token v in id order with target < sum_{v' <= v} w(v'),
-// w = p except at the id-sorted corrections.  Result in s.bonus.  Per chunk
-// of VER_THREADS * VEC tokens: float32 per-thread sums and scans, relative to
-// the chunk start (the target is rebased per chunk in float64 by thread 0).
-template <typename T>
-__device__ void bonus_scan(VerShared& s, const uint8_t* row, int V, float c, double target, uint32_t* margins) {
-  using E = VElem<T>;
-  constexpr int VEC = E::VEC;
-  constexpr int CH = VER_THREADS * VEC;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float M = s.M;
-  const float invZ = static_cast<float>(1.0 / s.Zp);
-  const int ncorr = s.ncorr;
-  const int nvec_full = static_cast<int>((static_cast<int64_t>(V) * E::ES) / 16);
-  int last_pos = -1;
-  if (tid == 0) {
-    s.bonus = -1;
-    s.bonus_last = -1;
-    s.running = 0.0;
-    s.target_rel = static_cast<float>(target);
-  }
-  __syncthreads();
-  for (int base = 0; base < V; base += CH) {
-    const int v0 = base + tid * VEC;
-    float w[VEC];
-    if (v0 / VEC < nvec_full) {
-      const uint4 v = ldg_stream(row + static_cast<int64_t>(v0) * E::ES);
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) w[j] = E::get(v, j);
-    } else {
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) w[j] = (v0 + j < V) ? E::load(row, v0 + j) : -INFINITY;
-    }
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) w[j] = (w[j] == -INFINITY) ? 0.0f : exp2f((w[j] - M) * c) * invZ;
-    // patch corrected tokens in [v0, v0 + VEC)
-    if (ncorr > 0 && v0 < V) {
-      int lo = 0, hi = ncorr;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (s.corr_id[mid] < v0) lo = mid + 1;
-        else hi = mid;
-      }
-      for (int k = lo; k < ncorr && s.corr_id[k] < v0 + VEC; ++k) {
-        const int j = s.corr_id[k] - v0;
-#pragma unroll
-        for (int jj = 0; jj < VEC; ++jj)
-          if (jj == j) w[jj] = s.corr_w[k];
-      }
-    }
-    float ts = 0.0f;
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) {
-      ts += w[j];
-      if (w[j] > 0.0f && v0 + j < V) last_pos = v0 + j;
-    }
-    float incl = ts;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float t = __shfl_up_sync(FULL, incl, o);
-      if (lane >= o) incl += t;
-    }
-    if (lane == 31) s.scan_w[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      const float x = s.scan_w[lane];
-      float wi = x;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float t = __shfl_up_sync(FULL, wi, o);
-        if (lane >= o) wi += t;
-      }
-      s.scan_x[lane] = wi - x;
-      if (lane == 31) s.chunk_total = wi;
-    }
-    __syncthreads();
-    const float before = s.scan_x[warp] + (incl - ts);
-    const float after = before + ts;
-    const float tr = s.target_rel;
-    if (before <= tr && tr < after) {
-      // the thread intervals [before, after) are disjoint: at most one thread gets here
-      float acc = before;
-      int pick = -1, last = -1;
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) {
-        if (pick < 0) {
-          if (w[j] > 0.0f) last = v0 + j;
-          const float nx = acc + w[j];
-          if (tr < nx) {
-            pick = v0 + j;
-            if (margins && (tr - acc < MASS_MARGIN || nx - tr < MASS_MARGIN)) atomicAdd(margins + 1, 1u);
-          }
-          acc = nx;
-        }
-      }
-      s.bonus = pick >= 0 ? pick : last;
-    }
-    __syncthreads();
-    if (s.bonus >= 0) break;
-    if (tid == 0) {
-      s.running += s.chunk_total;
-      s.target_rel = static_cast<float>(target - s.running);
-    }
-    __syncthreads();
-  }
-  if (s.bonus < 0) atomicMax(&s.bonus_last, last_pos);
-  __syncthreads();
-  if (tid == 0 && s.bonus < 0) s.bonus = s.bonus_last;
-  __syncthreads();
+// Support rank of the child in sibling slot `slot` (DET 0..m-1 -> ranks
+// 0..m-1, PROBE m -> the probe's rank, FILL -> next tail ranks skipping the probe).
+__device__ __forceinline__ int rank_of_slot(int slot, int m, int pp) {
+  if (slot < m) return slot;
+  if (slot == m && pp >= 0) return pp;
+  int r = slot - (pp >= 0 ? 1 : 0);
+  if (pp >= 0 && r >= pp) ++r;
+  return r;
 }
 
 template <typename T>
 __global__ void __launch_bounds__(VER_THREADS, 1) verify_kernel(VerifyLaunch L) {
   using E = VElem<T>;
+  constexpr int VEC = E::VEC;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   VerShared& s = *reinterpret_cast<VerShared*>(smem_raw);
-  const int b = blockIdx.x, tid = threadIdx.x;
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const spec_tree_t& t = L.tree;
-  const int m = L.p.m, D = L.p.depth, K = L.p.K, S = L.S;
+  const int m = L.p.m, D = L.p.depth, K = L.p.K, S = L.S, V = L.V;
   const float Tmp = L.p.temperature;
   const float c = LOG2E / Tmp;
   const int64_t nb = static_cast<int64_t>(b) * t.max_nodes;
-  const int n_nodes = t.n_nodes[b];
+  const int n_nodes = min(t.n_nodes[b], t.max_nodes);
   for (int i = tid; i < n_nodes; i += VER_THREADS) s.node_parent[i] = t.node_parent[nb + i];
   const int64_t row_bytes = L.row_stride * E::ES;
   const uint8_t* tgt = static_cast<const uint8_t*>(L.target);
+  const int nvec = static_cast<int>((static_cast<int64_t>(V) * E::ES) / 16);
   bool nonfinite = false;
   int node = 0, level = 0;
+  int32_t* ot = L.out_tok + static_cast<int64_t>(b) * (D + 1);
+  int32_t* on = L.out_node + static_cast<int64_t>(b) * (D + 1);
   __syncthreads();
   while (true) {
     const uint8_t* row = tgt + (nb + node) * row_bytes;
-    row_stats<T>(s, row, L.V, c, nonfinite);
-    // children of the node, verification order: probe first, then by slot
-    if (tid == 0) s.nkids = 0;
-    __syncthreads();
-    for (int i = tid + 1; i < n_nodes; i += VER_THREADS)
-      if (s.node_parent[i] == node) {
-        const int k = atomicAdd(&s.nkids, 1);
-        if (k < SPEC_TREE_MAX_SUPPORT) s.kids[k] = i;
-      }
-    __syncthreads();
-    // a node at depth D is a leaf (also bounds the walk for malformed trees)
-    const int nk = level >= D ? 0 : min(s.nkids, SPEC_TREE_MAX_SUPPORT);
+    if (tid < K) s.kid_by_slot[tid] = -1;
     if (tid == 0) {
-      // insertion sort: probe first, then slot ascending
-      for (int i = 1; i < nk; ++i) {
-        const int x = s.kids[i];
-        const int kx = t.node_kind[nb + x] == SPEC_TREE_PROBE ? -1 : t.node_slot[nb + x];
-        int j = i - 1;
-        while (j >= 0) {
-          const int y = s.kids[j];
-          const int ky = t.node_kind[nb + y] == SPEC_TREE_PROBE ? -1 : t.node_slot[nb + y];
-          if (ky <= kx) break;
-          s.kids[j + 1] = y;
-          --j;
-        }
-        s.kids[j + 1] = x;
-      }
       s.accepted = -1;
-      s.residual = 0;
-      s.ncorr = 0;
       s.Zr = 1.0;
+      s.ncorr = 0;
     }
-    __syncthreads();
+    row_stats<T>(s, row, V, c, nonfinite);
+    // children of the node by sibling slot; a node at depth D is a leaf
+    // (which also bounds the walk for malformed trees)
+    int nk = 0;
+    if (level < D) {
+      for (int i = tid + 1; i < n_nodes; i += VER_THREADS)
+        if (s.node_parent[i] == node) {
+          const int slot = t.node_slot[nb + i];
+          if (slot >= 0 && slot < K) s.kid_by_slot[slot] = i;
+        }
+      __syncthreads();
+      for (int k = 0; k < K; ++k) nk += s.kid_by_slot[k] >= 0;
+    }
     const float M = s.M;
     const float invZp = static_cast<float>(1.0 / s.Zp);
     int64_t srow = -1;
     if (nk > 0) {
       srow = static_cast<int64_t>(b) * t.n_rows + t.node_exp_row[nb + node];
+      const int pp = t.probe_pos[srow];
+      const int probe_node = (pp >= 0) ? s.kid_by_slot[m] : -1;
+      const bool residual = probe_node >= 0;  // the tail residual applies iff the probe child survived
       const float zT = t.sup_zT[srow];
+      float mn = 0.0f;
       if (tid < S) {
         const int v = t.sup_id[srow * t.sup_stride + tid];
-        const float x = E::load(row, v);
-        const float p = expf((x - M) / Tmp) * invZp;
-        s.p_sup[tid] = p;
+        const float p = expf((E::load(row, v) - M) / Tmp) * invZp;
         const float qt = (tid >= m && zT > 0.0f) ? t.sup_qT[srow * t.sup_stride + tid] / zT : 0.0f;
-        s.qt_sup[tid] = qt;
-        s.w_sup[tid] = p;
+        s.p_sup[tid] = p;
+        s.w_sup[tid] = (residual && tid >= m) ? fmaxf(0.0f, p - qt) : p;
+        mn = (residual && tid >= m) ? fminf(p, qt) : 0.0f;
       }
+      mn = warp_sum(mn);
+      if (lane == 0) s.red[warp] = mn;
       __syncthreads();
       if (tid == 0) {
         const float* uv = L.u_verify + (static_cast<int64_t>(b) * D + level) * K;
-        const int pp = t.probe_pos[srow];
-        int j = 0, i0 = 0;
+        int j = 0;
         double Zr = 1.0;
-        auto rank_of = [&](int node_i) -> int {
-          const int kind = t.node_kind[nb + node_i], slot = t.node_slot[nb + node_i];
-          if (kind == SPEC_TREE_DET) return slot;
-          if (kind == SPEC_TREE_PROBE) return pp;
-          int r = m + slot - m - (pp >= 0 ? 1 : 0);
-          if (pp >= 0 && r >= pp) ++r;
-          return r;
-        };
-        if (nk > 0 && t.node_kind[nb + s.kids[0]] == SPEC_TREE_PROBE) {
-          const int r = pp;
-          const double p = s.p_sup[r], qt = s.qt_sup[r];
+        bool empty = false;
+        if (probe_node >= 0) {
+          const double p = s.p_sup[pp];
+          const double qt = static_cast<double>(t.sup_qT[srow * t.sup_stride + pp]) / zT;
           const float u = uv[0];
           if (L.margins && fabs(u * qt - p) < MASS_MARGIN) atomicAdd(L.margins, 1u);
           if (static_cast<double>(u) * qt < p) {
-            s.accepted = s.kids[0];
+            s.accepted = probe_node;
           } else {
-            // residual max(0, p - q~) on the tail, mass 1 - sum_tail min(p, q~)
             double smin = 0.0;
-            for (int k = m; k < S; ++k) {
-              const float pk = s.p_sup[k], qk = s.qt_sup[k];
-              smin += fminf(pk, qk);
-              s.w_sup[k] = fmaxf(0.0f, pk - qk);
-            }
+            for (int w = 0; w < (S + 31) / 32; ++w) smin += s.red[w];
             Zr = 1.0 - smin;
-            s.residual = 1;
             j = 1;
           }
-          i0 = 1;
         }
         if (s.accepted < 0) {
-          bool empty = false;
-          for (int i = i0; i < nk; ++i, ++j) {
+          for (int slot = 0; slot < K; ++slot) {
+            const int kid = s.kid_by_slot[slot];
+            if (kid < 0 || kid == probe_node) continue;
             if (Zr <= 0.0) {
               empty = true;
               break;
             }
-            const int r = rank_of(s.kids[i]);
+            const int r = rank_of_slot(slot, m, pp);
             const double w = s.w_sup[r];
             const float u = uv[j];
             if (L.margins && fabs(u * Zr - w) < MASS_MARGIN) atomicAdd(L.margins, 1u);
             if (static_cast<double>(u) * Zr < w) {
-              s.accepted = s.kids[i];
+              s.accepted = kid;
               break;
             }
             Zr -= w;
             s.w_sup[r] = 0.0f;
+            ++j;
           }
           if (s.accepted < 0 && !empty && Zr <= 0.0) empty = true;
           if (empty) {
-            // rounding emptied the residual: bonus from p
+            // rounding emptied the residual: the bonus is drawn from p
             set_status(L.status, SPEC_TREE_S_RESIDUAL_EMPTY);
             for (int k = 0; k < S; ++k) s.w_sup[k] = s.p_sup[k];
-            s.residual = 0;
             Zr = 1.0;
           }
         }
@@ -402,38 +322,142 @@ __global__ void __launch_bounds__(VER_THREADS, 1) verify_kernel(VerifyLaunch L) 
     const int acc = s.accepted;
     if (acc >= 0) {
       if (tid == 0) {
-        L.out_tok[static_cast<int64_t>(b) * (D + 1) + level] = t.node_token[nb + acc];
-        L.out_node[static_cast<int64_t>(b) * (D + 1) + level] = acc;
+        ot[level] = t.node_token[nb + acc];
+        on[level] = acc;
       }
       node = acc;
       ++level;
       __syncthreads();
       continue;
     }
-    // bonus: corrections are the support tokens whose w differs from p
-    if (nk > 0) {
-      if (tid < S) {
-        const bool corr = s.w_sup[tid] != s.p_sup[tid];
+    // ------------------------------------------------------------- bonus ---
+    // w = p except at support tokens whose residual differs; slice masses of w
+    if (tid < VER_WARPS) s.slice_corr[tid] = 0.0f;
+    __syncthreads();
+    if (nk > 0 && tid < S) {
+      const float d = s.p_sup[tid] - s.w_sup[tid];
+      if (d != 0.0f)
+        atomicAdd(&s.slice_corr[slice_of_token(t.sup_id[srow * t.sup_stride + tid], nvec, VEC)], d);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const double target = static_cast<double>(L.u_bonus[b]) * s.Zr;
+      double acc_mass = 0.0, before = 0.0, before_last = 0.0;
+      int pick = -1, last = -1;
+      for (int w = 0; w < VER_WARPS; ++w) {
+        double mass = s.slice_m[w] > -INFINITY
+                          ? static_cast<double>(s.slice_s[w]) * ex2((s.slice_m[w] - M) * c) / s.Zp
+                          : 0.0;
+        mass -= s.slice_corr[w];
+        if (mass > 0.0) {
+          last = w;
+          before_last = acc_mass;
+        }
+        if (pick < 0 && mass > 0.0 && target < acc_mass + mass) {
+          pick = w;
+          before = acc_mass;
+        }
+        acc_mass += mass;
+      }
+      if (pick < 0) {  // rounding left the target past the total: the last slice with mass
+        pick = last < 0 ? VER_WARPS - 1 : last;
+        before = before_last;
+      }
+      s.bonus_slice = pick;
+      s.bonus_target = static_cast<float>(target - before);
+      s.bonus = -1;
+      s.bonus_last = -1;
+    }
+    __syncthreads();
+    const int bs = s.bonus_slice;
+    const Slice sl(bs, nvec);
+    const int t0 = sl.v0 * VEC;
+    const int t1 = (bs == VER_WARPS - 1) ? V : sl.v1 * VEC;
+    // corrected tokens inside the slice
+    if (nk > 0 && tid < S) {
+      const float wv = s.w_sup[tid];
+      if (wv != s.p_sup[tid]) {
         const int v = t.sup_id[srow * t.sup_stride + tid];
-        if (corr) {
-          int r = 0;
-          for (int k = 0; k < S; ++k) {
-            const bool ck = s.w_sup[k] != s.p_sup[k];
-            if (ck && t.sup_id[srow * t.sup_stride + k] < v) ++r;
-          }
-          s.corr_id[r] = v;
-          s.corr_w[r] = s.w_sup[tid];
-          atomicAdd(&s.ncorr, 1);
+        if (v >= t0 && v < t1) {
+          const int k = atomicAdd(&s.ncorr, 1);
+          s.corr_tok[k] = v;
+          s.corr_w[k] = wv;
         }
       }
+    }
+    __syncthreads();
+    // scan the slice in id order: thread i handles tokens [base + VEC * i, + VEC)
+    {
+      const int ncorr = s.ncorr;
+      const float invZ = static_cast<float>(1.0 / s.Zp);
+      const float tr = s.bonus_target;
+      float base_run = 0.0f;
+      int last_pos = -1;
+      for (int cb = t0; cb < t1; cb += VER_THREADS * VEC) {
+        const int v0 = cb + tid * VEC;
+        float w[VEC];
+        if (v0 + VEC <= t1 && v0 / VEC < nvec) {
+          const uint4 v = ldg_stream(row + static_cast<int64_t>(v0) * E::ES);
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) w[j] = E::get(v, j);
+        } else {
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) w[j] = (v0 + j < t1) ? E::load(row, v0 + j) : -INFINITY;
+        }
+        float ts = 0.0f;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+          w[j] = (w[j] == -INFINITY) ? 0.0f : ex2((w[j] - M) * c) * invZ;
+          for (int k = 0; k < ncorr; ++k)
+            if (s.corr_tok[k] == v0 + j) w[j] = s.corr_w[k];
+          ts += w[j];
+          if (w[j] > 0.0f) last_pos = v0 + j;
+        }
+        float incl = ts;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float x = __shfl_up_sync(FULL, incl, o);
+          if (lane >= o) incl += x;
+        }
+        if (lane == 31) s.scan_w[warp] = incl;
+        __syncthreads();
+        float wbefore = 0.0f, total = 0.0f;
+        for (int k = 0; k < VER_WARPS; ++k) {
+          const float x = s.scan_w[k];
+          if (k < warp) wbefore += x;
+          total += x;
+        }
+        const float before = base_run + wbefore + incl - ts;
+        if (ts > 0.0f && before <= tr && tr < before + ts) {
+          // the thread intervals [before, before + ts) are disjoint: one thread at most
+          float acc = before;
+          int pick = -1, lastp = -1;
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) {
+            if (pick < 0) {
+              if (w[j] > 0.0f) lastp = v0 + j;
+              const float nx = acc + w[j];
+              if (tr < nx) {
+                pick = v0 + j;
+                if (L.margins && (tr - acc < MASS_MARGIN || nx - tr < MASS_MARGIN)) atomicAdd(L.margins + 1, 1u);
+              }
+              acc = nx;
+            }
+          }
+          s.bonus = pick >= 0 ? pick : lastp;
+        }
+        base_run += total;
+        __syncthreads();
+        if (s.bonus >= 0) break;
+      }
+      if (s.bonus < 0 && last_pos >= 0) atomicMax(&s.bonus_last, last_pos);
       __syncthreads();
     }
-    const double target = static_cast<double>(L.u_bonus[b]) * s.Zr;
-    bonus_scan<T>(s, row, L.V, c, target, L.margins);
     if (tid == 0) {
-      int32_t* ot = L.out_tok + static_cast<int64_t>(b) * (D + 1);
-      int32_t* on = L.out_node + static_cast<int64_t>(b) * (D + 1);
-      ot[level] = s.bonus;
+      int bonus = s.bonus;
+      if (bonus < 0) bonus = s.bonus_last;
+      if (bonus < 0) bonus = t1 - 1;
+      ot[level] = bonus;
       on[level] = -1;
       for (int k = level + 1; k <= D; ++k) {
         ot[k] = -1;
