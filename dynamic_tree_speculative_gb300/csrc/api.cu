@@ -187,6 +187,8 @@ int spec_tree_verify(const spec_tree_params* p, int B, int V, int dtype, const v
   L.out_node = out_node;
   L.margins = margins;
   L.status = status;
+  L.num_sms = num_sms_of_current_device();
+  if (L.num_sms <= 0) return SPEC_TREE_E_CUDA;
   return st::launch_verify(L, as_stream(stream)) == cudaSuccess ? SPEC_TREE_OK : SPEC_TREE_E_CUDA;
 }
 

@@ -50,6 +50,7 @@ struct VerifyLaunch {
   int32_t* out_node;
   uint32_t* margins;
   uint32_t* status;
+  int num_sms;
 };
 
 size_t select_expand_smem_bytes();

@@ -1,4 +1,5 @@
-// Layer-by-layer verification of built trees (sm_103a): one CTA per tree.
+// Layer-by-layer verification of built trees (sm_103a): one thread-block
+// cluster of C CTAs per tree.
 //
 // RheoSampling notes, Method / Key design 3: the probe is tested first with
 // min(1, p/q~_T); on rejection the residual w = max(0, p - q~_T) (w = p off
@@ -8,14 +9,19 @@
 // p = softmax(t / T) over the whole vocabulary of the current node's target
 // row (training-strategy paragraph: verification runs at temperature T).
 //
-// Per level the CTA streams the node's target row once with 16-byte loads;
-// warp w owns a contiguous slice of the row and keeps the slice's maximum and
-// sum of exp2((t - max) * log2(e) / T), so the row normaliser and the mass of
-// every slice come out of the same pass.  The <= |S| support tokens of the
-// node's draft row (the tail and the children) are gathered for exact p, the
-// residual is formed in parallel, and thread 0 takes the <= K decisions.  For
-// the bonus token the slice masses locate the slice that holds it, and only
-// that slice is read again and scanned in token-id order.
+// The walk is sequential in depth, so the latency of one level is what
+// matters: every level's target row is split over the C CTAs of the tree's
+// cluster (C chosen so that the whole batch fits in one wave).  Each of the
+// 32*C warps owns a contiguous slice of the row and keeps the slice's maximum
+// and sum of exp2((t - max) * log2(e) / T).  After a cluster barrier the
+// leader CTA reads the slice statistics of all CTAs through distributed
+// shared memory, forms the row normaliser, gathers exact p at the <= |S|
+// support tokens of the node's draft row, forms the residual in parallel and
+// lets thread 0 take the <= K decisions; a second cluster barrier publishes
+// the outcome.  For the bonus token the slice masses locate the slice that
+// holds it, and the leader reads only that slice again, scanning it in
+// token-id order.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -24,30 +30,41 @@
 #include "st_common.cuh"
 #include "st_kernels.h"
 
+namespace cg = cooperative_groups;
+
 namespace st {
 
 constexpr int VER_THREADS = 1024;
 constexpr int VER_WARPS = VER_THREADS / 32;
+constexpr int VER_MAX_CLUSTER = 8;
+constexpr int VER_MAX_SLICES = VER_WARPS * VER_MAX_CLUSTER;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr double MASS_MARGIN = 1e-6;
 
 struct VerShared {
-  int32_t node_parent[SPEC_TREE_MAX_NODES];
+  int32_t nd_parent[SPEC_TREE_MAX_NODES];      // leader: the tree's node arrays
+  int32_t nd_slot[SPEC_TREE_MAX_NODES];
+  int32_t nd_exp_row[SPEC_TREE_MAX_NODES];
+  int32_t nd_token[SPEC_TREE_MAX_NODES];
   int32_t kid_by_slot[SPEC_TREE_MAX_SUPPORT];  // child node of each sibling slot, -1 if pruned
   float p_sup[SPEC_TREE_MAX_SUPPORT];          // p at support ranks of the node's draft row
+  float qt_sup[SPEC_TREE_MAX_SUPPORT];         // q~_T at support ranks (0 off the tail)
   float w_sup[SPEC_TREE_MAX_SUPPORT];          // residual at support ranks
-  float slice_m[VER_WARPS];                    // slice maximum (logit)
-  float slice_s[VER_WARPS];                    // slice sum of exp2((t - slice_m) * c)
-  float slice_corr[VER_WARPS];                 // per slice: sum over corrected tokens of (p - w)
+  float slice_m[VER_WARPS];                    // this CTA's slices: maximum logit
+  float slice_s[VER_WARPS];                    //   and sum of exp2((t - slice max) * c)
+  float all_m[VER_MAX_SLICES];                 // leader: every slice of the cluster
+  float all_s[VER_MAX_SLICES];
+  float slice_corr[VER_MAX_SLICES];            // leader: per slice, sum over corrected tokens of (p - w)
   float red[VER_WARPS];
   int32_t corr_tok[SPEC_TREE_MAX_SUPPORT];     // corrected tokens inside the bonus slice
   float corr_w[SPEC_TREE_MAX_SUPPORT];
   float scan_w[VER_WARPS];
   int ncorr;
   float M;       // row maximum
-  double Zp;     // row sum of exp2((t - M) * c)
-  double Zr;     // residual mass
-  int accepted;  // accepted child node or -1
+  float invZp;   // 1 / sum of exp2((t - M) * c) over the row
+  float Zr;      // residual mass
+  int accepted;  // leader's decision of the level: accepted child node, or -1
+  int nkids;     // children of the current node
   int bonus;
   int bonus_last;
   int bonus_slice;
@@ -99,34 +116,33 @@ struct VElem<float> {
   }
 };
 
-// Slice of warp w: vectors [w * per, min((w + 1) * per, nvec)); the scalar
-// tail (V not a multiple of the vector width) belongs to the last warp.
+// Slice g of ns: vectors [g * per, min((g + 1) * per, nvec)); the scalar tail
+// (V not a multiple of the vector width) belongs to the last slice.
 struct Slice {
   int v0, v1;
-  __device__ Slice(int w, int nvec) {
-    const int per = (nvec + VER_WARPS - 1) / VER_WARPS;
-    v0 = min(w * per, nvec);
+  __device__ Slice(int g, int ns, int nvec) {
+    const int per = (nvec + ns - 1) / ns;
+    v0 = min(g * per, nvec);
     v1 = min(v0 + per, nvec);
   }
 };
 
-__device__ __forceinline__ int slice_of_token(int v, int nvec, int vec) {
-  const int per = (nvec + VER_WARPS - 1) / VER_WARPS;
-  if (v >= nvec * vec || per == 0) return VER_WARPS - 1;
-  return min((v / vec) / per, VER_WARPS - 1);
+__device__ __forceinline__ int slice_of_token(int v, int ns, int nvec, int vec) {
+  const int per = (nvec + ns - 1) / ns;
+  if (v >= nvec * vec || per == 0) return ns - 1;
+  return min((v / vec) / per, ns - 1);
 }
 
-// Row statistics: per-slice maximum and sum of exp2((t - m) * c), the row
-// maximum M and Zp = sum exp2((t - M) * c), c = log2(e) / T.  Per lane:
-// online maximum with rescaling, compensated float32 sums of 8-element vector
-// sums; lanes combine in float32, slices in float64.
+// Statistics of this warp's slice: maximum and sum of exp2((t - max) * c),
+// c = log2(e) / T.  Per lane: online maximum with rescaling, compensated
+// float32 sums of vector sums; lanes combine in float32.
 template <typename T>
-__device__ void row_stats(VerShared& s, const uint8_t* row, int V, float c, bool& nonfinite) {
+__device__ void slice_stats(VerShared& s, const uint8_t* row, int V, int g, int ns, float c, bool& nonfinite) {
   using E = VElem<T>;
   constexpr int VEC = E::VEC;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nvec = static_cast<int>((static_cast<int64_t>(V) * E::ES) / 16);
-  const Slice sl(warp, nvec);
+  const Slice sl(g, ns, nvec);
   float m_run = -INFINITY, s_run = 0.0f, comp = 0.0f;
   auto rescale = [&](float vm) {
     const float f = ex2((m_run - vm) * c);
@@ -152,6 +168,13 @@ __device__ void row_stats(VerShared& s, const uint8_t* row, int V, float c, bool
   };
   const uint4* rv = reinterpret_cast<const uint4*>(row);
   int i = sl.v0 + lane;
+  for (; i + 224 < sl.v1; i += 256) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = ldg_stream(rv + i + 32 * u);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) consume(v[u]);
+  }
   for (; i + 96 < sl.v1; i += 128) {
     uint4 v[4];
 #pragma unroll
@@ -160,7 +183,7 @@ __device__ void row_stats(VerShared& s, const uint8_t* row, int V, float c, bool
     for (int u = 0; u < 4; ++u) consume(v[u]);
   }
   for (; i < sl.v1; i += 32) consume(ldg_stream(rv + i));
-  if (warp == VER_WARPS - 1) {
+  if (g == ns - 1) {
     const int tk = nvec * VEC + lane;
     if (tk < V) {
       const float x = E::load(row, tk);
@@ -171,7 +194,6 @@ __device__ void row_stats(VerShared& s, const uint8_t* row, int V, float c, bool
       }
     }
   }
-  // combine lanes: slice maximum and sum relative to it
   float m = m_run;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
@@ -181,17 +203,6 @@ __device__ void row_stats(VerShared& s, const uint8_t* row, int V, float c, bool
     s.slice_m[warp] = m;
     s.slice_s[warp] = part;
   }
-  __syncthreads();
-  if (tid == 0) {
-    float M = -INFINITY;
-    for (int w = 0; w < VER_WARPS; ++w) M = fmaxf(M, s.slice_m[w]);
-    double z = 0.0;
-    for (int w = 0; w < VER_WARPS; ++w)
-      if (s.slice_m[w] > -INFINITY) z += static_cast<double>(s.slice_s[w]) * ex2((s.slice_m[w] - M) * c);
-    s.M = M;
-    s.Zp = z;
-  }
-  __syncthreads();
 }
 
 // Support rank of the child in sibling slot `slot` (DET 0..m-1 -> ranks
@@ -204,192 +215,265 @@ __device__ __forceinline__ int rank_of_slot(int slot, int m, int pp) {
   return r;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(VER_THREADS, 1) verify_kernel(VerifyLaunch L) {
+template <typename T, int C>
+__global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) verify_kernel(VerifyLaunch L) {
   using E = VElem<T>;
   constexpr int VEC = E::VEC;
+  constexpr int NS = VER_WARPS * C;  // slices per row
   extern __shared__ __align__(16) uint8_t smem_raw[];
   VerShared& s = *reinterpret_cast<VerShared*>(smem_raw);
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int cr = static_cast<int>(cluster.block_rank());
+  const bool leader = cr == 0;
+  const int b = blockIdx.x / C, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const spec_tree_t& t = L.tree;
   const int m = L.p.m, D = L.p.depth, K = L.p.K, S = L.S, V = L.V;
   const float Tmp = L.p.temperature;
   const float c = LOG2E / Tmp;
   const int64_t nb = static_cast<int64_t>(b) * t.max_nodes;
   const int n_nodes = min(t.n_nodes[b], t.max_nodes);
-  for (int i = tid; i < n_nodes; i += VER_THREADS) s.node_parent[i] = t.node_parent[nb + i];
   const int64_t row_bytes = L.row_stride * E::ES;
   const uint8_t* tgt = static_cast<const uint8_t*>(L.target);
   const int nvec = static_cast<int>((static_cast<int64_t>(V) * E::ES) / 16);
+  if (leader) {
+    for (int i = tid; i < n_nodes; i += VER_THREADS) {
+      s.nd_parent[i] = t.node_parent[nb + i];
+      s.nd_slot[i] = t.node_slot[nb + i];
+      s.nd_exp_row[i] = t.node_exp_row[nb + i];
+      s.nd_token[i] = t.node_token[nb + i];
+    }
+    __syncthreads();
+  }
   bool nonfinite = false;
   int node = 0, level = 0;
   int32_t* ot = L.out_tok + static_cast<int64_t>(b) * (D + 1);
   int32_t* on = L.out_node + static_cast<int64_t>(b) * (D + 1);
-  __syncthreads();
+  VerShared* lead = cluster.map_shared_rank(&s, 0);
+  // support of the current node's draft row, prefetched per level by the leader
+  int sup_v = -1;
+  float sup_qt = 0.0f, zT = 0.0f;
+  int pp = -1;
   while (true) {
     const uint8_t* row = tgt + (nb + node) * row_bytes;
-    if (tid < K) s.kid_by_slot[tid] = -1;
-    if (tid == 0) {
-      s.accepted = -1;
-      s.Zr = 1.0;
-      s.ncorr = 0;
-    }
-    row_stats<T>(s, row, V, c, nonfinite);
-    // children of the node by sibling slot; a node at depth D is a leaf
-    // (which also bounds the walk for malformed trees)
-    int nk = 0;
-    if (level < D) {
-      for (int i = tid + 1; i < n_nodes; i += VER_THREADS)
-        if (s.node_parent[i] == node) {
-          const int slot = t.node_slot[nb + i];
-          if (slot >= 0 && slot < K) s.kid_by_slot[slot] = i;
+    int er = -1;
+    if (leader) {
+      er = level < D ? s.nd_exp_row[node] : -1;
+      if (er >= 0) {  // issued now, consumed after the row statistics
+        const int64_t srow = static_cast<int64_t>(b) * t.n_rows + er;
+        if (tid < S) {
+          sup_v = t.sup_id[srow * t.sup_stride + tid];
+          sup_qt = t.sup_qT[srow * t.sup_stride + tid];
         }
-      __syncthreads();
-      for (int k = 0; k < K; ++k) nk += s.kid_by_slot[k] >= 0;
-    }
-    const float M = s.M;
-    const float invZp = static_cast<float>(1.0 / s.Zp);
-    int64_t srow = -1;
-    if (nk > 0) {
-      srow = static_cast<int64_t>(b) * t.n_rows + t.node_exp_row[nb + node];
-      const int pp = t.probe_pos[srow];
-      const int probe_node = (pp >= 0) ? s.kid_by_slot[m] : -1;
-      const bool residual = probe_node >= 0;  // the tail residual applies iff the probe child survived
-      const float zT = t.sup_zT[srow];
-      float mn = 0.0f;
-      if (tid < S) {
-        const int v = t.sup_id[srow * t.sup_stride + tid];
-        const float p = expf((E::load(row, v) - M) / Tmp) * invZp;
-        const float qt = (tid >= m && zT > 0.0f) ? t.sup_qT[srow * t.sup_stride + tid] / zT : 0.0f;
-        s.p_sup[tid] = p;
-        s.w_sup[tid] = (residual && tid >= m) ? fmaxf(0.0f, p - qt) : p;
-        mn = (residual && tid >= m) ? fminf(p, qt) : 0.0f;
+        zT = t.sup_zT[srow];
+        pp = t.probe_pos[srow];
       }
-      mn = warp_sum(mn);
-      if (lane == 0) s.red[warp] = mn;
-      __syncthreads();
-      if (tid == 0) {
-        const float* uv = L.u_verify + (static_cast<int64_t>(b) * D + level) * K;
-        int j = 0;
-        double Zr = 1.0;
-        bool empty = false;
-        if (probe_node >= 0) {
-          const double p = s.p_sup[pp];
-          const double qt = static_cast<double>(t.sup_qT[srow * t.sup_stride + pp]) / zT;
-          const float u = uv[0];
-          if (L.margins && fabs(u * qt - p) < MASS_MARGIN) atomicAdd(L.margins, 1u);
-          if (static_cast<double>(u) * qt < p) {
-            s.accepted = probe_node;
-          } else {
-            double smin = 0.0;
-            for (int w = 0; w < (S + 31) / 32; ++w) smin += s.red[w];
-            Zr = 1.0 - smin;
-            j = 1;
-          }
-        }
-        if (s.accepted < 0) {
-          for (int slot = 0; slot < K; ++slot) {
-            const int kid = s.kid_by_slot[slot];
-            if (kid < 0 || kid == probe_node) continue;
-            if (Zr <= 0.0) {
-              empty = true;
-              break;
-            }
-            const int r = rank_of_slot(slot, m, pp);
-            const double w = s.w_sup[r];
-            const float u = uv[j];
-            if (L.margins && fabs(u * Zr - w) < MASS_MARGIN) atomicAdd(L.margins, 1u);
-            if (static_cast<double>(u) * Zr < w) {
-              s.accepted = kid;
-              break;
-            }
-            Zr -= w;
-            s.w_sup[r] = 0.0f;
-            ++j;
-          }
-          if (s.accepted < 0 && !empty && Zr <= 0.0) empty = true;
-          if (empty) {
-            // rounding emptied the residual: the bonus is drawn from p
-            set_status(L.status, SPEC_TREE_S_RESIDUAL_EMPTY);
-            for (int k = 0; k < S; ++k) s.w_sup[k] = s.p_sup[k];
-            Zr = 1.0;
-          }
-        }
-        s.Zr = Zr;
-      }
-      __syncthreads();
     }
-    const int acc = s.accepted;
+    slice_stats<T>(s, row, V, cr * VER_WARPS + warp, NS, c, nonfinite);
+    cluster.sync();  // A: every slice of the row is summarised
+    if (leader) {
+      if (tid < NS) {
+        const VerShared* src = cluster.map_shared_rank(&s, tid / VER_WARPS);
+        s.all_m[tid] = src->slice_m[tid % VER_WARPS];
+        s.all_s[tid] = src->slice_s[tid % VER_WARPS];
+      }
+      if (tid < K) s.kid_by_slot[tid] = -1;
+      __syncthreads();
+      if (warp == 0) {
+        // row maximum and normaliser (compensated per lane, pairwise across lanes)
+        float mx = -INFINITY;
+        for (int g = lane; g < NS; g += 32) mx = fmaxf(mx, s.all_m[g]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
+        float z = 0.0f, zc = 0.0f;
+        for (int g = lane; g < NS; g += 32) {
+          const float x = s.all_m[g] > -INFINITY ? s.all_s[g] * ex2((s.all_m[g] - mx) * c) : 0.0f;
+          const float y = x - zc;
+          const float tt = z + y;
+          zc = (tt - z) - y;
+          z = tt;
+        }
+        z = warp_sum(z - zc);
+        if (lane == 0) {
+          s.M = mx;
+          s.invZp = 1.0f / z;
+          s.Zr = 1.0f;
+          s.ncorr = 0;
+        }
+      }
+      // children of the node by sibling slot; a node at depth D is a leaf
+      // (which also bounds the walk for malformed trees)
+      if (er >= 0)
+        for (int i = tid + 1; i < n_nodes; i += VER_THREADS)
+          if (s.nd_parent[i] == node) {
+            const int slot = s.nd_slot[i];
+            if (slot >= 0 && slot < K) s.kid_by_slot[slot] = i;
+          }
+      __syncthreads();
+      int nk = 0;
+      if (er >= 0)
+        for (int k = 0; k < K; ++k) nk += s.kid_by_slot[k] >= 0;
+      const float M = s.M, invZp = s.invZp;
+      if (nk > 0) {
+        const int probe_node = (pp >= 0) ? s.kid_by_slot[m] : -1;
+        const bool residual = probe_node >= 0;  // the tail residual applies iff the probe child survived
+        float mn = 0.0f;
+        if (tid < S) {
+          const float p = expf((E::load(row, sup_v) - M) / Tmp) * invZp;
+          const float qt = (tid >= m && zT > 0.0f) ? sup_qt / zT : 0.0f;
+          s.p_sup[tid] = p;
+          s.qt_sup[tid] = qt;
+          s.w_sup[tid] = (residual && tid >= m) ? fmaxf(0.0f, p - qt) : p;
+          mn = (residual && tid >= m) ? fminf(p, qt) : 0.0f;
+        }
+        mn = warp_sum(mn);
+        if (lane == 0) s.red[warp] = mn;
+        __syncthreads();
+        if (tid == 0) {
+          const float* uv = L.u_verify + (static_cast<int64_t>(b) * D + level) * K;
+          int j = 0, accepted = -1;
+          float Zr = 1.0f;
+          bool empty = false;
+          if (probe_node >= 0) {
+            const float p = s.p_sup[pp], qt = s.qt_sup[pp];
+            const float u = uv[0];
+            if (L.margins && fabsf(u * qt - p) < static_cast<float>(MASS_MARGIN)) atomicAdd(L.margins, 1u);
+            if (u * qt < p) {
+              accepted = probe_node;
+            } else {
+              float smin = 0.0f;
+              for (int w = 0; w < (S + 31) / 32; ++w) smin += s.red[w];
+              Zr = 1.0f - smin;
+              j = 1;
+            }
+          }
+          if (accepted < 0) {
+            for (int slot = 0; slot < K; ++slot) {
+              const int kid = s.kid_by_slot[slot];
+              if (kid < 0 || kid == probe_node) continue;
+              if (Zr <= 0.0f) {
+                empty = true;
+                break;
+              }
+              const int r = rank_of_slot(slot, m, pp);
+              const float w = s.w_sup[r];
+              const float u = uv[j];
+              if (L.margins && fabsf(u * Zr - w) < static_cast<float>(MASS_MARGIN)) atomicAdd(L.margins, 1u);
+              if (u * Zr < w) {
+                accepted = kid;
+                break;
+              }
+              Zr -= w;
+              s.w_sup[r] = 0.0f;
+              ++j;
+            }
+            if (accepted < 0 && !empty && Zr <= 0.0f) empty = true;
+            if (empty) {
+              // rounding emptied the residual: the bonus is drawn from p
+              set_status(L.status, SPEC_TREE_S_RESIDUAL_EMPTY);
+              for (int k = 0; k < S; ++k) s.w_sup[k] = s.p_sup[k];
+              Zr = 1.0f;
+            }
+          }
+          s.Zr = Zr;
+          s.accepted = accepted;
+          if (accepted >= 0) {
+            ot[level] = s.nd_token[accepted];
+            on[level] = accepted;
+          }
+        }
+      } else if (tid == 0) {
+        s.accepted = -1;
+      }
+      if (tid == 0) s.nkids = nk;
+    }
+    cluster.sync();  // B: the leader's decision is published
+    const int acc = lead->accepted;
     if (acc >= 0) {
-      if (tid == 0) {
-        ot[level] = t.node_token[nb + acc];
-        on[level] = acc;
-      }
       node = acc;
       ++level;
-      __syncthreads();
       continue;
     }
+    if (!leader) break;  // the bonus is the leader's alone
     // ------------------------------------------------------------- bonus ---
-    // w = p except at support tokens whose residual differs; slice masses of w
-    if (tid < VER_WARPS) s.slice_corr[tid] = 0.0f;
+    const int nk = s.nkids;
+    const float M = s.M, invZp = s.invZp;
+    for (int g = tid; g < NS; g += VER_THREADS) s.slice_corr[g] = 0.0f;
     __syncthreads();
-    if (nk > 0 && tid < S) {
-      const float d = s.p_sup[tid] - s.w_sup[tid];
-      if (d != 0.0f)
-        atomicAdd(&s.slice_corr[slice_of_token(t.sup_id[srow * t.sup_stride + tid], nvec, VEC)], d);
-    }
+    const bool corrected = nk > 0 && tid < S && s.w_sup[tid] != s.p_sup[tid];
+    if (corrected) atomicAdd(&s.slice_corr[slice_of_token(sup_v, NS, nvec, VEC)], s.p_sup[tid] - s.w_sup[tid]);
     __syncthreads();
-    if (tid == 0) {
-      const double target = static_cast<double>(L.u_bonus[b]) * s.Zr;
-      double acc_mass = 0.0, before = 0.0, before_last = 0.0;
-      int pick = -1, last = -1;
-      for (int w = 0; w < VER_WARPS; ++w) {
-        double mass = s.slice_m[w] > -INFINITY
-                          ? static_cast<double>(s.slice_s[w]) * ex2((s.slice_m[w] - M) * c) / s.Zp
-                          : 0.0;
-        mass -= s.slice_corr[w];
-        if (mass > 0.0) {
-          last = w;
-          before_last = acc_mass;
+    if (warp == 0) {
+      // slice masses of w in id order; the first slice whose cumulative mass
+      // exceeds u * Zr holds the bonus token
+      constexpr int PER = (NS + 31) / 32;
+      const float target = L.u_bonus[b] * s.Zr;
+      float mass[PER], run = 0.0f;
+      int last_l = -1;
+#pragma unroll
+      for (int q = 0; q < PER; ++q) {
+        const int g = lane * PER + q;
+        float x = 0.0f;
+        if (g < NS) {
+          x = s.all_m[g] > -INFINITY ? s.all_s[g] * ex2((s.all_m[g] - M) * c) * invZp : 0.0f;
+          x -= s.slice_corr[g];
         }
-        if (pick < 0 && mass > 0.0 && target < acc_mass + mass) {
-          pick = w;
+        mass[q] = x;
+        run += x;
+        if (x > 0.0f) last_l = g;
+      }
+      float incl = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += y;
+      }
+      float acc_mass = incl - run;
+      int pick = -1;
+      float before = 0.0f;
+#pragma unroll
+      for (int q = 0; q < PER; ++q) {
+        if (pick < 0 && mass[q] > 0.0f && target < acc_mass + mass[q]) {
+          pick = lane * PER + q;
           before = acc_mass;
         }
-        acc_mass += mass;
+        acc_mass += mass[q];
       }
-      if (pick < 0) {  // rounding left the target past the total: the last slice with mass
-        pick = last < 0 ? VER_WARPS - 1 : last;
-        before = before_last;
+      const unsigned hit = __ballot_sync(FULL, pick >= 0);
+      int bs;
+      float bt;
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        bs = __shfl_sync(FULL, pick, src);
+        bt = target - __shfl_sync(FULL, before, src);
+      } else {
+        // rounding left the target past the total: the last slice with mass
+        int lastg = last_l;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lastg = max(lastg, __shfl_xor_sync(FULL, lastg, o));
+        bs = lastg < 0 ? NS - 1 : lastg;
+        bt = 3.0e38f;
       }
-      s.bonus_slice = pick;
-      s.bonus_target = static_cast<float>(target - before);
-      s.bonus = -1;
-      s.bonus_last = -1;
+      if (lane == 0) {
+        s.bonus_slice = bs;
+        s.bonus_target = bt;
+        s.bonus = -1;
+        s.bonus_last = -1;
+      }
     }
     __syncthreads();
     const int bs = s.bonus_slice;
-    const Slice sl(bs, nvec);
+    const Slice sl(bs, NS, nvec);
     const int t0 = sl.v0 * VEC;
-    const int t1 = (bs == VER_WARPS - 1) ? V : sl.v1 * VEC;
-    // corrected tokens inside the slice
-    if (nk > 0 && tid < S) {
-      const float wv = s.w_sup[tid];
-      if (wv != s.p_sup[tid]) {
-        const int v = t.sup_id[srow * t.sup_stride + tid];
-        if (v >= t0 && v < t1) {
-          const int k = atomicAdd(&s.ncorr, 1);
-          s.corr_tok[k] = v;
-          s.corr_w[k] = wv;
-        }
-      }
+    const int t1 = (bs == NS - 1) ? V : sl.v1 * VEC;
+    if (corrected && sup_v >= t0 && sup_v < t1) {
+      const int k = atomicAdd(&s.ncorr, 1);
+      s.corr_tok[k] = sup_v;
+      s.corr_w[k] = s.w_sup[tid];
     }
     __syncthreads();
     // scan the slice in id order: thread i handles tokens [base + VEC * i, + VEC)
     {
       const int ncorr = s.ncorr;
-      const float invZ = static_cast<float>(1.0 / s.Zp);
       const float tr = s.bonus_target;
       float base_run = 0.0f;
       int last_pos = -1;
@@ -407,7 +491,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) verify_kernel(VerifyLaunch L) 
         float ts = 0.0f;
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
-          w[j] = (w[j] == -INFINITY) ? 0.0f : ex2((w[j] - M) * c) * invZ;
+          w[j] = (w[j] == -INFINITY) ? 0.0f : ex2((w[j] - M) * c) * invZp;
           for (int k = 0; k < ncorr; ++k)
             if (s.corr_tok[k] == v0 + j) w[j] = s.corr_w[k];
           ts += w[j];
@@ -439,7 +523,8 @@ __global__ void __launch_bounds__(VER_THREADS, 1) verify_kernel(VerifyLaunch L) 
               const float nx = acc + w[j];
               if (tr < nx) {
                 pick = v0 + j;
-                if (L.margins && (tr - acc < MASS_MARGIN || nx - tr < MASS_MARGIN)) atomicAdd(L.margins + 1, 1u);
+                if (L.margins && (tr - acc < static_cast<float>(MASS_MARGIN) || nx - tr < static_cast<float>(MASS_MARGIN)))
+                  atomicAdd(L.margins + 1, 1u);
               }
               acc = nx;
             }
@@ -468,22 +553,51 @@ __global__ void __launch_bounds__(VER_THREADS, 1) verify_kernel(VerifyLaunch L) 
     break;
   }
   if (nonfinite) set_status(L.status, SPEC_TREE_S_NONFINITE_TARGET);
+  // no CTA leaves while a peer may still read its shared memory
+  cluster.sync();
+}
+
+template <typename T, int C>
+cudaError_t launch_verify_c(const VerifyLaunch& L, cudaStream_t stream) {
+  const int smem = static_cast<int>(sizeof(VerShared));
+  cudaError_t err = cudaFuncSetAttribute(verify_kernel<T, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  verify_kernel<T, C><<<L.B * C, VER_THREADS, smem, stream>>>(L);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_verify_t(const VerifyLaunch& L, cudaStream_t stream) {
+  // the largest cluster (<= 8 CTAs, one per SM) that keeps the batch in one
+  // wave; a cluster shape the device cannot place is refused at launch, and
+  // the next smaller one is tried
+  int C = 1;
+  while (C < VER_MAX_CLUSTER && static_cast<int64_t>(L.B) * C * 2 <= L.num_sms) C *= 2;
+  cudaError_t err = cudaErrorInvalidValue;
+  for (; C >= 1; C /= 2) {
+    switch (C) {
+      case 8:
+        err = launch_verify_c<T, 8>(L, stream);
+        break;
+      case 4:
+        err = launch_verify_c<T, 4>(L, stream);
+        break;
+      case 2:
+        err = launch_verify_c<T, 2>(L, stream);
+        break;
+      default:
+        err = launch_verify_c<T, 1>(L, stream);
+        break;
+    }
+    if (err == cudaSuccess) break;
+  }
+  return err;
 }
 
 cudaError_t launch_verify(const VerifyLaunch& L, cudaStream_t stream) {
   if (L.B == 0) return cudaSuccess;
-  const int smem = static_cast<int>(sizeof(VerShared));
-  if (L.dtype == SPEC_TREE_BF16) {
-    cudaError_t err =
-        cudaFuncSetAttribute(verify_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (err != cudaSuccess) return err;
-    verify_kernel<__nv_bfloat16><<<L.B, VER_THREADS, smem, stream>>>(L);
-  } else {
-    cudaError_t err = cudaFuncSetAttribute(verify_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (err != cudaSuccess) return err;
-    verify_kernel<float><<<L.B, VER_THREADS, smem, stream>>>(L);
-  }
-  return cudaGetLastError();
+  if (L.dtype == SPEC_TREE_BF16) return launch_verify_t<__nv_bfloat16>(L, stream);
+  return launch_verify_t<float>(L, stream);
 }
 
 }  // namespace st
