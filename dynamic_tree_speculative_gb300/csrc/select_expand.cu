@@ -37,9 +37,11 @@
 
 namespace st {
 
-constexpr int SX_CONS = 256;                     // consumer threads (8 warps)
+constexpr int SX_CONS = 256;                     // streaming consumer threads (8 warps)
 constexpr int SX_CWARPS = SX_CONS / 32;
-constexpr int SX_THREADS = SX_CONS + 32;         // + one producer warp
+constexpr int SX_SEL_WARP = SX_CWARPS;           // warp 8: exact selection + epilogue
+constexpr int SX_PROD_WARP = SX_CWARPS + 1;      // warp 9: bulk-copy producer
+constexpr int SX_THREADS = SX_CONS + 64;
 constexpr int SX_VPT = 4;                        // 16-byte vectors per consumer thread per stage
 constexpr int SX_CHUNK = SX_CONS * 16 * SX_VPT;  // 16 KB per stage
 constexpr int SX_STAGES = 4;
@@ -52,16 +54,21 @@ constexpr int SX_FB_HIGH = SX_CAP - SX_FB_STEP;
 
 struct SelShared {
   alignas(128) uint8_t ring[SX_STAGES][SX_CHUNK];
-  uint64_t cand[SX_CAP];
+  uint64_t cand[2][SX_CAP];  // double-buffered candidates: streamers fill one, the selector drains the other
   uint4 qvec[SX_QCAP];
   uint32_t qid[SX_QCAP];
-  uint64_t sel[SPEC_TREE_MAX_SUPPORT];
+  uint64_t sel[SPEC_TREE_MAX_SUPPORT];   // streamers' scratch (robust path)
+  uint64_t ssel[SPEC_TREE_MAX_SUPPORT];  // selector's scratch
   uint64_t tie[32];
   uint64_t full[SX_STAGES];
   uint64_t empty[SX_STAGES];
+  uint64_t cfull[2];   // candidates of a row ready for the selector
+  uint64_t cempty[2];  // selector done with a candidate buffer
+  int64_t cand_row[2];
   uint32_t hist[256];
+  uint32_t shist[256];
   uint32_t warp_bound[SX_CWARPS];
-  int count;
+  int count[2];
   int qn_warp[SX_CWARPS];
   int sel_count;
   int tie_count;
@@ -71,10 +78,12 @@ struct SelShared {
   uint32_t thr_key;
   int strict;
   int timeout;
-  float epi_red[4][4];  // per-warp sums of the epilogue (warps 0..3)
-  float epi_scan[4];
-  int probe_first;
-  int probe_last;
+};
+
+// A candidate buffer and its fill count.
+struct CandBuf {
+  uint64_t* c;
+  int* n;
 };
 
 size_t select_expand_smem_bytes() { return sizeof(SelShared); }
@@ -218,7 +227,7 @@ __device__ __forceinline__ uint64_t make_comp(uint32_t key, uint32_t id) {
 // Warp-aggregated append of the elements selected by `mask` (bit j: key
 // keys[j], id id0 + j).  All 32 lanes of the warp call it.
 template <int VEC>
-__device__ __forceinline__ void append_warp(SelShared& s, uint32_t mask, const uint32_t* keys, uint32_t id0,
+__device__ __forceinline__ void append_warp(CandBuf cb, uint32_t mask, const uint32_t* keys, uint32_t id0,
                                             bool& overflow) {
   const int lane = threadIdx.x & 31;
   if (!__any_sync(FULL, mask != 0)) return;
@@ -231,13 +240,13 @@ __device__ __forceinline__ void append_warp(SelShared& s, uint32_t mask, const u
   }
   const int total = __shfl_sync(FULL, incl, 31);
   int base = 0;
-  if (lane == 31) base = atomicAdd(&s.count, total);
+  if (lane == 31) base = atomicAdd(cb.n, total);
   base = __shfl_sync(FULL, base, 31);
   int pos = base + incl - cnt;
 #pragma unroll
   for (int j = 0; j < VEC; ++j) {
     if (mask & (1u << j)) {
-      if (pos < SX_CAP) s.cand[pos] = make_comp(keys[j], id0 + j);
+      if (pos < SX_CAP) cb.c[pos] = make_comp(keys[j], id0 + j);
       else overflow = true;
       ++pos;
     }
@@ -283,7 +292,7 @@ struct Filter<__nv_bfloat16> {
     mx = __hmax2(mx, __lowhigh2highlow(mx));
     return __hbge2(mx, b2);
   }
-  __device__ __forceinline__ void emit(SelShared& s, const uint4& v, uint32_t id0, bool& overflow) const {
+  __device__ __forceinline__ void emit(CandBuf cb, const uint4& v, uint32_t id0, bool& overflow) const {
     const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
     const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
     const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
@@ -292,12 +301,12 @@ struct Filter<__nv_bfloat16> {
     const uint32_t m2 = __hge2_mask(c, b2), m3 = __hge2_mask(d, b2);
     const uint32_t mask = (m0 & 1u) | ((m0 >> 15) & 2u) | ((m1 & 1u) << 2) | ((m1 >> 13) & 8u) |
                           ((m2 & 1u) << 4) | ((m2 >> 11) & 0x20u) | ((m3 & 1u) << 6) | ((m3 >> 9) & 0x80u);
-    int pos = atomicAdd(&s.count, __popc(mask));
+    int pos = atomicAdd(cb.n, __popc(mask));
     bool nf = false;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (mask & (1u << j)) {
-        if (pos < SX_CAP) s.cand[pos] = make_comp(elem_key<__nv_bfloat16>(v, j, nf), id0 + j);
+        if (pos < SX_CAP) cb.c[pos] = make_comp(elem_key<__nv_bfloat16>(v, j, nf), id0 + j);
         else overflow = true;
         ++pos;
       }
@@ -329,7 +338,7 @@ struct Filter<float> {
     for (int j = 0; j < 4; ++j) k = max(k, elem_key<float>(v, j, nf));
     return k >= bound;
   }
-  __device__ __forceinline__ void emit(SelShared& s, const uint4& v, uint32_t id0, bool& overflow) const {
+  __device__ __forceinline__ void emit(CandBuf cb, const uint4& v, uint32_t id0, bool& overflow) const {
     bool nf = false;
     uint32_t keys[4], mask = 0;
 #pragma unroll
@@ -337,11 +346,11 @@ struct Filter<float> {
       keys[j] = elem_key<float>(v, j, nf);
       if (keys[j] >= bound) mask |= 1u << j;
     }
-    int pos = atomicAdd(&s.count, __popc(mask));
+    int pos = atomicAdd(cb.n, __popc(mask));
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       if (mask & (1u << j)) {
-        if (pos < SX_CAP) s.cand[pos] = make_comp(keys[j], id0 + j);
+        if (pos < SX_CAP) cb.c[pos] = make_comp(keys[j], id0 + j);
         else overflow = true;
         ++pos;
       }
@@ -361,11 +370,11 @@ __device__ __forceinline__ uint32_t warp_kth_largest(uint32_t key, int j) {
   return res;
 }
 
-// Exact top-k of s.cand[0..n) (distinct composites) sorted descending into
-// s.cand[0..min(n,k)); count = min(n,k); when n >= k the strict threshold
-// becomes the key of the k-th.  Consumer threads only.
+// Exact top-k of cb.c[0..n) (distinct composites) sorted descending into
+// cb.c[0..min(n,k)); count = min(n,k); when n >= k the strict threshold
+// becomes the key of the k-th.  Streamer threads only (robust path).
 template <int KEY_BITS>
-__device__ void select_topk(SelShared& s, int n, int k) {
+__device__ void select_topk(SelShared& s, CandBuf cb, int n, int k) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (n > k) {
     // digits: the key bytes, then bits 23..0 of ~id (bits 31..24 of ~id are
@@ -382,7 +391,7 @@ __device__ void select_topk(SelShared& s, int n, int k) {
       csync();
       for (int i = tid; i < n_round; i += SX_CONS) {
         bool valid = i < n;
-        const uint64_t c = valid ? s.cand[i] : 0ull;
+        const uint64_t c = valid ? cb.c[i] : 0ull;
         valid = valid && ((c & pmask) == prefix);
         const uint32_t bin = static_cast<uint32_t>(c >> sh) & 0xffu;
         const uint32_t tag = valid ? bin : (0x100u | lane);
@@ -437,7 +446,7 @@ __device__ void select_topk(SelShared& s, int n, int k) {
     }
     csync();
     for (int i = tid; i < n; i += SX_CONS) {
-      const uint64_t c = s.cand[i];
+      const uint64_t c = cb.c[i];
       const uint64_t m = c & pmask;
       if (tie_mode ? m > prefix : m >= prefix) {
         const int pos = atomicAdd(&s.sel_count, 1);
@@ -460,7 +469,7 @@ __device__ void select_topk(SelShared& s, int n, int k) {
     }
     csync();
   } else {
-    for (int i = tid; i < n; i += SX_CONS) s.sel[i] = s.cand[i];
+    for (int i = tid; i < n; i += SX_CONS) s.sel[i] = cb.c[i];
     csync();
   }
   const int kk = n < k ? n : k;
@@ -471,12 +480,12 @@ __device__ void select_topk(SelShared& s, int n, int k) {
     for (int j = 0; j < kk; ++j) r += (s.sel[j] > c);
   }
   csync();
-  if (tid < kk) s.cand[r] = c;
+  if (tid < kk) cb.c[r] = c;
   csync();
   if (tid == 0) {
-    s.count = kk;
+    *cb.n = kk;
     if (n >= k) {
-      s.thr_key = static_cast<uint32_t>(s.cand[kk - 1] >> 32);
+      s.thr_key = static_cast<uint32_t>(cb.c[kk - 1] >> 32);
       s.strict = 1;
     }
   }
@@ -508,7 +517,7 @@ struct SelArgs {
 // the exact top-|S| of the prefix seen, then only elements strictly above
 // its last key (an equal key later in id order loses the tie).
 template <typename T>
-__device__ void select_row_fallback(SelShared& s, const uint8_t* row, int V, int S, bool& nonfinite,
+__device__ void select_row_fallback(SelShared& s, CandBuf cb, const uint8_t* row, int V, int S, bool& nonfinite,
                                     bool& overflow) {
   using E = Elem<T>;
   constexpr int VEC = E::VEC;
@@ -516,7 +525,7 @@ __device__ void select_row_fallback(SelShared& s, const uint8_t* row, int V, int
   const int nvec = static_cast<int>((static_cast<int64_t>(V) * E::ES) / 16);
   csync();
   if (tid == 0) {
-    s.count = 0;
+    *cb.n = 0;
     s.thr_key = 0;
     s.strict = 0;
   }
@@ -549,73 +558,183 @@ __device__ void select_row_fallback(SelShared& s, const uint8_t* row, int V, int
         }
       }
     }
-    append_warp<VEC>(s, mask, keys, id0, overflow);
+    append_warp<VEC>(cb, mask, keys, id0, overflow);
     csync();
-    if (s.count > SX_FB_HIGH) select_topk<E::KEY_BITS>(s, s.count, S);
+    if (*cb.n > SX_FB_HIGH) select_topk<E::KEY_BITS>(s, cb, *cb.n, S);
   }
 }
 
-// Softmaxes, tail masses and the probe of one row from its sorted support,
-// by consumer warps 0..3 (one support rank per thread).  RheoSampling Key
-// design 2; the probe is the first tail rank k with
-// u * z_T < sum_{j=m..k} q_T(j), computed on unnormalised weights.
-__device__ __forceinline__ void esync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+// Exact top-k (k <= 128) of c[0..n) by one warp, sorted descending: a radix
+// select over the composite digits (warp-private histogram), then a bitonic
+// network over 128 slots held 4 per lane (element j*32 + lane).  Returns the
+// number of valid ranks, min(n, k); `val` receives the sorted composites.
+template <int KEY_BITS>
+__device__ int warp_select_sort(SelShared& s, const uint64_t* c, int n, int k, uint64_t (&val)[4]) {
+  const int lane = threadIdx.x & 31;
+  uint64_t* out = s.ssel;
+  int kk = n < k ? n : k;
+  if (n > k) {
+    constexpr int NKD = KEY_BITS / 8;
+    uint64_t prefix = 0, pmask = 0;
+    int need = k;
+#pragma unroll 1
+    for (int d = 0; d < NKD + 3; ++d) {
+      const int sh = d < NKD ? 32 + KEY_BITS - 8 * (d + 1) : 8 * (NKD + 2 - d);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s.shist[lane * 8 + j] = 0;
+      __syncwarp();
+      for (int i = lane; i < n; i += 32) {
+        const uint64_t x = c[i];
+        if ((x & pmask) == prefix) atomicAdd(&s.shist[static_cast<uint32_t>(x >> sh) & 0xffu], 1u);
+      }
+      __syncwarp();
+      uint32_t h[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        h[j] = s.shist[255 - 8 * lane - j];
+        tot += h[j];
+      }
+      uint32_t incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const uint32_t excl = incl - tot;
+      int bin = -1, above = 0, cnt = 0;
+      if (excl < static_cast<uint32_t>(need) && static_cast<uint32_t>(need) <= incl) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (bin < 0 && acc + h[j] >= static_cast<uint32_t>(need)) {
+            bin = 255 - 8 * lane - j;
+            above = static_cast<int>(acc);
+            cnt = static_cast<int>(h[j]);
+          }
+          acc += h[j];
+        }
+      }
+      const int src = __ffs(__ballot_sync(FULL, bin >= 0)) - 1;
+      bin = __shfl_sync(FULL, bin, src);
+      above = __shfl_sync(FULL, above, src);
+      cnt = __shfl_sync(FULL, cnt, src);
+      need -= above;
+      prefix |= static_cast<uint64_t>(bin) << sh;
+      pmask |= 0xffull << sh;
+      __syncwarp();
+      if (cnt == need) break;
+    }
+    // gather the k winners (order fixed by the sort below)
+    int base = 0;
+    for (int i0 = 0; i0 < n; i0 += 32) {
+      const int i = i0 + lane;
+      const uint64_t x = i < n ? c[i] : 0ull;
+      const bool take = i < n && (x & pmask) >= prefix;
+      const unsigned bal = __ballot_sync(FULL, take);
+      if (take) out[base + __popc(bal & ((1u << lane) - 1u))] = x;
+      base += __popc(bal);
+    }
+  } else {
+    for (int i = lane; i < n; i += 32) out[i] = c[i];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = j * 32 + lane;
+    val[j] = e < kk ? out[e] : 0ull;  // 0 sorts below every composite
+  }
+  // bitonic sort, descending, over e = j*32 + lane
+#pragma unroll
+  for (int size = 2; size <= 128; size <<= 1) {
+#pragma unroll
+    for (int d = size >> 1; d > 0; d >>= 1) {
+      uint64_t nv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = j * 32 + lane;
+        const uint64_t x = val[j];
+        const uint64_t y = d >= 32 ? val[j ^ (d >> 5)] : __shfl_xor_sync(FULL, x, d);
+        const bool desc = (e & size) == 0;
+        const bool lower = (e & d) == 0;
+        nv[j] = (desc == lower) ? (x > y ? x : y) : (x < y ? x : y);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) val[j] = nv[j];
+    }
+  }
+  return kk;
+}
 
+// Softmaxes, tail masses and the probe of one row from its sorted support,
+// by the selector warp (rank j*32 + lane in val[j]).  RheoSampling Key design
+// 2; the probe is the first tail rank k with u * z_T < sum_{j=m..k} q_T(j),
+// computed on unnormalised weights.
 template <typename T>
-__device__ void expand_epilogue(SelShared& s, const SelArgs& a, int64_t out_row, int n_sup) {
-  const int r = threadIdx.x, lane = r & 31, w = r >> 5;
-  const bool valid = r < n_sup, tail = valid && r >= a.m;
-  const uint64_t c = valid ? s.cand[r] : 0ull;
-  const float l = key_value<T>(static_cast<uint32_t>(c >> 32));
-  const float lmax = key_value<T>(static_cast<uint32_t>(s.cand[0] >> 32));
-  if (r == 0 && !(lmax < INFINITY)) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
-  const float d = l - lmax;
-  const float e = valid ? expf(d) : 0.0f;
-  const float eT = valid ? expf(d / a.temperature) : 0.0f;
-  const float te = tail ? e : 0.0f, teT = tail ? eT : 0.0f;
-  // inclusive scan of the tail weights (rank order) within the warp
-  float incl = teT;
+__device__ void expand_epilogue(const uint64_t (&val)[4], const SelArgs& a, int64_t out_row, int n_sup) {
+  const int lane = threadIdx.x & 31;
+  float l[4], e[4], eT[4];
+  const float lmax = key_value<T>(static_cast<uint32_t>(__shfl_sync(FULL, val[0], 0) >> 32));
+  if (lane == 0 && !(lmax < INFINITY)) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
+  float se = 0.0f, seT = 0.0f, te = 0.0f, teT = 0.0f;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float t = __shfl_up_sync(FULL, incl, o);
-    if (lane >= o) incl += t;
+  for (int j = 0; j < 4; ++j) {
+    const int r = j * 32 + lane;
+    const bool valid = r < n_sup;
+    l[j] = key_value<T>(static_cast<uint32_t>(val[j] >> 32));
+    const float dd = l[j] - lmax;
+    e[j] = valid ? expf(dd) : 0.0f;
+    eT[j] = valid ? expf(dd / a.temperature) : 0.0f;
+    se += e[j];
+    seT += eT[j];
+    if (valid && r >= a.m) {
+      te += e[j];
+      teT += eT[j];
+    }
   }
-  const float w_e = warp_sum(e), w_eT = warp_sum(eT), w_te = warp_sum(te);
-  if (lane == 31) s.epi_scan[w] = incl;
+  se = warp_sum(se);
+  seT = warp_sum(seT);
+  te = warp_sum(te);
+  teT = warp_sum(teT);
+  int32_t* sid = a.sup_id + out_row * a.sup_stride;
+  float* sq = a.sup_q + out_row * a.sup_stride;
+  float* sqT = a.sup_qT + out_row * a.sup_stride;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = j * 32 + lane;
+    if (r < n_sup) {
+      sid[r] = static_cast<int32_t>(~static_cast<uint32_t>(val[j]));
+      sq[r] = e[j] / se;
+      sqT[r] = eT[j] / seT;
+    }
+  }
+  int probe = -1;
+  if (a.m < n_sup && teT > 0.0f) {
+    const float target = a.u_probe[out_row] * teT;
+    float carry = 0.0f;
+    int last = -1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = j * 32 + lane;
+      const bool tl = r < n_sup && r >= a.m;
+      const float x = tl ? eT[j] : 0.0f;
+      float incl = x;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(FULL, tl && target < carry + incl);
+      if (probe < 0 && hit) probe = j * 32 + __ffs(hit) - 1;
+      const unsigned pos = __ballot_sync(FULL, tl && x > 0.0f);
+      if (pos) last = j * 32 + 31 - __clz(pos);
+      carry += __shfl_sync(FULL, incl, 31);
+    }
+    if (probe < 0) probe = last;
+  }
   if (lane == 0) {
-    s.epi_red[w][0] = w_e;
-    s.epi_red[w][1] = w_eT;
-    s.epi_red[w][2] = w_te;
-  }
-  esync();
-  float se = 0.0f, seT = 0.0f, tz = 0.0f, tzT = 0.0f, before = 0.0f;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    se += s.epi_red[k][0];
-    seT += s.epi_red[k][1];
-    tz += s.epi_red[k][2];
-    tzT += s.epi_scan[k];
-    if (k < w) before += s.epi_scan[k];
-  }
-  if (valid) {
-    a.sup_id[out_row * a.sup_stride + r] = static_cast<int32_t>(~static_cast<uint32_t>(c));
-    a.sup_q[out_row * a.sup_stride + r] = e / se;
-    a.sup_qT[out_row * a.sup_stride + r] = eT / seT;
-  }
-  if (a.m < n_sup && tzT > 0.0f) {
-    const float target = a.u_probe[out_row] * tzT;
-    if (tail && target < before + incl) atomicMin(&s.probe_first, r);
-    if (tail && eT > 0.0f) atomicMax(&s.probe_last, r);
-  }
-  esync();
-  if (r == 0) {
-    int probe = -1;
-    if (a.m < n_sup && tzT > 0.0f) probe = s.probe_first < SPEC_TREE_MAX_SUPPORT ? s.probe_first : s.probe_last;
-    a.sup_z[out_row] = tz / se;
-    a.sup_zT[out_row] = tzT / seT;
+    a.sup_z[out_row] = te / se;
+    a.sup_zT[out_row] = teT / seT;
     a.probe_pos[out_row] = probe;
-    s.probe_first = 1 << 30;
-    s.probe_last = -1;
   }
 }
 
@@ -640,14 +759,36 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], SX_CWARPS);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.cfull[i], 1);
+      mbar_init(&s.cempty[i], 1);
+    }
     fence_mbar_init();
     s.timeout = 0;
-    s.probe_first = 1 << 30;
-    s.probe_last = -1;
   }
   __syncthreads();  // the last CTA-wide barrier: the roles split below
 
-  if (warp == SX_CWARPS) {
+  if (warp == SX_SEL_WARP) {
+    // ------------------------------------------------------------ selector ---
+    // Rows in order: wait for the streamers' candidates, select the exact
+    // top-|S|, sort, expand, write the outputs, hand the buffer back.
+    bool timed_out = false;
+    for (int64_t lr = 0; lr < my_rows; ++lr) {
+      const int q = static_cast<int>(lr & 1);
+      if (!mbar_wait(&s.cfull[q], static_cast<uint32_t>((lr >> 1) & 1))) timed_out = true;
+      const int n = s.count[q];
+      const int64_t out_row = s.cand_row[q];
+      uint64_t val[4];
+      const int n_sup = warp_select_sort<E::KEY_BITS>(s, s.cand[q], min(n, SX_CAP), a.S, val);
+      expand_epilogue<T>(val, a, out_row, n_sup);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.cempty[q]);
+    }
+    if (timed_out && lane == 0) set_status(a.status, SPEC_TREE_S_TIMEOUT);
+    return;
+  }
+
+  if (warp == SX_PROD_WARP) {
     // ------------------------------------------------------------ producer ---
     if (lane == 0 && nch > 0) {
       const uint64_t keep = l2_evict_last_policy();
@@ -728,10 +869,16 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
       tail_key = scalar_key<T>(row, tail_id, nonfinite);
       rm.add_key(tail_key);
     }
+    // candidate buffer of this row (the selector may still drain it from two rows ago)
+    const int q = static_cast<int>(lr & 1);
+    const CandBuf cb{s.cand[q], &s.count[q]};
     // bound: min over consumer warps of the warp's jth-largest thread maximum
     const uint32_t wb = warp_kth_largest<E::KEY_BITS>(rm.key(nonfinite), jth);
     if (lane == 0) s.warp_bound[warp] = wb;
-    if (tid == 0) s.count = 0;
+    if (tid == 0) {
+      if (lr >= 2 && !mbar_wait(&s.cempty[q], static_cast<uint32_t>(((lr >> 1) - 1) & 1))) s.timeout = 1;
+      *cb.n = 0;
+    }
     csync();
     uint32_t bound = 0xffffffffu;
 #pragma unroll
@@ -806,22 +953,23 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
           rem -= s.qn_warp[w];
           ++w;
         }
-        flt.emit(s, s.qvec[w * SX_QW + rem], s.qid[w * SX_QW + rem], p2over);
+        flt.emit(cb, s.qvec[w * SX_QW + rem], s.qid[w * SX_QW + rem], p2over);
       }
       if (tail_id < a.V && tail_key >= bound && !robust) {
-        const int pos = atomicAdd(&s.count, 1);
-        if (pos < SX_CAP) s.cand[pos] = make_comp(tail_key, static_cast<uint32_t>(tail_id));
+        const int pos = atomicAdd(cb.n, 1);
+        if (pos < SX_CAP) cb.c[pos] = make_comp(tail_key, static_cast<uint32_t>(tail_id));
       }
     }
     csync();
-    int n = s.count;
-    if (n > SX_CAP || robust || q_over) {
+    if (*cb.n > SX_CAP || robust || q_over) {
       // massive ties at the bound: redo the row in id order from global memory
-      select_row_fallback<T>(s, row, a.V, a.S, nonfinite, overflow);
-      n = s.count;
+      select_row_fallback<T>(s, cb, row, a.V, a.S, nonfinite, overflow);
     }
-    select_topk<E::KEY_BITS>(s, n, a.S);
-    if (warp < 4) expand_epilogue<T>(s, a, out_row, n < a.S ? n : a.S);
+    // hand the candidates to the selector warp and move on to the next row
+    if (tid == 0) {
+      s.cand_row[q] = out_row;
+      mbar_arrive(&s.cfull[q]);
+    }
     e += gridDim.x;
     while (e >= a.rows_used) {
       e -= a.rows_used;
