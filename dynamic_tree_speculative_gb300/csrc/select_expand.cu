@@ -44,13 +44,14 @@ constexpr int SX_PROD_WARP = SX_CWARPS + 1;      // warp 9: bulk-copy producer
 constexpr int SX_THREADS = SX_CONS + 64;
 constexpr int SX_VPT = 4;                        // 16-byte vectors per consumer thread per stage
 constexpr int SX_CHUNK = SX_CONS * 16 * SX_VPT;  // 16 KB per stage
-constexpr int SX_STAGES = 4;
+constexpr int SX_STAGES = 5;
 constexpr int SX_FB_THREADS = 128;               // robust path: threads reading per step
-constexpr int SX_CAP = 512 + SX_FB_THREADS * 8;  // candidate buffer (64-bit composites)
-constexpr int SX_QCAP = 1024;                    // pass-2 queue of vectors that reach the bound
+constexpr int SX_CAP = 640;                      // candidates of one row (64-bit composites)
+constexpr int SX_QCAP = 896;                     // pass-2 queue of vectors that reach the bound
 constexpr int SX_QW = SX_QCAP / SX_CWARPS;       // queue slots owned by each consumer warp
 constexpr int SX_FB_STEP = SX_FB_THREADS * 8;    // robust path: at most this many appends per step
-constexpr int SX_FB_HIGH = SX_CAP - SX_FB_STEP;
+constexpr int SX_FB_CAP = SX_QCAP * 2;           // robust path: candidates live in the queue's storage
+constexpr int SX_FB_HIGH = SX_FB_CAP - SX_FB_STEP;
 
 struct SelShared {
   alignas(128) uint8_t ring[SX_STAGES][SX_CHUNK];
@@ -84,6 +85,7 @@ struct SelShared {
 struct CandBuf {
   uint64_t* c;
   int* n;
+  int cap;
 };
 
 size_t select_expand_smem_bytes() { return sizeof(SelShared); }
@@ -246,7 +248,7 @@ __device__ __forceinline__ void append_warp(CandBuf cb, uint32_t mask, const uin
 #pragma unroll
   for (int j = 0; j < VEC; ++j) {
     if (mask & (1u << j)) {
-      if (pos < SX_CAP) cb.c[pos] = make_comp(keys[j], id0 + j);
+      if (pos < cb.cap) cb.c[pos] = make_comp(keys[j], id0 + j);
       else overflow = true;
       ++pos;
     }
@@ -306,7 +308,7 @@ struct Filter<__nv_bfloat16> {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (mask & (1u << j)) {
-        if (pos < SX_CAP) cb.c[pos] = make_comp(elem_key<__nv_bfloat16>(v, j, nf), id0 + j);
+        if (pos < cb.cap) cb.c[pos] = make_comp(elem_key<__nv_bfloat16>(v, j, nf), id0 + j);
         else overflow = true;
         ++pos;
       }
@@ -350,7 +352,7 @@ struct Filter<float> {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       if (mask & (1u << j)) {
-        if (pos < SX_CAP) cb.c[pos] = make_comp(keys[j], id0 + j);
+        if (pos < cb.cap) cb.c[pos] = make_comp(keys[j], id0 + j);
         else overflow = true;
         ++pos;
       }
@@ -564,93 +566,19 @@ __device__ void select_row_fallback(SelShared& s, CandBuf cb, const uint8_t* row
   }
 }
 
-// Exact top-k (k <= 128) of c[0..n) by one warp, sorted descending: a radix
-// select over the composite digits (warp-private histogram), then a bitonic
-// network over 128 slots held 4 per lane (element j*32 + lane).  Returns the
-// number of valid ranks, min(n, k); `val` receives the sorted composites.
-template <int KEY_BITS>
-__device__ int warp_select_sort(SelShared& s, const uint64_t* c, int n, int k, uint64_t (&val)[4]) {
+// Bitonic sort, descending, of 32*PER composites held PER per lane
+// (element j*32 + lane in val[j]) by one warp.
+template <int PER>
+__device__ __forceinline__ void warp_bitonic_desc(uint64_t (&val)[PER]) {
   const int lane = threadIdx.x & 31;
-  uint64_t* out = s.ssel;
-  int kk = n < k ? n : k;
-  if (n > k) {
-    constexpr int NKD = KEY_BITS / 8;
-    uint64_t prefix = 0, pmask = 0;
-    int need = k;
-#pragma unroll 1
-    for (int d = 0; d < NKD + 3; ++d) {
-      const int sh = d < NKD ? 32 + KEY_BITS - 8 * (d + 1) : 8 * (NKD + 2 - d);
+  constexpr int N = 32 * PER;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) s.shist[lane * 8 + j] = 0;
-      __syncwarp();
-      for (int i = lane; i < n; i += 32) {
-        const uint64_t x = c[i];
-        if ((x & pmask) == prefix) atomicAdd(&s.shist[static_cast<uint32_t>(x >> sh) & 0xffu], 1u);
-      }
-      __syncwarp();
-      uint32_t h[8], tot = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        h[j] = s.shist[255 - 8 * lane - j];
-        tot += h[j];
-      }
-      uint32_t incl = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(FULL, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const uint32_t excl = incl - tot;
-      int bin = -1, above = 0, cnt = 0;
-      if (excl < static_cast<uint32_t>(need) && static_cast<uint32_t>(need) <= incl) {
-        uint32_t acc = excl;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (bin < 0 && acc + h[j] >= static_cast<uint32_t>(need)) {
-            bin = 255 - 8 * lane - j;
-            above = static_cast<int>(acc);
-            cnt = static_cast<int>(h[j]);
-          }
-          acc += h[j];
-        }
-      }
-      const int src = __ffs(__ballot_sync(FULL, bin >= 0)) - 1;
-      bin = __shfl_sync(FULL, bin, src);
-      above = __shfl_sync(FULL, above, src);
-      cnt = __shfl_sync(FULL, cnt, src);
-      need -= above;
-      prefix |= static_cast<uint64_t>(bin) << sh;
-      pmask |= 0xffull << sh;
-      __syncwarp();
-      if (cnt == need) break;
-    }
-    // gather the k winners (order fixed by the sort below)
-    int base = 0;
-    for (int i0 = 0; i0 < n; i0 += 32) {
-      const int i = i0 + lane;
-      const uint64_t x = i < n ? c[i] : 0ull;
-      const bool take = i < n && (x & pmask) >= prefix;
-      const unsigned bal = __ballot_sync(FULL, take);
-      if (take) out[base + __popc(bal & ((1u << lane) - 1u))] = x;
-      base += __popc(bal);
-    }
-  } else {
-    for (int i = lane; i < n; i += 32) out[i] = c[i];
-  }
-  __syncwarp();
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int e = j * 32 + lane;
-    val[j] = e < kk ? out[e] : 0ull;  // 0 sorts below every composite
-  }
-  // bitonic sort, descending, over e = j*32 + lane
-#pragma unroll
-  for (int size = 2; size <= 128; size <<= 1) {
+  for (int size = 2; size <= N; size <<= 1) {
 #pragma unroll
     for (int d = size >> 1; d > 0; d >>= 1) {
-      uint64_t nv[4];
+      uint64_t nv[PER];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < PER; ++j) {
         const int e = j * 32 + lane;
         const uint64_t x = val[j];
         const uint64_t y = d >= 32 ? val[j ^ (d >> 5)] : __shfl_xor_sync(FULL, x, d);
@@ -659,9 +587,104 @@ __device__ int warp_select_sort(SelShared& s, const uint64_t* c, int n, int k, u
         nv[j] = (desc == lower) ? (x > y ? x : y) : (x < y ? x : y);
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) val[j] = nv[j];
+      for (int j = 0; j < PER; ++j) val[j] = nv[j];
     }
   }
+}
+
+// Loads c[0..n) (n <= 32*PER) into PER-per-lane registers padded with 0,
+// which sorts below every composite.
+template <int PER>
+__device__ __forceinline__ void warp_load(const uint64_t* c, int n, uint64_t (&val)[PER]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) val[j] = j * 32 + lane < n ? c[j * 32 + lane] : 0ull;
+}
+
+// Exact radix select of the k largest of c[0..n) into out[0..k) (unordered),
+// by one warp with a warp-private histogram (plain shared atomics measured
+// faster here than aggregating equal digits with a match first).
+template <int KEY_BITS>
+__device__ void warp_radix_select(SelShared& s, const uint64_t* c, int n, int k, uint64_t* out) {
+  const int lane = threadIdx.x & 31;
+  constexpr int NKD = KEY_BITS / 8;
+  uint64_t prefix = 0, pmask = 0;
+  int need = k;
+#pragma unroll 1
+  for (int d = 0; d < NKD + 3; ++d) {
+    const int sh = d < NKD ? 32 + KEY_BITS - 8 * (d + 1) : 8 * (NKD + 2 - d);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s.shist[lane * 8 + j] = 0;
+    __syncwarp();
+    for (int i0 = 0; i0 < n; i0 += 32) {
+      const int i = i0 + lane;
+      const uint64_t x = i < n ? c[i] : 0ull;
+      const bool valid = i < n && (x & pmask) == prefix;
+      const uint32_t bin = static_cast<uint32_t>(x >> sh) & 0xffu;
+      if (valid) atomicAdd(&s.shist[bin], 1u);
+    }
+    __syncwarp();
+    uint32_t h[8], tot = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      h[j] = s.shist[255 - 8 * lane - j];
+      tot += h[j];
+    }
+    uint32_t incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const uint32_t excl = incl - tot;
+    int bin = -1, above = 0, cnt = 0;
+    if (excl < static_cast<uint32_t>(need) && static_cast<uint32_t>(need) <= incl) {
+      uint32_t acc = excl;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (bin < 0 && acc + h[j] >= static_cast<uint32_t>(need)) {
+          bin = 255 - 8 * lane - j;
+          above = static_cast<int>(acc);
+          cnt = static_cast<int>(h[j]);
+        }
+        acc += h[j];
+      }
+    }
+    const int src = __ffs(__ballot_sync(FULL, bin >= 0)) - 1;
+    bin = __shfl_sync(FULL, bin, src);
+    above = __shfl_sync(FULL, above, src);
+    cnt = __shfl_sync(FULL, cnt, src);
+    need -= above;
+    prefix |= static_cast<uint64_t>(bin) << sh;
+    pmask |= 0xffull << sh;
+    __syncwarp();
+    if (cnt == need) break;
+  }
+  int base = 0;
+  for (int i0 = 0; i0 < n; i0 += 32) {
+    const int i = i0 + lane;
+    const uint64_t x = i < n ? c[i] : 0ull;
+    const bool take = i < n && (x & pmask) >= prefix;
+    const unsigned bal = __ballot_sync(FULL, take);
+    if (take) out[base + __popc(bal & ((1u << lane) - 1u))] = x;
+    base += __popc(bal);
+  }
+  __syncwarp();
+}
+
+// Exact top-k (k <= 128) of c[0..n), sorted descending, by one warp: a
+// radix select cuts larger sets to k, then a 128-wide register bitonic
+// network sorts them.  Returns min(n, k); val[j] holds rank j*32 + lane.
+template <int KEY_BITS>
+__device__ int warp_select_sort(SelShared& s, const uint64_t* c, int n, int k, uint64_t (&val)[4]) {
+  const int kk = n < k ? n : k;
+  if (n <= k) {
+    warp_load<4>(c, n, val);
+  } else {
+    warp_radix_select<KEY_BITS>(s, c, n, k, s.ssel);
+    warp_load<4>(s.ssel, k, val);
+  }
+  warp_bitonic_desc<4>(val);
   return kk;
 }
 
@@ -871,7 +894,7 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
     }
     // candidate buffer of this row (the selector may still drain it from two rows ago)
     const int q = static_cast<int>(lr & 1);
-    const CandBuf cb{s.cand[q], &s.count[q]};
+    const CandBuf cb{s.cand[q], &s.count[q], SX_CAP};
     // bound: min over consumer warps of the warp's jth-largest thread maximum
     const uint32_t wb = warp_kth_largest<E::KEY_BITS>(rm.key(nonfinite), jth);
     if (lane == 0) s.warp_bound[warp] = wb;
@@ -957,13 +980,19 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
       }
       if (tail_id < a.V && tail_key >= bound && !robust) {
         const int pos = atomicAdd(cb.n, 1);
-        if (pos < SX_CAP) cb.c[pos] = make_comp(tail_key, static_cast<uint32_t>(tail_id));
+        if (pos < cb.cap) cb.c[pos] = make_comp(tail_key, static_cast<uint32_t>(tail_id));
       }
     }
     csync();
     if (*cb.n > SX_CAP || robust || q_over) {
-      // massive ties at the bound: redo the row in id order from global memory
-      select_row_fallback<T>(s, cb, row, a.V, a.S, nonfinite, overflow);
+      // massive ties at the bound: redo the row in id order from global
+      // memory, with the (now idle) queue storage as the candidate buffer,
+      // then hand the selector the exact top-|S|
+      const CandBuf fb{reinterpret_cast<uint64_t*>(s.qvec), &s.count[q], SX_FB_CAP};
+      select_row_fallback<T>(s, fb, row, a.V, a.S, nonfinite, overflow);
+      select_topk<E::KEY_BITS>(s, fb, *fb.n, a.S);
+      for (int i = tid; i < *fb.n; i += SX_CONS) cb.c[i] = fb.c[i];
+      csync();
     }
     // hand the candidates to the selector warp and move on to the next row
     if (tid == 0) {
