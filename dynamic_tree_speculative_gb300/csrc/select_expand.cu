@@ -790,6 +790,8 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
     s.timeout = 0;
   }
   __syncthreads();  // the last CTA-wide barrier: the roles split below
+  grid_dependency_wait();
+  grid_dependents_launch();
 
   if (warp == SX_SEL_WARP) {
     // ------------------------------------------------------------ selector ---
@@ -1037,14 +1039,15 @@ cudaError_t launch_select_expand(int dtype, const SelLaunch& L, cudaStream_t str
     cudaError_t err = cudaFuncSetAttribute(select_expand_kernel<__nv_bfloat16>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    select_expand_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), SX_THREADS, smem, stream>>>(a);
+    return launch_pdl(select_expand_kernel<__nv_bfloat16>, dim3(static_cast<unsigned>(grid)), dim3(SX_THREADS), smem,
+                      stream, a);
   } else {
     cudaError_t err = cudaFuncSetAttribute(select_expand_kernel<float>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    select_expand_kernel<float><<<static_cast<unsigned>(grid), SX_THREADS, smem, stream>>>(a);
+    return launch_pdl(select_expand_kernel<float>, dim3(static_cast<unsigned>(grid)), dim3(SX_THREADS), smem, stream,
+                      a);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace st

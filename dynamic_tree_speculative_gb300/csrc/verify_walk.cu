@@ -231,6 +231,8 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
   const float Tmp = L.p.temperature;
   const float c = LOG2E / Tmp;
   const int64_t nb = static_cast<int64_t>(b) * t.max_nodes;
+  grid_dependency_wait();  // the tree comes from the previous kernel
+  grid_dependents_launch();
   const int n_nodes = min(t.n_nodes[b], t.max_nodes);
   const int64_t row_bytes = L.row_stride * E::ES;
   const uint8_t* tgt = static_cast<const uint8_t*>(L.target);
@@ -562,8 +564,7 @@ cudaError_t launch_verify_c(const VerifyLaunch& L, cudaStream_t stream) {
   const int smem = static_cast<int>(sizeof(VerShared));
   cudaError_t err = cudaFuncSetAttribute(verify_kernel<T, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  verify_kernel<T, C><<<L.B * C, VER_THREADS, smem, stream>>>(L);
-  return cudaGetLastError();
+  return launch_pdl(verify_kernel<T, C>, dim3(L.B * C), dim3(VER_THREADS), smem, stream, L);
 }
 
 template <typename T>
