@@ -12,15 +12,19 @@
 // The walk is sequential in depth, so the latency of one level is what
 // matters: every level's target row is split over the C CTAs of the tree's
 // cluster (C chosen so that the whole batch fits in one wave).  Each of the
-// 32*C warps owns a contiguous slice of the row and keeps the slice's maximum
-// and sum of exp2((t - max) * log2(e) / T).  After a cluster barrier the
-// leader CTA reads the slice statistics of all CTAs through distributed
-// shared memory, forms the row normaliser, gathers exact p at the <= |S|
-// support tokens of the node's draft row, forms the residual in parallel and
-// lets thread 0 take the <= K decisions; a second cluster barrier publishes
-// the outcome.  For the bonus token the slice masses locate the slice that
-// holds it, and the leader reads only that slice again, scanning it in
-// token-id order.
+// 32*C warps owns a contiguous slice of the row, loads all of it in one batch
+// of predicated 16-byte loads (one memory latency per level) and keeps the
+// slice's maximum and sum of exp2((t - max) * log2(e) / T) with packed
+// float32x2 arithmetic.  Each warp pushes its two numbers into the leader
+// CTA's shared memory (distributed shared memory) and arrives on the leader's
+// mbarrier; no cluster-wide barrier is taken per level.  The leader forms the
+// row normaliser, turns the target logits of the node's <= |S| support tokens
+// (loaded at the start of the level, with the support itself prefetched when
+// the previous level decided) into exact p, forms the residual in parallel and
+// lets thread 0 take the <= K decisions, which it pushes to the other CTAs
+// with a remote mbarrier arrival.  For the bonus token the slice masses locate
+// the slice that holds it, and the leader reads only that slice again,
+// scanning it in token-id order.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -50,10 +54,11 @@ struct VerShared {
   float p_sup[SPEC_TREE_MAX_SUPPORT];          // p at support ranks of the node's draft row
   float qt_sup[SPEC_TREE_MAX_SUPPORT];         // q~_T at support ranks (0 off the tail)
   float w_sup[SPEC_TREE_MAX_SUPPORT];          // residual at support ranks
-  float slice_m[VER_WARPS];                    // this CTA's slices: maximum logit
-  float slice_s[VER_WARPS];                    //   and sum of exp2((t - slice max) * c)
-  float all_m[VER_MAX_SLICES];                 // leader: every slice of the cluster
-  float all_s[VER_MAX_SLICES];
+  float all_m[2][VER_MAX_SLICES];              // leader, per level parity: every slice's maximum logit
+  float all_s[2][VER_MAX_SLICES];              //   and sum of exp2((t - slice max) * c)
+  uint64_t stats_bar[2];                       // leader: all slices of the level have arrived
+  uint64_t dec_bar[2];                         // the leader's decision for the level has arrived
+  int dec[2];                                  //   accepted child node, or -1
   float slice_corr[VER_MAX_SLICES];            // leader: per slice, sum over corrected tokens of (p - w)
   float red[VER_WARPS];
   int32_t corr_tok[SPEC_TREE_MAX_SUPPORT];     // corrected tokens inside the bonus slice
@@ -133,76 +138,181 @@ __device__ __forceinline__ int slice_of_token(int v, int ns, int nvec, int vec) 
   return min((v / vec) / per, ns - 1);
 }
 
-// Statistics of this warp's slice: maximum and sum of exp2((t - max) * c),
-// c = log2(e) / T.  Per lane: online maximum with rescaling, compensated
-// float32 sums of vector sums; lanes combine in float32.
+// ------------------------------------------------- packed float32x2 math ---
+// Two IEEE float32 operations per instruction (round to nearest), so every
+// result equals its scalar counterpart.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 ra, rb, rr;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " add.rn.f32x2 rr, ra, rb;\n mov.b64 {%0, %1}, rr;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 ra, rb, rr;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " sub.rn.f32x2 rr, ra, rb;\n mov.b64 {%0, %1}, rr;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 ra, rb, rr;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rr, ra, rb;\n mov.b64 {%0, %1}, rr;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+// The 16-byte vector as float pairs: element (2j, 2j+1) in pair j.
 template <typename T>
-__device__ void slice_stats(VerShared& s, const uint8_t* row, int V, int g, int ns, float c, bool& nonfinite) {
+struct Pairs;
+template <>
+struct Pairs<__nv_bfloat16> {
+  static constexpr int N = 4;
+  __device__ static __forceinline__ float2 get(const uint4& v, int j) {
+    const uint32_t w = (j == 0) ? v.x : (j == 1) ? v.y : (j == 2) ? v.z : v.w;
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
+  __device__ static __forceinline__ uint4 neg_inf() { return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u); }
+};
+template <>
+struct Pairs<float> {
+  static constexpr int N = 2;
+  __device__ static __forceinline__ float2 get(const uint4& v, int j) {
+    return j == 0 ? make_float2(__uint_as_float(v.x), __uint_as_float(v.y))
+                  : make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+  }
+  __device__ static __forceinline__ uint4 neg_inf() { return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u); }
+};
+
+// Statistics of warp slice g of ns: maximum and sum of exp2((t - max) * c),
+// c = log2(e) / T.  Every lane loads its vectors of the slice in batches of
+// eight predicated 16-byte loads issued together (a 128K-token row split over
+// 64 slices is one batch, so one memory latency); per batch the lane's
+// running maximum is raised once, then each vector's elements contribute
+// exp2((t - max) * c) in float pairs, and the vector sums enter a compensated
+// per-lane sum.  Vectors holding NaN or +inf are left out and reported.
+// Lanes combine in float32; lane 0 returns the slice's (max, sum).
+template <typename T>
+__device__ void slice_stats(const uint8_t* row, int V, int g, int ns, float c, bool& nonfinite, float& m_out,
+                            float& s_out) {
   using E = VElem<T>;
+  using P = Pairs<T>;
   constexpr int VEC = E::VEC;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int BATCH = 8;
+  const int lane = threadIdx.x & 31;
   const int nvec = static_cast<int>((static_cast<int64_t>(V) * E::ES) / 16);
   const Slice sl(g, ns, nvec);
-  float m_run = -INFINITY, s_run = 0.0f, comp = 0.0f;
-  auto rescale = [&](float vm) {
-    const float f = ex2((m_run - vm) * c);
-    s_run *= f;
-    comp *= f;
-    m_run = vm;
-  };
-  auto consume = [&](const uint4& v) {
-    const float vm = E::vmax(v);
-    if (!(vm < INFINITY)) {  // NaN or +inf in the row
-      nonfinite = true;
-      return;
-    }
-    if (vm == -INFINITY) return;
-    if (vm > m_run) rescale(vm);
-    float vs = 0.0f;
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) vs += ex2((E::get(v, j) - m_run) * c);
-    const float y = vs - comp;
-    const float t = s_run + y;
-    comp = (t - s_run) - y;
-    s_run = t;
-  };
   const uint4* rv = reinterpret_cast<const uint4*>(row);
-  int i = sl.v0 + lane;
-  for (; i + 224 < sl.v1; i += 256) {
-    uint4 v[8];
+  float m_run = -INFINITY;
+  float2 s_run = make_float2(0.0f, 0.0f), comp = make_float2(0.0f, 0.0f);
+  for (int base = sl.v0; base < sl.v1; base += 32 * BATCH) {
+    uint4 v[BATCH];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = ldg_stream(rv + i + 32 * u);
+    for (int k = 0; k < BATCH; ++k) {
+      const int i = base + lane + 32 * k;
+      v[k] = i < sl.v1 ? ldg_stream(rv + i) : P::neg_inf();
+    }
+    float bm = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) consume(v[u]);
+    for (int k = 0; k < BATCH; ++k) {
+      const float vm = E::vmax(v[k]);
+      if (!(vm < INFINITY)) {  // NaN or +inf: left out, reported
+        nonfinite = true;
+        v[k] = P::neg_inf();
+      } else {
+        bm = fmaxf(bm, vm);
+      }
+    }
+    if (bm > m_run) {
+      const float f = ex2((m_run - bm) * c);
+      s_run = mul2(s_run, make_float2(f, f));
+      comp = mul2(comp, make_float2(f, f));
+      m_run = bm;
+    }
+    if (m_run == -INFINITY) continue;
+    const float2 mm = make_float2(m_run, m_run), cc = make_float2(c, c);
+#pragma unroll
+    for (int k = 0; k < BATCH; ++k) {
+      float2 vs = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int j = 0; j < P::N; ++j) {
+        const float2 y = mul2(sub2(P::get(v[k], j), mm), cc);
+        vs = add2(vs, make_float2(ex2(y.x), ex2(y.y)));
+      }
+      // compensated accumulation of the vector sums (pairwise lanes)
+      const float2 yk = sub2(vs, comp);
+      const float2 tk = add2(s_run, yk);
+      comp = sub2(sub2(tk, s_run), yk);
+      s_run = tk;
+    }
   }
-  for (; i + 96 < sl.v1; i += 128) {
-    uint4 v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = ldg_stream(rv + i + 32 * u);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) consume(v[u]);
-  }
-  for (; i < sl.v1; i += 32) consume(ldg_stream(rv + i));
+  float s_lane = (s_run.x - comp.x) + (s_run.y - comp.y);
   if (g == ns - 1) {
     const int tk = nvec * VEC + lane;
     if (tk < V) {
       const float x = E::load(row, tk);
       if (!(x < INFINITY)) nonfinite = true;
       if (x > -INFINITY && x < INFINITY) {
-        if (x > m_run) rescale(x);
-        s_run += ex2((x - m_run) * c);
+        if (x > m_run) {
+          s_lane *= ex2((m_run - x) * c);
+          m_run = x;
+        }
+        s_lane += ex2((x - m_run) * c);
       }
     }
   }
   float m = m_run;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
-  float part = (m_run == -INFINITY) ? 0.0f : (s_run - comp) * ex2((m_run - m) * c);
+  float part = (m_run == -INFINITY) ? 0.0f : s_lane * ex2((m_run - m) * c);
   part = warp_sum(part);
-  if (lane == 0) {
-    s.slice_m[warp] = m;
-    s.slice_s[warp] = part;
+  m_out = m;
+  s_out = part;
+}
+
+// ------------------------------------------------- cluster signalling ---
+
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Arrival on an mbarrier of a CTA of the cluster, ordered after this
+// thread's earlier stores (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+// Bounded wait (as mbar_wait) with acquire at cluster scope, so that stores
+// made by other CTAs before their arrivals are visible.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+  const uint32_t addr = smem_u32(bar);
+  for (uint32_t it = 0; it < WAIT_LIMIT; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(addr), "r"(parity), "r"(WAIT_SUSPEND_NS)
+        : "memory");
+    if (done) return true;
   }
+  return false;
 }
 
 // Support rank of the child in sibling slot `slot` (DET 0..m-1 -> ranks
@@ -237,6 +347,13 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
   const int64_t row_bytes = L.row_stride * E::ES;
   const uint8_t* tgt = static_cast<const uint8_t*>(L.target);
   const int nvec = static_cast<int>((static_cast<int64_t>(V) * E::ES) / 16);
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.stats_bar[i], NS);  // one arrival per warp of the cluster
+      mbar_init(&s.dec_bar[i], 1);
+    }
+    fence_mbar_init();
+  }
   if (leader) {
     for (int i = tid; i < n_nodes; i += VER_THREADS) {
       s.nd_parent[i] = t.node_parent[nb + i];
@@ -244,51 +361,63 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
       s.nd_exp_row[i] = t.node_exp_row[nb + i];
       s.nd_token[i] = t.node_token[nb + i];
     }
-    __syncthreads();
   }
-  bool nonfinite = false;
+  cluster.sync();  // barriers initialised cluster-wide before any remote arrival
+  bool nonfinite = false, timed_out = false;
   int node = 0, level = 0;
   int32_t* ot = L.out_tok + static_cast<int64_t>(b) * (D + 1);
   int32_t* on = L.out_node + static_cast<int64_t>(b) * (D + 1);
-  VerShared* lead = cluster.map_shared_rank(&s, 0);
-  // support of the current node's draft row, prefetched per level by the leader
-  int sup_v = -1;
+  // where this warp's slice statistics go in the leader's shared memory
+  const uint32_t lead_m0 = cluster_addr(&s.all_m[0][cr * VER_WARPS + warp], 0);
+  const uint32_t lead_m1 = cluster_addr(&s.all_m[1][cr * VER_WARPS + warp], 0);
+  const uint32_t lead_s0 = cluster_addr(&s.all_s[0][cr * VER_WARPS + warp], 0);
+  const uint32_t lead_s1 = cluster_addr(&s.all_s[1][cr * VER_WARPS + warp], 0);
+  const uint32_t lead_bar0 = cluster_addr(&s.stats_bar[0], 0);
+  const uint32_t lead_bar1 = cluster_addr(&s.stats_bar[1], 0);
+  // support of the current node's draft row (leader): prefetched when the
+  // previous level decided (for the root: now)
+  int sup_v = -1, pp = -1;
   float sup_qt = 0.0f, zT = 0.0f;
-  int pp = -1;
-  while (true) {
-    const uint8_t* row = tgt + (nb + node) * row_bytes;
-    int er = -1;
-    if (leader) {
-      er = level < D ? s.nd_exp_row[node] : -1;
-      if (er >= 0) {  // issued now, consumed after the row statistics
-        const int64_t srow = static_cast<int64_t>(b) * t.n_rows + er;
-        if (tid < S) {
-          sup_v = t.sup_id[srow * t.sup_stride + tid];
-          sup_qt = t.sup_qT[srow * t.sup_stride + tid];
-        }
-        zT = t.sup_zT[srow];
-        pp = t.probe_pos[srow];
-      }
+  auto load_support = [&](int er) {
+    if (er < 0) return;
+    const int64_t srow = static_cast<int64_t>(b) * t.n_rows + er;
+    if (tid < S) {
+      sup_v = t.sup_id[srow * t.sup_stride + tid];
+      sup_qt = t.sup_qT[srow * t.sup_stride + tid];
     }
-    slice_stats<T>(s, row, V, cr * VER_WARPS + warp, NS, c, nonfinite);
-    cluster.sync();  // A: every slice of the row is summarised
+    zT = t.sup_zT[srow];
+    pp = t.probe_pos[srow];
+  };
+  if (leader) load_support(D > 0 ? s.nd_exp_row[0] : -1);
+  while (true) {
+    const int par = level & 1;
+    const uint32_t wpar = static_cast<uint32_t>((level >> 1) & 1);
+    const uint8_t* row = tgt + (nb + node) * row_bytes;
+    const int er = leader && level < D ? s.nd_exp_row[node] : -1;
+    float wm, ws;
+    slice_stats<T>(row, V, cr * VER_WARPS + warp, NS, c, nonfinite, wm, ws);
+    // target logits of the support tokens, landing while the slices arrive
+    float t_sup = 0.0f;
+    if (er >= 0 && tid < S) t_sup = E::load(row, sup_v);
+    if (lane == 0) {
+      st_cluster_f32(par ? lead_m1 : lead_m0, wm);
+      st_cluster_f32(par ? lead_s1 : lead_s0, ws);
+      mbar_arrive_cluster(par ? lead_bar1 : lead_bar0);
+    }
+    int acc;
     if (leader) {
-      if (tid < NS) {
-        const VerShared* src = cluster.map_shared_rank(&s, tid / VER_WARPS);
-        s.all_m[tid] = src->slice_m[tid % VER_WARPS];
-        s.all_s[tid] = src->slice_s[tid % VER_WARPS];
-      }
+      if (!mbar_wait_cluster(&s.stats_bar[par], wpar)) timed_out = true;
       if (tid < K) s.kid_by_slot[tid] = -1;
-      __syncthreads();
       if (warp == 0) {
         // row maximum and normaliser (compensated per lane, pairwise across lanes)
         float mx = -INFINITY;
-        for (int g = lane; g < NS; g += 32) mx = fmaxf(mx, s.all_m[g]);
+        for (int g = lane; g < NS; g += 32) mx = fmaxf(mx, s.all_m[par][g]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
         float z = 0.0f, zc = 0.0f;
         for (int g = lane; g < NS; g += 32) {
-          const float x = s.all_m[g] > -INFINITY ? s.all_s[g] * ex2((s.all_m[g] - mx) * c) : 0.0f;
+          const float am = s.all_m[par][g];
+          const float x = am > -INFINITY ? s.all_s[par][g] * ex2((am - mx) * c) : 0.0f;
           const float y = x - zc;
           const float tt = z + y;
           zc = (tt - z) - y;
@@ -302,6 +431,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
           s.ncorr = 0;
         }
       }
+      __syncthreads();
       // children of the node by sibling slot; a node at depth D is a leaf
       // (which also bounds the walk for malformed trees)
       if (er >= 0)
@@ -320,7 +450,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
         const bool residual = probe_node >= 0;  // the tail residual applies iff the probe child survived
         float mn = 0.0f;
         if (tid < S) {
-          const float p = expf((E::load(row, sup_v) - M) / Tmp) * invZp;
+          const float p = expf((t_sup - M) / Tmp) * invZp;
           const float qt = (tid >= m && zT > 0.0f) ? sup_qt / zT : 0.0f;
           s.p_sup[tid] = p;
           s.qt_sup[tid] = qt;
@@ -387,9 +517,19 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
         s.accepted = -1;
       }
       if (tid == 0) s.nkids = nk;
+      __syncthreads();
+      acc = s.accepted;
+      // publish the decision to the other CTAs of the cluster
+      if (tid >= 1 && tid < C) {
+        st_cluster_s32(cluster_addr(&s.dec[par], tid), acc);
+        mbar_arrive_cluster(cluster_addr(&s.dec_bar[par], tid));
+      }
+      // the next node's support, while the decision travels
+      if (acc >= 0) load_support(level + 1 < D ? s.nd_exp_row[acc] : -1);
+    } else {
+      if (!mbar_wait_cluster(&s.dec_bar[par], wpar)) timed_out = true;
+      acc = s.dec[par];
     }
-    cluster.sync();  // B: the leader's decision is published
-    const int acc = lead->accepted;
     if (acc >= 0) {
       node = acc;
       ++level;
@@ -416,7 +556,8 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
         const int g = lane * PER + q;
         float x = 0.0f;
         if (g < NS) {
-          x = s.all_m[g] > -INFINITY ? s.all_s[g] * ex2((s.all_m[g] - M) * c) * invZp : 0.0f;
+          const float am = s.all_m[level & 1][g];
+          x = am > -INFINITY ? s.all_s[level & 1][g] * ex2((am - M) * c) * invZp : 0.0f;
           x -= s.slice_corr[g];
         }
         mass[q] = x;
@@ -555,7 +696,8 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
     break;
   }
   if (nonfinite) set_status(L.status, SPEC_TREE_S_NONFINITE_TARGET);
-  // no CTA leaves while a peer may still read its shared memory
+  if (timed_out) set_status(L.status, SPEC_TREE_S_TIMEOUT);
+  // no CTA leaves while another may still write to its shared memory
   cluster.sync();
 }
 
