@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libspec_tree.so")
 
 BF16, F32 = 0, 1
 BUILDER_TOPR, BUILDER_SMART = 0, 1
+PROBE_FIRST, PROBE_LAST = 0, 1
 ROOT, DET, PROBE, FILL = 0, 1, 2, 3
 OK, E_PARAM, E_LAYOUT, E_CUDA = 0, -1, -3, -4
 S_NONFINITE_DRAFT, S_NONFINITE_TARGET, S_RESIDUAL_EMPTY = 1, 2, 4
@@ -38,7 +39,7 @@ class c_params(ctypes.Structure):
                 ("R", ctypes.c_int32), ("support", ctypes.c_int32), ("temperature", ctypes.c_float),
                 ("builder", ctypes.c_int32), ("lam", ctypes.c_float), ("beta", ctypes.c_float),
                 ("gamma", ctypes.c_float), ("delta", ctypes.c_float), ("rho", ctypes.c_float),
-                ("eta", ctypes.c_float), ("alpha", ctypes.c_float)]
+                ("eta", ctypes.c_float), ("alpha", ctypes.c_float), ("verify_order", ctypes.c_int32)]
 
 
 class c_tree(ctypes.Structure):
@@ -87,17 +88,19 @@ class Params:
     rho: float = 1.3
     eta: float = 0.0
     alpha: float = 1.0
+    verify_order: int = PROBE_FIRST
 
     def c(self) -> c_params:
         return c_params(self.K, self.m, self.W, self.depth, self.R, self.support, self.temperature, self.builder,
-                        self.lam, self.beta, self.gamma, self.delta, self.rho, self.eta, self.alpha)
+                        self.lam, self.beta, self.gamma, self.delta, self.rho, self.eta, self.alpha,
+                        self.verify_order)
 
     @staticmethod
     def from_workload(wl) -> "Params":
         return Params(K=wl.K, m=wl.m, W=wl.W, depth=wl.depth, R=wl.R, temperature=wl.temperature,
                       support=wl.support, builder=BUILDER_SMART if wl.builder == "smart" else BUILDER_TOPR,
                       lam=wl.lam, beta=wl.beta, gamma=wl.gamma, delta=wl.delta, rho=wl.rho, eta=wl.eta,
-                      alpha=wl.alpha)
+                      alpha=wl.alpha, verify_order=PROBE_LAST if wl.verify_order == "rrsw" else PROBE_FIRST)
 
 
 def _cp(params) -> c_params:

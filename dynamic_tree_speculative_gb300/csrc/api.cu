@@ -76,7 +76,8 @@ int spec_tree_check_params(const spec_tree_params* p, int V) {
   if (V < 1 || V >= (1 << 24)) return SPEC_TREE_E_PARAM;
   if (p->support < 0 || p->support > SPEC_TREE_MAX_SUPPORT) return SPEC_TREE_E_PARAM;
   const int S = support_size(p, V);
-  if (p->K < 1 || p->K > S || p->m < 0 || p->m >= p->K) return SPEC_TREE_E_PARAM;
+  if (p->K < 1 || p->K > S || p->m < 0 || p->m > p->K) return SPEC_TREE_E_PARAM;
+  if (p->verify_order != SPEC_TREE_PROBE_FIRST && p->verify_order != SPEC_TREE_PROBE_LAST) return SPEC_TREE_E_PARAM;
   if (p->depth < 1 || p->depth > 255 || p->R < 1 || p->R + 1 > SPEC_TREE_MAX_NODES) return SPEC_TREE_E_PARAM;
   if (!(p->temperature > 0.0f) || !isfinite(p->temperature)) return SPEC_TREE_E_PARAM;
   if (p->builder == SPEC_TREE_BUILDER_TOPR) {
@@ -114,6 +115,7 @@ int spec_tree_select_expand(const spec_tree_params* p, int B, int V, int dtype, 
   L.V = V;
   L.S = support_size(p, V);
   L.m = p->m;
+  L.draw_probe = p->m < p->K;
   L.temperature = p->temperature;
   L.u_probe = u_probe;
   L.sup_id = tree->sup_id;

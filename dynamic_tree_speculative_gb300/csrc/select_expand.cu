@@ -503,6 +503,7 @@ struct SelArgs {
   int V;
   int S;
   int m;
+  int draw_probe;
   float temperature;
   const float* u_probe;
   int32_t* sup_id;
@@ -731,7 +732,7 @@ __device__ void expand_epilogue(const uint64_t (&val)[4], const SelArgs& a, int6
     }
   }
   int probe = -1;
-  if (a.m < n_sup && teT > 0.0f) {
+  if (a.draw_probe && a.m < n_sup && teT > 0.0f) {
     const float target = a.u_probe[out_row] * teT;
     float carry = 0.0f;
     int last = -1;
@@ -1022,6 +1023,7 @@ cudaError_t launch_select_expand(int dtype, const SelLaunch& L, cudaStream_t str
   a.V = L.V;
   a.S = L.S;
   a.m = L.m;
+  a.draw_probe = L.draw_probe ? 1 : 0;
   a.temperature = L.temperature;
   a.u_probe = L.u_probe;
   a.sup_id = L.sup_id;

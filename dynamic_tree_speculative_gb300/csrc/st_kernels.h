@@ -15,6 +15,7 @@ struct SelLaunch {
   int64_t n_rows;      // rows per tree in memory
   int64_t rows_used;   // rows per tree to process
   int B, V, S, m;
+  bool draw_probe;  // m < K: a probe child exists
   float temperature;
   const float* u_probe;
   int32_t* sup_id;

@@ -446,8 +446,10 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
         for (int k = 0; k < K; ++k) nk += s.kid_by_slot[k] >= 0;
       const float M = s.M, invZp = s.invZp;
       if (nk > 0) {
-        const int probe_node = (pp >= 0) ? s.kid_by_slot[m] : -1;
-        const bool residual = probe_node >= 0;  // the tail residual applies iff the probe child survived
+        const int probe_node = (pp >= 0 && m < K) ? s.kid_by_slot[m] : -1;
+        const bool probe_last = L.p.verify_order == SPEC_TREE_PROBE_LAST;
+        // probe first: the tail residual applies to the one-hot children iff the probe child survived
+        const bool residual = probe_node >= 0 && !probe_last;
         float mn = 0.0f;
         if (tid < S) {
           const float p = expf((t_sup - M) / Tmp) * invZp;
@@ -465,7 +467,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
           int j = 0, accepted = -1;
           float Zr = 1.0f;
           bool empty = false;
-          if (probe_node >= 0) {
+          if (probe_node >= 0 && !probe_last) {
             const float p = s.p_sup[pp], qt = s.qt_sup[pp];
             const float u = uv[0];
             if (L.margins && fabsf(u * qt - p) < static_cast<float>(MASS_MARGIN)) atomicAdd(L.margins, 1u);
@@ -479,6 +481,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
             }
           }
           if (accepted < 0) {
+            // one-hot children in slot order (the probe, if any, is done above or last)
             for (int slot = 0; slot < K; ++slot) {
               const int kid = s.kid_by_slot[slot];
               if (kid < 0 || kid == probe_node) continue;
@@ -497,6 +500,29 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
               Zr -= w;
               s.w_sup[r] = 0.0f;
               ++j;
+            }
+            if (probe_last && accepted < 0 && !empty && probe_node >= 0) {
+              // the probe last, against the residual the one-hot rejections left
+              if (Zr <= 0.0f) {
+                empty = true;
+              } else {
+                const float w = s.w_sup[pp], qt = s.qt_sup[pp];
+                const float u = uv[j];
+                if (L.margins && fabsf(u * qt - w / Zr) < static_cast<float>(MASS_MARGIN)) atomicAdd(L.margins, 1u);
+                if (u * qt * Zr < w) {
+                  accepted = probe_node;
+                } else {
+                  // residual max(0, w - Zr q~_T) on the tail, of mass Zr - sum_tail min(w, Zr q~_T)
+                  float smin = 0.0f;
+                  for (int r = m; r < S; ++r) {
+                    const float a = s.w_sup[r], q2 = Zr * s.qt_sup[r];
+                    smin += fminf(a, q2);
+                    s.w_sup[r] = fmaxf(0.0f, a - q2);
+                  }
+                  Zr -= smin;
+                }
+                ++j;
+              }
             }
             if (accepted < 0 && !empty && Zr <= 0.0f) empty = true;
             if (empty) {

@@ -57,6 +57,7 @@ class Workload:
     rho: float = 1.3
     eta: float = 0.0
     alpha: float = 1.0
+    verify_order: str = "rheo"  # "rheo" (probe first) | "rrsw" (probe last)
 
     @property
     def n_exp(self) -> int:

@@ -58,6 +58,10 @@ typedef struct CUstream_st* spec_tree_stream_t;
 #define SPEC_TREE_BUILDER_TOPR 0  /* expand-then-rerank, frontier top-W, global top-R */
 #define SPEC_TREE_BUILDER_SMART 1 /* SMART marginal keep rule, budget R */
 
+/* verification orders */
+#define SPEC_TREE_PROBE_FIRST 0
+#define SPEC_TREE_PROBE_LAST 1
+
 /* node kinds */
 #define SPEC_TREE_ROOT 0
 #define SPEC_TREE_DET 1
@@ -86,7 +90,9 @@ typedef struct CUstream_st* spec_tree_stream_t;
 /*
  * Parameters of the method.
  *   K        children (slots) per expanded node, 1 <= K <= support.
- *   m        deterministic children (top-m), 0 <= m < K.
+ *   m        deterministic children (top-m), 0 <= m <= K.  m = K gives the
+ *            one-hot Top-K tree (every child deterministic, no probe): the
+ *            pages' Top-K baseline.
  *   W        frontier width: nodes expanded per layer (top-R builder).
  *   depth    D >= 1: layers of draft nodes.
  *   R        pruned tree size in draft nodes, root excluded (top-R builder);
@@ -97,12 +103,19 @@ typedef struct CUstream_st* spec_tree_stream_t;
  *   builder  SPEC_TREE_BUILDER_TOPR or SPEC_TREE_BUILDER_SMART.
  *   lambda, beta, gamma, delta, rho, eta, alpha: SMART cost model (units of
  *            one target decoding step) and discount; ignored by top-R.
+ *   verify_order SPEC_TREE_PROBE_FIRST: the probe is tested first and the
+ *            others are one-hot drafts under its residual (RheoSampling Key
+ *            design 3, optimal-transport verification); SPEC_TREE_PROBE_LAST:
+ *            the one-hot children first, the probe last against the residual
+ *            they leave (recursive rejection sampling with the probe as one
+ *            more draft, the pages' "Rheo + RRSw" ablation).
  */
 typedef struct spec_tree_params {
   int32_t K, m, W, depth, R, support;
   float temperature;
   int32_t builder;
   float lambda, beta, gamma, delta, rho, eta, alpha;
+  int32_t verify_order;
 } spec_tree_params;
 
 /*
@@ -190,12 +203,15 @@ int spec_tree_build(const spec_tree_params* p, int B, int V, int dtype,
 /*
  * Layer-by-layer verification of built trees (RheoSampling Key design 3).
  * For each tree, from the root: p = softmax(t / T) over the full vocabulary
- * of the current node's target row; the node's children are tested probe
- * first (accept iff u < p(x_s) / q~_T(x_s)), then, under the residual
- * w = max(0, p - q~_T) on the tail (w = p elsewhere, mass
+ * of the current node's target row.  With SPEC_TREE_PROBE_FIRST the node's
+ * children are tested probe first (accept iff u < p(x_s) / q~_T(x_s)), then,
+ * under the residual w = max(0, p - q~_T) on the tail (w = p elsewhere, mass
  * Zr = 1 - sum_tail min(p, q~_T)), each remaining child x in slot order
  * (accept iff u < w(x) / Zr, else Zr -= w(x), w(x) = 0).  Without a probe
- * child, w = p and Zr = 1.  The j-th decision at level l uses
+ * child, w = p and Zr = 1.  With SPEC_TREE_PROBE_LAST the children other
+ * than the probe go first under w = p, Zr = 1 (as above), then the probe is
+ * accepted iff u < (w(x_s) / Zr) / q~_T(x_s), and on rejection the residual
+ * becomes max(0, w - Zr q~_T), of mass Zr - sum_tail min(w, Zr q~_T).  The j-th decision at level l uses
  * u_verify[b][l][j].  An accepted child becomes the node; when every child
  * is rejected or the node has none, the bonus token is the first token in id
  * order with u_bonus[b] * Zr < sum_{v' <= v} w(v').

@@ -160,6 +160,8 @@ def expand_row(row, p: Params, u_probe: float, force_probe_pos: Optional[int] = 
     * proxy = min{q(x_m), z} for m >= 1, and q(x_1) + eps (one ulp) for m = 0.
     * fillers: the next tail tokens in rank order, skipping x_s, until the
       node has min(K, |S|) children.
+    * m = K is the one-hot Top-K node (the pages' Top-K baseline): K
+      deterministic children and no probe (none is drawn).
     * slots: DET 0..m-1, PROBE m, FILL after; local probability q(child)
       (untempered), the proxy for the probe.
 
@@ -169,8 +171,8 @@ def expand_row(row, p: Params, u_probe: float, force_probe_pos: Optional[int] = 
     row = as_f64(row)
     V = row.shape[0]
     S = min(p.support, V)
-    if p.K > S or p.m >= p.K or p.m < 0:
-        raise ValueError("need 0 <= m < K <= |S|")
+    if p.K > S or p.m > p.K or p.m < 0:
+        raise ValueError("need 0 <= m <= K <= |S|")
     sup = support_of(row, S)
     l = row[sup]
     q, qT, _, _ = truncated_softmax(l, p.temperature)
@@ -179,7 +181,7 @@ def expand_row(row, p: Params, u_probe: float, force_probe_pos: Optional[int] = 
     zT = float(qT[m:].sum())
     mg = Margins()
     probe_pos = -1
-    if m < S and zT > 0.0:
+    if m < p.K and m < S and zT > 0.0:
         if force_probe_pos is not None:
             probe_pos = int(force_probe_pos)
             assert m <= probe_pos < S and qT[probe_pos] > 0

@@ -162,7 +162,8 @@ def run_parity(wl: WL.Workload, seed: int, sample=None, row_stride=None, verify=
     if verify:
         op = oracle_params(wl)
         tnp = {b: WL.to_numpy_f64(target[b, :, :wl.V]) for b in idx}
-        results = {b: O.verify(trees[b], tnp[b], case.u_verify[b].numpy(), float(case.u_bonus[b]), op)
+        results = {b: O.verify(trees[b], tnp[b], case.u_verify[b].numpy(), float(case.u_bonus[b]), op,
+                               mode=wl.verify_order)
                    for b in idx}
         vx, vxm = compare_verify(g, trees, results)
         out.update(verify_exact=vx, verify_exempt=vxm, results=results)

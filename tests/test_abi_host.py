@@ -38,7 +38,10 @@ def test_rows_needed(binding):
 
 @pytest.mark.parametrize("kw,V,ok", [
     (dict(K=8, m=1, W=8, depth=8, R=60), 128256, True),
-    (dict(K=8, m=8, W=8, depth=8, R=60), 128256, False),    # m >= K
+    (dict(K=8, m=8, W=8, depth=8, R=60), 128256, True),     # m = K: one-hot Top-K tree
+    (dict(K=8, m=9, W=8, depth=8, R=60), 128256, False),    # m > K
+    (dict(K=8, m=1, W=8, depth=8, R=60, verify_order=1), 128256, True),   # probe last
+    (dict(K=8, m=1, W=8, depth=8, R=60, verify_order=2), 128256, False),  # unknown order
     (dict(K=8, m=1, W=8, depth=8, R=60), 5, False),         # K > |S| = V
     (dict(K=4, m=1, W=4, depth=3, R=8), 32, True),
     (dict(K=8, m=1, W=8, depth=0, R=60), 1000, False),      # depth < 1

@@ -75,6 +75,12 @@ EDGE = {
     "depth1": dict(V=3000, K=8, m=1, W=8, depth=1, R=8),
     "support_32": dict(V=3000, K=4, m=1, W=3, depth=3, R=10, support=32),
     "wide": dict(V=9000, K=16, m=1, W=16, depth=3, R=100),
+    # the pages' Top-K baseline: every child deterministic, no probe
+    "topk_m_eq_K": dict(V=3000, K=4, m=4, W=4, depth=4, R=16),
+    # probe-last verification (the pages' "Rheo + RRSw" ablation), with and without fillers
+    "rrsw": dict(V=3000, K=4, m=1, W=4, depth=4, R=16, verify_order="rrsw"),
+    "rrsw_no_fillers": dict(V=3000, K=2, m=1, W=2, depth=5, R=14, verify_order="rrsw"),
+    "rrsw_m0": dict(V=3000, K=3, m=0, W=3, depth=4, R=14, verify_order="rrsw"),
 }
 
 
@@ -183,3 +189,65 @@ def test_gpu_losslessness_chi_square():
         stat += (rest_o - rest_e) ** 2 / rest_e
     dof = keep.sum() + (1 if rest_e > 0 else 0) - 1
     assert chi2.sf(stat, dof) > 1e-3
+
+
+def _exact_level0_acceptance(rows, wl, target_row, mode):
+    """Probability (over the probe draw and the accept uniforms) that the root accepts a child."""
+    from oracle import spec_tree_oracle as O
+    op = parity.oracle_params(wl)
+    p_full = O.target_probs(WL.to_numpy_f64(target_row), wl.temperature)
+    ex0 = O.expand_row(rows[0], op, 0.5)
+    draws = [(1.0, 0.5)]
+    if ex0.probe_pos >= 0:
+        cum = np.cumsum(ex0.qT[op.m:])
+        draws = []
+        for s in range(op.m, len(ex0.q)):
+            lo = cum[s - op.m - 1] if s > op.m else 0.0
+            if ex0.qT[s] > 0:
+                draws.append((ex0.qT[s] / ex0.zT, (lo + cum[s - op.m]) / 2.0 / ex0.zT))
+    total = 0.0
+    for wgt, u in draws:
+        t = O.build(rows, np.array([u]), op)
+        kids = O.children_in_order(t, 0, mode)
+        steps, _, _ = O.level_thresholds(p_full, t.expansions[0], op.m, [int(t.token[j]) for j in kids],
+                                         [int(t.kind[j]) for j in kids], mode)
+        reach = 1.0
+        for _, _, a, _, _ in steps:
+            total += wgt * reach * a
+            reach *= 1.0 - a
+    return total
+
+
+def test_depth1_acceptance_of_the_three_verifiers():
+    """The pages' single-layer controlled experiment on the GPU path: one root with K = 2
+    children verified probe first (RheoSampling), probe last (Rheo + RRSw) and as one-hot
+    Top-K (m = K); each GPU acceptance rate over 20000 trees matches the oracle's exact
+    expectation, and probe first never accepts less than probe last (Key design 3)."""
+    from dynamic_tree_speculative_gb300 import binding as B
+    n = 20000
+    base = WL.WORKLOADS["tiny"].with_(B=n, K=2, m=1, W=2, depth=1, R=2)
+    rows, _ = WL.draft_logits(base.with_(B=1), 31, n_rows=1)
+    target_row = WL.latent_rows((31, "tgt-d1"), 1, base.V, 1.2, 0.5)[0]
+    dev = "cuda"
+    rates, exact = {}, {}
+    for name, wl in (("rheo", base), ("rrsw", base.with_(verify_order="rrsw")), ("topk", base.with_(m=2))):
+        params = B.Params.from_workload(wl)
+        draft = rows.expand(n, -1, -1).contiguous()
+        u_probe = WL.uniforms(41, "p", (n, 1))
+        uv, ub = WL.uniforms(41, "v", (n, 1, wl.K)), WL.uniforms(41, "b", (n,))
+        tree = B.TreeBuffers(params, n, device=dev)
+        out = B.VerifyOutputs(params, n, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        B.spec_tree_build(params, wl.V, draft.to(dev), u_probe.to(dev), tree, status)
+        target = target_row.reshape(1, 1, -1).expand(n, wl.R + 1, -1).contiguous()
+        B.spec_tree_verify(params, wl.V, target.to(dev), tree, uv.to(dev), ub.to(dev), out.accept_len,
+                           out.out_tok, out.out_node, None, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        rates[name] = float((out.accept_len >= 1).float().mean())
+        exact[name] = _exact_level0_acceptance(WL.to_numpy_f64(rows[0]), wl, target_row,
+                                               "rrsw" if name == "rrsw" else "rheo")
+        sd = (exact[name] * (1 - exact[name]) / n) ** 0.5
+        assert abs(rates[name] - exact[name]) < 5 * sd + 1e-9, (name, rates[name], exact[name])
+    print("depth-1 acceptance (gpu / exact):", {k: (round(rates[k], 4), round(exact[k], 4)) for k in rates})
+    assert exact["rheo"] >= exact["rrsw"] - 1e-12

@@ -469,6 +469,40 @@ def test_no_probe_reduces_to_one_hot_recursive_rejection():
     assert checked >= 10
 
 
+def test_m_equal_k_is_the_one_hot_topk_tree():
+    """m = K: K deterministic children (ranks 0..K-1), no probe drawn, one-hot recursive
+    rejection in verification, and the first emitted token still has law p exactly."""
+    p = O.Params(K=4, m=4, W=2, depth=3, R=12, temperature=1.0)
+    n_rows = 1 + (p.depth - 1) * p.W
+    for seed in range(8):
+        rows = _tiny_rows(700 + seed, n_rows)
+        rng = np.random.default_rng(seed)
+        t = O.build_topr(rows, rng.random(n_rows), p)
+        assert not (t.kind == O.PROBE).any()
+        for ex in t.expansions.values():
+            assert ex.probe_pos == -1
+            assert [(slot, kind, rank) for slot, kind, rank, _, _ in ex.children] == \
+                [(k, O.DET, k) for k in range(p.K)]
+        target = WL.to_numpy_f64(WL.latent_rows((seed, "tgt7"), t.n_nodes, 32, 1.2, 0.5))
+        for trial in range(10):
+            uv = rng.random((p.depth, p.K))
+            ub = float(rng.random())
+            res = O.verify(t, target, uv, ub, p)
+            nodes, bonus = _independent_onehot_walk(t, target, uv, ub, 1.0)
+            assert res.nodes == nodes and res.tokens[-1] == bonus
+        # exact law of the first token at the root
+        p_full = O.target_probs(target[0], p.temperature)
+        kids = O.children_in_order(t, 0)
+        steps, w, Zr = O.level_thresholds(p_full, t.expansions[0], p.m, [int(t.token[j]) for j in kids],
+                                          [int(t.kind[j]) for j in kids])
+        law, reach = np.zeros_like(p_full), 1.0
+        for _, x, a, _, _ in steps:
+            law[x] += reach * a
+            reach *= 1.0 - a
+        law += reach * w / Zr
+        np.testing.assert_allclose(law, p_full, atol=1e-12, rtol=0)
+
+
 # -------------------------------------------------------- multi-level chi^2 ---
 
 def _chi2_pvalue(counts, probs, n):
