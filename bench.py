@@ -35,7 +35,7 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama3_b64")
@@ -101,7 +101,8 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, window=None):
+        """Summary of the samples; `window` = (t0, t1) host times keeps those taken inside it."""
         if self.proc is None:
             return {"error": "nvidia-smi unavailable"}
         time.sleep(0.05)
@@ -119,13 +120,26 @@ class ClockSampler:
         os.unlink(self.path)
         if not rows:
             return {"error": "no samples"}
+        where = "warm-up + timed steps"
+        if window is not None:
+            inside = []
+            for r in rows:
+                try:
+                    ts = time.mktime(time.strptime(r[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + r[0].split(".")[1]) if "." in r[0] else 0.0
+                except Exception:
+                    continue
+                if window[0] - 0.01 <= ts <= window[1] + 0.01:
+                    inside.append(r)
+            if inside:
+                rows, where = inside, "timed steps"
         sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[k] for r in rows for k in range(4) if r[6 + k].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(rows), "interval_ms": 20,
-                "window": "warm-up + timed steps"}
+                "window": where}
 
 
 # ------------------------------------------------------------ CPU oracle ---
@@ -253,13 +267,15 @@ def run_ours(args):
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     R.barrier(info, dev)
     torch.cuda.synchronize()
+    host_t0 = time.time()
     t_start.record(stream)
     for k in range(K):
         step(evs[k])
     t_end.record(stream)
     torch.cuda.synchronize()
+    host_t1 = time.time()
     R.barrier(info, dev)
-    clk = clocks.stop()
+    clk = clocks.stop((host_t0, host_t1))
     elapsed = t_start.elapsed_time(t_end) / 1e3
     k1_s = statistics.mean(a.elapsed_time(b) for a, b in evs) / 1e3
     st = int(status.item())
