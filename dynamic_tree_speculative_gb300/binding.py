@@ -23,11 +23,12 @@ PROBE_FIRST, PROBE_LAST = 0, 1
 ROOT, DET, PROBE, FILL = 0, 1, 2, 3
 OK, E_PARAM, E_LAYOUT, E_CUDA = 0, -1, -3, -4
 S_NONFINITE_DRAFT, S_NONFINITE_TARGET, S_RESIDUAL_EMPTY = 1, 2, 4
-S_OVERFLOW, S_TIMEOUT, S_ROWS = 8, 16, 32
+S_OVERFLOW, S_TIMEOUT, S_ROWS, S_LAYERS = 8, 16, 32, 64
 MAX_SUPPORT = 128
 
 EXPORTS = ("spec_tree_rows_needed", "spec_tree_check_params", "spec_tree_select_expand", "spec_tree_rank",
-           "spec_tree_build", "spec_tree_verify", "spec_tree_strerror")
+           "spec_tree_build", "spec_tree_verify", "spec_tree_layer_state_bytes", "spec_tree_layer_rows",
+           "spec_tree_layer", "spec_tree_finish", "spec_tree_strerror")
 
 
 class SpecTreeError(RuntimeError):
@@ -60,10 +61,15 @@ def _load():
     lib.spec_tree_rank.argtypes = [P, i32, i32, T, vp, vp]
     lib.spec_tree_build.argtypes = [P, i32, i32, i32, vp, i64, vp, T, vp, vp]
     lib.spec_tree_verify.argtypes = [P, i32, i32, i32, vp, i64, T, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.spec_tree_layer_state_bytes.argtypes = []
+    lib.spec_tree_layer_state_bytes.restype = ctypes.c_size_t
+    lib.spec_tree_layer_rows.argtypes = [P, i32]
+    lib.spec_tree_layer.argtypes = [P, i32, i32, i32, i32, vp, i64, vp, T, vp, vp, vp, vp, vp]
+    lib.spec_tree_finish.argtypes = [P, i32, i32, T, vp, vp, vp]
     lib.spec_tree_strerror.argtypes = [i32]
     lib.spec_tree_strerror.restype = ctypes.c_char_p
     for name in EXPORTS:
-        if name != "spec_tree_strerror":
+        if name not in ("spec_tree_strerror", "spec_tree_layer_state_bytes"):
             getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -202,6 +208,39 @@ def spec_tree_verify(params: Params, V: int, target: torch.Tensor, tree: TreeBuf
     _check(_lib.spec_tree_verify(ctypes.byref(_cp(params)), tree.B, V, _dtype_code(target), _ptr(target),
                                  _row_stride(target, tree.max_nodes), ctypes.byref(tree.c()), _ptr(u_verify),
                                  _ptr(u_bonus), _ptr(accept_len), _ptr(out_tok), _ptr(out_node), _ptr(margins),
+                                 _ptr(status), _stream(stream)))
+
+
+def spec_tree_layer_state_bytes() -> int:
+    return _lib.spec_tree_layer_state_bytes()
+
+
+def spec_tree_layer_rows(params: Params, layer: int) -> int:
+    return _lib.spec_tree_layer_rows(ctypes.byref(_cp(params)), layer)
+
+
+class LayerState:
+    """Caller-owned per-tree state of the layer-by-layer builder, and the frontier it names."""
+
+    def __init__(self, params: Params, B: int, device="cuda"):
+        self.B = B
+        self.state = torch.empty((B, spec_tree_layer_state_bytes()), dtype=torch.uint8, device=device)
+        self.frontier_token = torch.empty((B, params.W), dtype=torch.int32, device=device)
+        self.frontier_parent = torch.empty((B, params.W), dtype=torch.int32, device=device)
+
+
+def spec_tree_layer(params: Params, V: int, layer: int, layer_draft: torch.Tensor, u_probe: torch.Tensor,
+                    tree: TreeBuffers, state: LayerState, status: torch.Tensor, stream=None):
+    rows = spec_tree_layer_rows(params, layer)
+    _check(_lib.spec_tree_layer(ctypes.byref(_cp(params)), tree.B, V, layer, _dtype_code(layer_draft),
+                                _ptr(layer_draft), _row_stride(layer_draft, rows), _ptr(u_probe),
+                                ctypes.byref(tree.c()), _ptr(state.state), _ptr(state.frontier_token),
+                                _ptr(state.frontier_parent), _ptr(status), _stream(stream)))
+
+
+def spec_tree_finish(params: Params, V: int, tree: TreeBuffers, state: LayerState, status: torch.Tensor,
+                     stream=None):
+    _check(_lib.spec_tree_finish(ctypes.byref(_cp(params)), tree.B, V, ctypes.byref(tree.c()), _ptr(state.state),
                                  _ptr(status), _stream(stream)))
 
 

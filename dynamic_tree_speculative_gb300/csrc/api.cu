@@ -109,7 +109,9 @@ int spec_tree_select_expand(const spec_tree_params* p, int B, int V, int dtype, 
   st::SelLaunch L;
   L.logits = draft_logits;
   L.row_stride = row_stride;
+  L.in_rows = tree->n_rows;
   L.n_rows = tree->n_rows;
+  L.sup_row0 = 0;
   L.rows_used = needed < tree->n_rows ? needed : tree->n_rows;
   L.B = B;
   L.V = V;
@@ -146,6 +148,10 @@ int spec_tree_rank(const spec_tree_params* p, int B, int V, const spec_tree_t* t
   L.rows_avail = needed < tree->n_rows ? needed : tree->n_rows;
   L.tree = *tree;
   L.status = status;
+  L.layer = 0;
+  L.state = nullptr;
+  L.frontier_token = nullptr;
+  L.frontier_parent = nullptr;
   const cudaError_t err = p->builder == SPEC_TREE_BUILDER_SMART ? st::launch_rank_smart(L, as_stream(stream))
                                                                  : st::launch_rank_topr(L, as_stream(stream));
   return err == cudaSuccess ? SPEC_TREE_OK : SPEC_TREE_E_CUDA;
@@ -160,6 +166,92 @@ int spec_tree_build(const spec_tree_params* p, int B, int V, int dtype, const vo
   if ((rc = spec_tree_select_expand(p, B, V, dtype, draft_logits, row_stride, u_probe, tree, status, stream)))
     return rc;
   return spec_tree_rank(p, B, V, tree, status, stream);
+}
+
+size_t spec_tree_layer_state_bytes(void) { return st::layer_state_bytes(); }
+
+int spec_tree_layer_rows(const spec_tree_params* p, int layer) {
+  if (p == nullptr || p->builder != SPEC_TREE_BUILDER_TOPR || p->W < 1 || p->K < 1) return 0;
+  if (layer < 0 || layer >= p->depth) return 0;
+  if (layer == 0) return 1;
+  int64_t ln = p->K;  // size of layer 1
+  for (int d = 1; d < layer && ln <= SPEC_TREE_MAX_CAND; ++d) ln = (ln < p->W ? ln : p->W) * p->K;
+  return static_cast<int>(ln < p->W ? ln : p->W);
+}
+
+int spec_tree_layer(const spec_tree_params* p, int B, int V, int layer, int dtype, const void* layer_logits,
+                    int64_t row_stride, const float* u_probe, const spec_tree_t* tree, void* state,
+                    int32_t* frontier_token, int32_t* frontier_parent, uint32_t* status,
+                    spec_tree_stream_t stream) {
+  int rc = spec_tree_check_params(p, V);
+  if (rc) return rc;
+  if (p->builder != SPEC_TREE_BUILDER_TOPR || layer < 0 || layer >= p->depth) return SPEC_TREE_E_PARAM;
+  if (B < 0 || u_probe == nullptr || state == nullptr) return SPEC_TREE_E_PARAM;
+  if (!aligned16(state)) return SPEC_TREE_E_LAYOUT;
+  if ((rc = check_rows(dtype, layer_logits, row_stride, V))) return rc;
+  if ((rc = check_tree(p, tree, V, false, true))) return rc;
+  const int rows = spec_tree_layer_rows(p, layer);
+  const int row0 = layer == 0 ? 0 : 1 + (layer - 1) * p->W;
+  if (B == 0) return SPEC_TREE_OK;
+  st::SelLaunch S;
+  S.logits = layer_logits;
+  S.row_stride = row_stride;
+  S.in_rows = rows;
+  S.n_rows = tree->n_rows;
+  S.sup_row0 = row0;
+  S.rows_used = rows;
+  S.B = B;
+  S.V = V;
+  S.S = support_size(p, V);
+  S.m = p->m;
+  S.draw_probe = p->m < p->K;
+  S.temperature = p->temperature;
+  S.u_probe = u_probe;
+  S.sup_id = tree->sup_id;
+  S.sup_q = tree->sup_q;
+  S.sup_qT = tree->sup_qT;
+  S.sup_z = tree->sup_z;
+  S.sup_zT = tree->sup_zT;
+  S.probe_pos = tree->probe_pos;
+  S.sup_stride = tree->sup_stride;
+  S.status = status;
+  S.num_sms = num_sms_of_current_device();
+  S.ctas_per_sm = 2;
+  if (S.num_sms <= 0) return SPEC_TREE_E_CUDA;
+  if (st::launch_select_expand(dtype, S, as_stream(stream)) != cudaSuccess) return SPEC_TREE_E_CUDA;
+  st::RankLaunch L;
+  L.p = *p;
+  L.B = B;
+  L.S = support_size(p, V);
+  L.rows_avail = rows;
+  L.tree = *tree;
+  L.status = status;
+  L.layer = layer;
+  L.state = state;
+  L.frontier_token = frontier_token;
+  L.frontier_parent = frontier_parent;
+  return st::launch_layer_topr(L, as_stream(stream)) == cudaSuccess ? SPEC_TREE_OK : SPEC_TREE_E_CUDA;
+}
+
+int spec_tree_finish(const spec_tree_params* p, int B, int V, const spec_tree_t* tree, const void* state,
+                     uint32_t* status, spec_tree_stream_t stream) {
+  int rc = spec_tree_check_params(p, V);
+  if (rc) return rc;
+  if (p->builder != SPEC_TREE_BUILDER_TOPR || B < 0 || state == nullptr) return SPEC_TREE_E_PARAM;
+  if (!aligned16(state)) return SPEC_TREE_E_LAYOUT;
+  if ((rc = check_tree(p, tree, V, true, false))) return rc;
+  st::RankLaunch L;
+  L.p = *p;
+  L.B = B;
+  L.S = support_size(p, V);
+  L.rows_avail = 0;
+  L.tree = *tree;
+  L.status = status;
+  L.layer = p->depth;
+  L.state = const_cast<void*>(state);
+  L.frontier_token = nullptr;
+  L.frontier_parent = nullptr;
+  return st::launch_layer_finish(L, as_stream(stream)) == cudaSuccess ? SPEC_TREE_OK : SPEC_TREE_E_CUDA;
 }
 
 int spec_tree_verify(const spec_tree_params* p, int B, int V, int dtype, const void* target_logits,

@@ -65,7 +65,8 @@ struct RankShared {
   };
   int32_t nodes[SPEC_TREE_MAX_NODES];     // candidate of canonical node i + 1
   int32_t kept[SPEC_TREE_MAX_NODES];      // SMART: kept candidates in keep order
-  int32_t front[2][SPEC_TREE_MAX_NODES];  // SMART: kept nodes of the previous / current layer
+  int32_t front[2][SPEC_TREE_MAX_NODES];  // SMART, layer mode: frontier of the previous / current layer
+  float fscore[SPEC_TREE_MAX_NODES];      // layer mode: path scores of the previous frontier
   float cost[SPEC_TREE_MAX_NODES + 1];    // SMART: C(n)
   float dcost[SPEC_TREE_MAX_NODES + 1];   // SMART: C'(n)
   uint8_t has_kid[SPEC_TREE_MAX_CAND];    // SMART: kept node already has a kept child
@@ -116,18 +117,19 @@ struct PendingTokens {
   int32_t v[RK_PER_THREAD];
 };
 
-__device__ __forceinline__ void load_children(RankShared& s, const RankLaunch& L, int b, int rows,
+__device__ __forceinline__ void load_children(RankShared& s, const RankLaunch& L, int b, int row0, int rows,
                                               PendingTokens& tok) {
   const int K = L.p.K, m = L.p.m;
   const spec_tree_t& t = L.tree;
   const int n = rows * K;
+  const int e0 = row0 * K;  // child-table entry of the range's first child
   int pp[RK_PER_THREAD];
   float qa[RK_PER_THREAD], qb[RK_PER_THREAD], z[RK_PER_THREAD];
 #pragma unroll
   for (int u = 0; u < RK_PER_THREAD; ++u) {
     const int idx = threadIdx.x + u * RANK_THREADS;
     if (idx < n) {
-      const int r = idx / K, slot = idx - r * K;
+      const int r = row0 + idx / K, slot = idx % K;
       const int64_t row = static_cast<int64_t>(b) * t.n_rows + r;
       const float* q = t.sup_q + row * t.sup_stride;
       pp[u] = t.probe_pos[row];
@@ -140,7 +142,7 @@ __device__ __forceinline__ void load_children(RankShared& s, const RankLaunch& L
   for (int u = 0; u < RK_PER_THREAD; ++u) {
     const int idx = threadIdx.x + u * RANK_THREADS;
     if (idx < n) {
-      const int r = idx / K, slot = idx - r * K;
+      const int r = row0 + idx / K, slot = idx % K;
       int kind, rank;
       float lp;
       if (slot < m) {
@@ -157,19 +159,19 @@ __device__ __forceinline__ void load_children(RankShared& s, const RankLaunch& L
         rank = (pp[u] >= 0 && slot - 1 < pp[u]) ? slot - 1 : slot;
         lp = rank == slot ? qa[u] : qb[u];
       }
-      s.ch_lp[idx] = lp;
-      s.ch_rk[idx] = rank | (kind << 16);
+      s.ch_lp[e0 + idx] = lp;
+      s.ch_rk[e0 + idx] = rank | (kind << 16);
       const int64_t row = static_cast<int64_t>(b) * t.n_rows + r;
       tok.v[u] = t.sup_id[row * t.sup_stride + rank];
     }
   }
 }
 
-__device__ __forceinline__ void store_tokens(RankShared& s, int n, const PendingTokens& tok) {
+__device__ __forceinline__ void store_tokens(RankShared& s, int row0, int rows, int K, const PendingTokens& tok) {
 #pragma unroll
   for (int u = 0; u < RK_PER_THREAD; ++u) {
     const int idx = threadIdx.x + u * RANK_THREADS;
-    if (idx < n) s.ch_tok[idx] = tok.v[u];
+    if (idx < rows * K) s.ch_tok[row0 * K + idx] = tok.v[u];
   }
 }
 
@@ -300,6 +302,62 @@ __device__ void write_nodes(RankShared& s, const RankLaunch& L, int b, int nsel)
   if (threadIdx.x == 0) t.n_nodes[b] = 1 + nsel;
 }
 
+// Global top-R of a tree whose D layers are ranked: s.mkey[0] / s.mcand[0]
+// hold each layer's sorted list at the layer's base (s.layer_base), s.lrank
+// each candidate's rank in its layer, s.lst_start[0] / s.lst_len[0] the
+// lists cut to R, s.layer_sel zero.  Sets s.pos and s.nodes of the min(R, nc)
+// survivors in canonical order.  Rounds of pairwise merges of the sorted
+// layer lists, each cut to R: list i keeps the start of the block of layers
+// it covers, and a merge of two neighbours fits in their joint block.  Each
+// output entry is one thread's merge-path search.
+__device__ void topr_cut(RankShared& s, int D, int R) {
+  const int tid = threadIdx.x;
+  int nl = D, cur = 0;
+  while (nl > 1) {
+    const int nl2 = (nl + 1) >> 1;
+    const int32_t* st = s.lst_start[cur];
+    const int32_t* len = s.lst_len[cur];
+    for (int e = tid; e < nl2 * R; e += RANK_THREADS) {
+      const int i = e / R, p = e - i * R;
+      const int a0 = st[2 * i], la = len[2 * i];
+      const bool pair = 2 * i + 1 < nl;
+      const int b0 = pair ? st[2 * i + 1] : a0, lb = pair ? len[2 * i + 1] : 0;
+      if (p == 0) {
+        s.lst_start[cur ^ 1][i] = a0;
+        s.lst_len[cur ^ 1][i] = min(R, la + lb);
+      }
+      if (p < la + lb) {
+        uint64_t k;
+        int32_t c;
+        merge_entry(s.mkey[cur] + a0, s.mcand[cur] + a0, la, s.mkey[cur] + b0, s.mcand[cur] + b0, lb, p, k, c);
+        s.mkey[cur ^ 1][a0 + p] = k;
+        s.mcand[cur ^ 1][a0 + p] = c;
+      }
+    }
+    __syncthreads();
+    nl = nl2;
+    cur ^= 1;
+  }
+  // s.mkey[cur][0..nsel): the top-R by key; survivors per layer
+  const int nsel = min(R, s.layer_base[D + 1]);
+  for (int p = tid; p < nsel; p += RANK_THREADS) {
+    const int c = s.mcand[cur][p];
+    s.pos[c] = 0;  // survivor; canonical index set below
+    atomicAdd(&s.layer_sel[key_depth(s.key[c])], 1);
+  }
+  __syncthreads();
+  // canonical index: survivors of shallower layers, then rank in the layer
+  for (int p = tid; p < nsel; p += RANK_THREADS) {
+    const int c = s.mcand[cur][p];
+    const int d = key_depth(s.key[c]);
+    int q = 1 + s.lrank[c];
+    for (int e = 1; e < d; ++e) q += s.layer_sel[e];
+    s.pos[c] = static_cast<int16_t>(q);
+    if (q - 1 < SPEC_TREE_MAX_NODES) s.nodes[q - 1] = c;
+  }
+}
+
+
 // Expand-then-rerank with a frontier of width W per layer, then global top-R.
 __global__ void __launch_bounds__(RANK_THREADS) rank_topr_kernel(RankLaunch L) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -309,7 +367,7 @@ __global__ void __launch_bounds__(RANK_THREADS) rank_topr_kernel(RankLaunch L) {
   const int rows = static_cast<int>(L.rows_avail);
   grid_dependency_wait();  // the support arrays come from the previous kernel
   PendingTokens tok;
-  load_children(s, L, b, rows, tok);
+  load_children(s, L, b, 0, rows, tok);
   // layer sizes: K, then min(previous, W) * K; each sorted layer list is
   // list d - 1 of the merge tree
   if (tid == 0) {
@@ -353,56 +411,10 @@ __global__ void __launch_bounds__(RANK_THREADS) rank_topr_kernel(RankLaunch L) {
     __syncthreads();
   }
   grid_dependents_launch();
-  // global top-R: rounds of pairwise merges of the sorted layer lists, each
-  // cut to R.  List i keeps the start of the block of layers it covers; a
-  // merge of two neighbours fits in their joint block.  Each output entry is
-  // one thread's merge-path search.
-  int nl = D, cur = 0;
-  while (nl > 1) {
-    const int nl2 = (nl + 1) >> 1;
-    const int32_t* st = s.lst_start[cur];
-    const int32_t* len = s.lst_len[cur];
-    for (int e = tid; e < nl2 * R; e += RANK_THREADS) {
-      const int i = e / R, p = e - i * R;
-      const int a0 = st[2 * i], la = len[2 * i];
-      const bool pair = 2 * i + 1 < nl;
-      const int b0 = pair ? st[2 * i + 1] : a0, lb = pair ? len[2 * i + 1] : 0;
-      if (p == 0) {
-        s.lst_start[cur ^ 1][i] = a0;
-        s.lst_len[cur ^ 1][i] = min(R, la + lb);
-      }
-      if (p < la + lb) {
-        uint64_t k;
-        int32_t c;
-        merge_entry(s.mkey[cur] + a0, s.mcand[cur] + a0, la, s.mkey[cur] + b0, s.mcand[cur] + b0, lb, p, k, c);
-        s.mkey[cur ^ 1][a0 + p] = k;
-        s.mcand[cur ^ 1][a0 + p] = c;
-      }
-    }
-    __syncthreads();
-    nl = nl2;
-    cur ^= 1;
-  }
-  // s.mkey[cur][0..nsel): the top-R by key; survivors per layer
-  const int nsel = min(R, s.layer_base[D + 1]);
-  for (int p = tid; p < nsel; p += RANK_THREADS) {
-    const int c = s.mcand[cur][p];
-    s.pos[c] = 0;  // survivor; canonical index set below
-    atomicAdd(&s.layer_sel[key_depth(s.key[c])], 1);
-  }
+  topr_cut(s, D, R);
+  store_tokens(s, 0, rows, K, tok);
   __syncthreads();
-  // canonical index: survivors of shallower layers, then rank in the layer
-  for (int p = tid; p < nsel; p += RANK_THREADS) {
-    const int c = s.mcand[cur][p];
-    const int d = key_depth(s.key[c]);
-    int q = 1 + s.lrank[c];
-    for (int e = 1; e < d; ++e) q += s.layer_sel[e];
-    s.pos[c] = static_cast<int16_t>(q);
-    s.nodes[q - 1] = c;
-  }
-  store_tokens(s, rows * K, tok);
-  __syncthreads();
-  write_nodes(s, L, b, nsel);
+  write_nodes(s, L, b, min(R, s.layer_base[D + 1]));
 }
 
 // SMART: layer-wise greedy keep rule over dual-identity children.
@@ -439,7 +451,7 @@ __global__ void __launch_bounds__(RANK_THREADS) rank_smart_kernel(RankLaunch L) 
   grid_dependency_wait();
   const int rows = static_cast<int>(L.rows_avail);
   PendingTokens tok;
-  load_children(s, L, b, rows, tok);
+  load_children(s, L, b, 0, rows, tok);
   if (tid == 0) {
     s.front[0][0] = -1;
     s.nf = 1;
@@ -519,9 +531,196 @@ __global__ void __launch_bounds__(RANK_THREADS) rank_smart_kernel(RankLaunch L) 
   grid_dependents_launch();
   const int nsel = s.n_kept;
   for (int i = tid; i < nsel; i += RANK_THREADS) s.nodes[i] = s.kept[i];
-  store_tokens(s, rows * K, tok);
+  store_tokens(s, 0, rows, K, tok);
   __syncthreads();
   write_nodes(s, L, b, nsel);
+}
+
+// ------------------------------------------------- layer-by-layer builder ---
+// The same tree as rank_topr_kernel, built one layer per call so that a draft
+// model can produce each frontier's logits in between (RheoSampling notes,
+// overall framework: the frontier is expanded layer by layer).  Call `layer`
+// (0 .. depth-1) finds the draft rows of the current frontier (layer 0: the
+// root) expanded into the tree's support rows; it scores their children, the
+// candidates of depth layer + 1, ranks them inside their layer, names the
+// next frontier and keeps all of it in a per-tree state in global memory.
+// The finish call cuts the global top-R from the state exactly as the
+// one-shot build does, so both give the same tree bit for bit.  The state
+// holds every candidate's token and kind, so the finish call never reads a
+// support row (rows of frontier ranks that did not exist are never written).
+struct alignas(16) LayerState {
+  int32_t nc;      // candidates so far
+  int32_t nf;      // size of the frontier to expand next
+  int32_t layers;  // layers ranked so far; -1 after a call out of order
+  int32_t pad;
+  int32_t front[SPEC_TREE_MAX_NODES];     // candidate of frontier rank r
+  int32_t layer_base[RK_MAX_LAYERS + 4];  // first candidate of layer d, then the end
+  uint64_t key[SPEC_TREE_MAX_CAND];
+  int32_t link[SPEC_TREE_MAX_CAND];
+  int32_t ch_rk[SPEC_TREE_MAX_CAND];   // child-table entry: support rank | kind << 16
+  int32_t ch_tok[SPEC_TREE_MAX_CAND];  // child-table entry: token id
+  int16_t exp_row[SPEC_TREE_MAX_CAND];
+  int16_t lrank[SPEC_TREE_MAX_CAND];
+};
+
+size_t layer_state_bytes() { return sizeof(LayerState); }
+
+// Frontier outputs of tree b from rank r0 on: none.
+__device__ __forceinline__ void clear_frontier(const RankLaunch& L, int b, int r0) {
+  const int W = L.p.W;
+  for (int r = r0 + static_cast<int>(threadIdx.x); r < W; r += RANK_THREADS) {
+    if (L.frontier_token) L.frontier_token[static_cast<int64_t>(b) * W + r] = -1;
+    if (L.frontier_parent) L.frontier_parent[static_cast<int64_t>(b) * W + r] = -1;
+  }
+}
+
+__global__ void __launch_bounds__(RANK_THREADS) layer_topr_kernel(RankLaunch L) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  RankShared& s = *reinterpret_cast<RankShared*>(smem_raw);
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int K = L.p.K, W = L.p.W, D = L.p.depth;
+  const int layer = L.layer, depth = layer + 1;
+  const int nf = static_cast<int>(L.rows_avail);  // frontier rows expanded for this call
+  LayerState* g = reinterpret_cast<LayerState*>(L.state) + b;
+  grid_dependency_wait();  // the support rows (and the state) come from earlier kernels
+  const int ln = nf * K;
+  const int nc = layer == 0 ? 0 : g->nc;
+  // the state must come from the previous layer's call; every index read
+  // from it is range-checked, so a spoiled state is never followed
+  bool bad = layer > 0 && (g->layers != layer || g->nf != nf || nc < 0 || nc > SPEC_TREE_MAX_CAND - ln);
+  const int row0 = layer == 0 ? 0 : 1 + (layer - 1) * W;
+  PendingTokens tok;
+  load_children(s, L, b, row0, nf, tok);
+  if (!bad) {
+    for (int f = tid; f < nf; f += RANK_THREADS) {
+      const int pc = layer == 0 ? -1 : g->front[f];
+      if (layer > 0 && (pc < 0 || pc >= nc)) {
+        bad = true;
+        break;
+      }
+      s.front[0][f] = pc;
+      s.fscore[f] = pc < 0 ? 1.0f : key_score(g->key[pc]);
+    }
+  }
+  store_tokens(s, row0, nf, K, tok);
+  if (__syncthreads_or(bad)) {  // every thread has read the header
+    if (tid == 0) {
+      g->layers = -1;
+      set_status(L.status, SPEC_TREE_S_LAYERS);
+    }
+    clear_frontier(L, b, 0);
+    return;
+  }
+  for (int idx = tid; idx < ln; idx += RANK_THREADS) {
+    const int f = idx / K, slot = idx - f * K;
+    make_candidate(s, nc + idx, s.front[0][f], s.fscore[f], row0 + f, depth, f, slot, K);
+  }
+  __syncthreads();
+  const bool more = depth < D;
+  const int nf2 = ln < W ? ln : W;
+  // rank the layer; its first W are the next frontier, expanded from the
+  // draft rows 1 + layer * W + r
+  rank_layer(s, nc, ln, [&](int i, int r, int, int part) {
+    if (part != 0) return;
+    const int c = nc + i;
+    s.lrank[c] = static_cast<int16_t>(r);
+    if (more && r < W) {
+      s.exp_row[c] = static_cast<int16_t>(1 + layer * W + r);
+      s.front[1][r] = c;
+      const int64_t o = static_cast<int64_t>(b) * W + r;
+      if (L.frontier_token) L.frontier_token[o] = s.ch_tok[s.link[c] >> 12];
+      if (L.frontier_parent)
+        L.frontier_parent[o] = layer == 0 ? -1 : static_cast<int>((key_creation(s.key[c]) >> 12) & 0xfffu);
+    }
+  });
+  __syncthreads();
+  grid_dependents_launch();
+  for (int idx = tid; idx < ln; idx += RANK_THREADS) {
+    const int c = nc + idx, e = row0 * K + idx;
+    g->key[c] = s.key[c];
+    g->link[c] = s.link[c];
+    g->exp_row[c] = s.exp_row[c];
+    g->lrank[c] = s.lrank[c];
+    g->ch_rk[e] = s.ch_rk[e];
+    g->ch_tok[e] = s.ch_tok[e];
+  }
+  if (more)
+    for (int r = tid; r < nf2; r += RANK_THREADS) g->front[r] = s.front[1][r];
+  clear_frontier(L, b, more ? nf2 : 0);
+  if (tid == 0) {
+    g->nc = nc + ln;
+    g->nf = more ? nf2 : 0;
+    g->layers = depth;
+    if (layer == 0) g->layer_base[1] = 0;
+    g->layer_base[depth + 1] = nc + ln;
+  }
+}
+
+__global__ void __launch_bounds__(RANK_THREADS) layer_finish_kernel(RankLaunch L) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  RankShared& s = *reinterpret_cast<RankShared*>(smem_raw);
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int D = L.p.depth, R = L.p.R;
+  const LayerState* g = reinterpret_cast<const LayerState*>(L.state) + b;
+  grid_dependency_wait();
+  const int nc = g->nc;
+  // the state must hold all D layers; every index read from it is
+  // range-checked, so a spoiled state is never followed
+  bool bad = g->layers != D || nc < 0 || nc > SPEC_TREE_MAX_CAND;
+  if (!bad) {
+    for (int d = 1 + tid; d <= D + 1; d += RANK_THREADS) s.layer_base[d] = g->layer_base[d];
+    for (int c = tid; c < nc; c += RANK_THREADS) {
+      s.key[c] = g->key[c];
+      s.link[c] = g->link[c];
+      s.lrank[c] = g->lrank[c];
+      s.exp_row[c] = g->exp_row[c];
+      s.pos[c] = -1;
+      s.mkey[0][c] = 0;
+      s.mcand[0][c] = 0;
+    }
+    for (int i = tid; i < R; i += RANK_THREADS) s.nodes[i] = 0;
+  }
+  if (tid <= D) s.layer_sel[tid] = 0;
+  if (__syncthreads_or(bad)) {
+    // not every layer was ranked, in order: the root alone and a status bit
+    if (tid == 0) set_status(L.status, SPEC_TREE_S_LAYERS);
+    write_nodes(s, L, b, 0);
+    return;
+  }
+  for (int d = 1 + tid; d <= D; d += RANK_THREADS) {
+    const int lo = s.layer_base[d], hi = s.layer_base[d + 1];
+    if ((d == 1 && lo != 0) || hi < lo || hi > nc || (d == D && hi != nc)) bad = true;
+  }
+  for (int c = tid; c < nc; c += RANK_THREADS) {
+    const int link = s.link[c], e = link >> 12, pc = (link & 0xfff) - 1, d = key_depth(s.key[c]);
+    if (e < 0 || e >= SPEC_TREE_MAX_CAND || pc >= c || d < 1 || d > D || s.lrank[c] < 0 ||
+        s.lrank[c] >= s.layer_base[d + 1] - s.layer_base[d]) {
+      bad = true;
+      continue;
+    }
+    s.ch_rk[e] = g->ch_rk[e];
+    s.ch_tok[e] = g->ch_tok[e];
+  }
+  if (__syncthreads_or(bad)) {
+    if (tid == 0) set_status(L.status, SPEC_TREE_S_LAYERS);
+    write_nodes(s, L, b, 0);
+    return;
+  }
+  grid_dependents_launch();
+  // each layer's sorted list, cut to R, from the ranks kept in the state
+  for (int d = 1 + tid; d <= D; d += RANK_THREADS) {
+    s.lst_start[0][d - 1] = s.layer_base[d];
+    s.lst_len[0][d - 1] = min(R, s.layer_base[d + 1] - s.layer_base[d]);
+  }
+  for (int c = tid; c < nc; c += RANK_THREADS) {
+    const int p = s.layer_base[key_depth(s.key[c])] + s.lrank[c];
+    s.mkey[0][p] = s.key[c];
+    s.mcand[0][p] = c;
+  }
+  __syncthreads();
+  topr_cut(s, D, R);
+  __syncthreads();
+  write_nodes(s, L, b, min(R, nc));
 }
 
 template <typename Kern>
@@ -539,6 +738,14 @@ cudaError_t launch_rank_topr(const RankLaunch& L, cudaStream_t stream) {
 
 cudaError_t launch_rank_smart(const RankLaunch& L, cudaStream_t stream) {
   return launch_rank(rank_smart_kernel, L, stream);
+}
+
+cudaError_t launch_layer_topr(const RankLaunch& L, cudaStream_t stream) {
+  return launch_rank(layer_topr_kernel, L, stream);
+}
+
+cudaError_t launch_layer_finish(const RankLaunch& L, cudaStream_t stream) {
+  return launch_rank(layer_finish_kernel, L, stream);
 }
 
 }  // namespace st

@@ -65,7 +65,8 @@ struct SelShared {
   uint64_t empty[SX_STAGES];
   uint64_t cfull[2];   // candidates of a row ready for the selector
   uint64_t cempty[2];  // selector done with a candidate buffer
-  int64_t cand_row[2];
+  int64_t cand_row[2];  // output row (support arrays) of the candidates
+  int64_t cand_in[2];   // input row (logits, u_probe) of the candidates
   uint32_t hist[256];
   uint32_t shist[256];
   uint32_t warp_bound[SX_CWARPS];
@@ -497,7 +498,9 @@ __device__ void select_topk(SelShared& s, CandBuf cb, int n, int k) {
 struct SelArgs {
   const uint8_t* logits;
   int64_t row_bytes_stride;  // bytes between consecutive rows
-  int64_t n_rows;            // rows per tree in the logits / support arrays
+  int64_t in_rows;           // rows per tree in the logits / u_probe
+  int64_t n_rows;            // rows per tree in the support arrays
+  int64_t sup_row0;          // support row of a tree's first processed row
   int64_t rows_used;         // rows per tree to process
   int64_t total_rows;        // B * rows_used
   int V;
@@ -694,7 +697,8 @@ __device__ int warp_select_sort(SelShared& s, const uint64_t* c, int n, int k, u
 // 2; the probe is the first tail rank k with u * z_T < sum_{j=m..k} q_T(j),
 // computed on unnormalised weights.
 template <typename T>
-__device__ void expand_epilogue(const uint64_t (&val)[4], const SelArgs& a, int64_t out_row, int n_sup) {
+__device__ void expand_epilogue(const uint64_t (&val)[4], const SelArgs& a, int64_t out_row, int64_t in_row,
+                                int n_sup) {
   const int lane = threadIdx.x & 31;
   float l[4], e[4], eT[4];
   const float lmax = key_value<T>(static_cast<uint32_t>(__shfl_sync(FULL, val[0], 0) >> 32));
@@ -733,7 +737,7 @@ __device__ void expand_epilogue(const uint64_t (&val)[4], const SelArgs& a, int6
   }
   int probe = -1;
   if (a.draw_probe && a.m < n_sup && teT > 0.0f) {
-    const float target = a.u_probe[out_row] * teT;
+    const float target = a.u_probe[in_row] * teT;
     float carry = 0.0f;
     int last = -1;
 #pragma unroll
@@ -803,10 +807,10 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
       const int q = static_cast<int>(lr & 1);
       if (!mbar_wait(&s.cfull[q], static_cast<uint32_t>((lr >> 1) & 1))) timed_out = true;
       const int n = s.count[q];
-      const int64_t out_row = s.cand_row[q];
+      const int64_t out_row = s.cand_row[q], in_row = s.cand_in[q];
       uint64_t val[4];
       const int n_sup = warp_select_sort<E::KEY_BITS>(s, s.cand[q], min(n, SX_CAP), a.S, val);
-      expand_epilogue<T>(val, a, out_row, n_sup);
+      expand_epilogue<T>(val, a, out_row, in_row, n_sup);
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.cempty[q]);
     }
@@ -825,7 +829,7 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
       bool timed_out = false;
       int64_t b = blockIdx.x / a.rows_used, e = blockIdx.x % a.rows_used;
       for (int64_t lr = 0; lr < my_rows; ++lr) {
-        const uint8_t* row = a.logits + (b * a.n_rows + e) * a.row_bytes_stride;
+        const uint8_t* row = a.logits + (b * a.in_rows + e) * a.row_bytes_stride;
         for (int pass = 0; pass < 2; ++pass) {
           for (int c = 0; c < nch; ++c, ++g) {
             // stage reuse: wait until every consumer warp released its last use
@@ -858,8 +862,9 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
   int64_t b = blockIdx.x / a.rows_used, e = blockIdx.x % a.rows_used;
   const int jth = (a.S + SX_CWARPS - 1) / SX_CWARPS;
   for (int64_t lr = 0; lr < my_rows; ++lr) {
-    const int64_t out_row = b * a.n_rows + e;
-    const uint8_t* row = a.logits + out_row * a.row_bytes_stride;
+    const int64_t out_row = b * a.n_rows + a.sup_row0 + e;
+    const int64_t in_row = b * a.in_rows + e;
+    const uint8_t* row = a.logits + in_row * a.row_bytes_stride;
 
     // pass 1: running maximum of this thread's elements
     RunMax<T> rm;
@@ -1000,6 +1005,7 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
     // hand the candidates to the selector warp and move on to the next row
     if (tid == 0) {
       s.cand_row[q] = out_row;
+      s.cand_in[q] = in_row;
       mbar_arrive(&s.cfull[q]);
     }
     e += gridDim.x;
@@ -1017,7 +1023,9 @@ cudaError_t launch_select_expand(int dtype, const SelLaunch& L, cudaStream_t str
   SelArgs a;
   a.logits = static_cast<const uint8_t*>(L.logits);
   a.row_bytes_stride = L.row_stride * (dtype == SPEC_TREE_BF16 ? 2 : 4);
+  a.in_rows = L.in_rows;
   a.n_rows = L.n_rows;
+  a.sup_row0 = L.sup_row0;
   a.rows_used = L.rows_used;
   a.total_rows = static_cast<int64_t>(L.B) * L.rows_used;
   a.V = L.V;

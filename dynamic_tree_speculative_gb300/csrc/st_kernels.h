@@ -12,7 +12,9 @@ namespace st {
 struct SelLaunch {
   const void* logits;
   int64_t row_stride;  // elements
-  int64_t n_rows;      // rows per tree in memory
+  int64_t in_rows;     // rows per tree in the logits and u_probe
+  int64_t n_rows;      // rows per tree in the support arrays
+  int64_t sup_row0;    // support row of a tree's first processed row
   int64_t rows_used;   // rows per tree to process
   int B, V, S, m;
   bool draw_probe;  // m < K: a probe child exists
@@ -36,6 +38,11 @@ struct RankLaunch {
   int64_t rows_avail;  // rows per tree that were expanded
   spec_tree_t tree;
   uint32_t* status;
+  // layer mode only
+  int layer;
+  void* state;
+  int32_t* frontier_token;
+  int32_t* frontier_parent;
 };
 
 struct VerifyLaunch {
@@ -58,6 +65,9 @@ size_t select_expand_smem_bytes();
 cudaError_t launch_select_expand(int dtype, const SelLaunch& L, cudaStream_t stream);
 cudaError_t launch_rank_topr(const RankLaunch& L, cudaStream_t stream);
 cudaError_t launch_rank_smart(const RankLaunch& L, cudaStream_t stream);
+size_t layer_state_bytes();
+cudaError_t launch_layer_topr(const RankLaunch& L, cudaStream_t stream);
+cudaError_t launch_layer_finish(const RankLaunch& L, cudaStream_t stream);
 cudaError_t launch_verify(const VerifyLaunch& L, cudaStream_t stream);
 
 }  // namespace st

@@ -81,6 +81,7 @@ typedef struct CUstream_st* spec_tree_stream_t;
 #define SPEC_TREE_S_OVERFLOW 8u          /* internal candidate buffer overflow (not expected) */
 #define SPEC_TREE_S_TIMEOUT 16u          /* a bounded wait on a bulk copy gave up */
 #define SPEC_TREE_S_ROWS 32u             /* a tree wanted more draft rows than n_rows */
+#define SPEC_TREE_S_LAYERS 64u           /* layer mode: a call out of order, or finish before the last layer */
 
 /* Limits of this build. */
 #define SPEC_TREE_MAX_SUPPORT 128
@@ -230,6 +231,52 @@ int spec_tree_verify(const spec_tree_params* p, int B, int V, int dtype,
                      const spec_tree_t* tree, const float* u_verify, const float* u_bonus,
                      int32_t* accept_len, int32_t* out_tok, int32_t* out_node,
                      uint32_t* margins, uint32_t* status, spec_tree_stream_t stream);
+
+/*
+ * Layer mode: the top-R tree of spec_tree_build, built one layer per call so
+ * that the draft model can run on each frontier in between (RheoSampling
+ * overall framework: the frontier is expanded layer by layer).  Top-R builder
+ * only (SPEC_TREE_BUILDER_SMART returns SPEC_TREE_E_PARAM).
+ *
+ * For layer = 0, 1, ..., depth - 1 in order, per batch of trees:
+ *   spec_tree_layer(layer): expands the rows_l = spec_tree_layer_rows(p, layer)
+ *     draft rows of the current frontier (layer 0: the root) exactly as
+ *     spec_tree_select_expand does, into support rows r0 .. r0 + rows_l - 1 of
+ *     `tree` (r0 = 0 for layer 0, else 1 + (layer - 1) * W), scores their
+ *     children (the candidates of depth layer + 1), ranks them in their
+ *     layer and, unless layer = depth - 1, names the next frontier: its first
+ *     W candidates by key.
+ *       layer_logits: device [B][rows_l][row_stride] of dtype; row f holds the
+ *         draft logits after frontier rank f of the previous call's frontier
+ *         (layer 0: after the root).
+ *       u_probe: device [B][rows_l] float, U[0,1): row f's probe draw.
+ *       state: device, B * spec_tree_layer_state_bytes() bytes, 16-byte
+ *         aligned, owned by the caller; written by layer 0, read and updated
+ *         by every later call, read by spec_tree_finish.  No initialisation
+ *         is needed.
+ *       frontier_token, frontier_parent: device [B][W] int32, or NULL: the
+ *         token of frontier rank f (the draft's next input for row f of the
+ *         next call) and the previous frontier's rank of its parent (-1 for
+ *         the root's children); -1 past the frontier and after the last layer.
+ *   spec_tree_finish: the global top-R cut; writes the node arrays and
+ *     n_nodes of `tree`, equal to what spec_tree_build writes for the same
+ *     draft rows and draws.
+ * A call out of order sets SPEC_TREE_S_LAYERS and spoils the tree's state
+ * until the next layer 0; spec_tree_finish then writes the root alone.
+ */
+size_t spec_tree_layer_state_bytes(void);
+
+/* Frontier rows expanded by call `layer` (host only): 1 for layer 0, else
+ * min(W, size of layer `layer`); 0 if layer is out of range or p invalid. */
+int spec_tree_layer_rows(const spec_tree_params* p, int layer);
+
+int spec_tree_layer(const spec_tree_params* p, int B, int V, int layer, int dtype,
+                    const void* layer_logits, int64_t row_stride, const float* u_probe,
+                    const spec_tree_t* tree, void* state, int32_t* frontier_token,
+                    int32_t* frontier_parent, uint32_t* status, spec_tree_stream_t stream);
+
+int spec_tree_finish(const spec_tree_params* p, int B, int V, const spec_tree_t* tree,
+                     const void* state, uint32_t* status, spec_tree_stream_t stream);
 
 /* Message for a return code (static string). */
 const char* spec_tree_strerror(int code);

@@ -223,6 +223,9 @@ class Tree:
     expansions: dict        # draft row -> Expansion
     margins: Margins
     n_candidates: int
+    # top-R builder: for each layer d < D, its frontier in rank order as
+    # (token, rank of the parent in the previous frontier, -1 for the root)
+    frontiers: list = dataclasses.field(default_factory=list)
 
     @property
     def n_nodes(self) -> int:
@@ -321,6 +324,7 @@ def build_topr(rows, u_probe, p: Params) -> Tree:
     cache = {}
     root = _new_root()
     frontier = [root]
+    frontiers = []
     allc: List[_Cand] = []
     for d in range(1, p.depth + 1):
         layer = []
@@ -334,9 +338,12 @@ def build_topr(rows, u_probe, p: Params) -> Tree:
             frontier = ordered[:p.W]
             for r, c in enumerate(frontier):
                 c.exp_row = 1 + (d - 1) * p.W + r
+            frontiers.append([(c.token, -1 if d == 1 else c.prank) for c in frontier])
     ordered = sorted(allc, key=_Cand.key)
     _record_order_margins(ordered, p.R, mg)
-    return _emit(ordered[:p.R], root, cache, mg, len(allc))
+    tree = _emit(ordered[:p.R], root, cache, mg, len(allc))
+    tree.frontiers = frontiers
+    return tree
 
 
 def smart_cost(n: float, p: Params) -> float:

@@ -87,3 +87,45 @@ def test_bad_arguments_fail_before_any_launch(binding):
                                 ctypes.byref(t), ctypes.c_void_p(256), ctypes.c_void_p(256), None, None, None,
                                 None, None, None) == binding.E_PARAM
     assert binding._lib.spec_tree_strerror(binding.E_LAYOUT).startswith(b"unsupported")
+
+
+def test_layer_rows_and_state(binding):
+    P = binding.Params
+    p = P(K=2, m=1, W=8, depth=5, R=24)
+    assert [binding.spec_tree_layer_rows(p, layer) for layer in range(-1, 6)] == [0, 1, 2, 4, 8, 8, 0]
+    assert [binding.spec_tree_layer_rows(P(K=8, m=1, W=8, depth=8, R=60), layer) for layer in range(8)] == \
+        [1] + [8] * 7
+    # the rows of all calls are the one-shot build's rows
+    for kw in (dict(K=2, m=1, W=8, depth=5, R=24), dict(K=6, m=1, W=6, depth=6, R=32)):
+        q = P(**kw)
+        assert sum(binding.spec_tree_layer_rows(q, layer) for layer in range(q.depth)) <= binding.rows_needed(q)
+    assert binding.spec_tree_layer_rows(P(K=8, m=1, W=8, depth=8, R=60, builder=binding.BUILDER_SMART), 0) == 0
+    n = binding.spec_tree_layer_state_bytes()
+    assert n > 0 and n % 16 == 0
+
+
+def test_layer_mode_bad_arguments(binding):
+    lib = binding._lib
+    t = binding.c_tree()
+    for name, _ in binding.c_tree._fields_[:14]:
+        setattr(t, name, 256)
+    t.n_rows, t.max_nodes, t.sup_stride = 57, 61, 128
+    vp = ctypes.c_void_p
+
+    def layer(p, layer_idx, state):
+        return lib.spec_tree_layer(ctypes.byref(p.c()), 1, 1000, layer_idx, binding.BF16, vp(256), 1008, vp(256),
+                                   ctypes.byref(t), state, None, None, None, None)
+
+    p = binding.Params(K=8, m=1, W=8, depth=8, R=60)
+    assert layer(p, 8, vp(256)) == binding.E_PARAM                       # past the last layer
+    assert layer(p, -1, vp(256)) == binding.E_PARAM
+    assert layer(p, 0, None) == binding.E_PARAM                          # no state
+    assert layer(p, 0, vp(264)) == binding.E_LAYOUT                      # state not 16-byte aligned
+    smart = binding.Params(K=8, m=1, W=8, depth=8, R=60, builder=binding.BUILDER_SMART)
+    t.n_rows = 61
+    assert layer(smart, 0, vp(256)) == binding.E_PARAM                   # top-R builder only
+    t.n_rows = 57
+    assert lib.spec_tree_finish(ctypes.byref(p.c()), 1, 1000, ctypes.byref(t), None, None, None) == \
+        binding.E_PARAM
+    assert lib.spec_tree_finish(ctypes.byref(p.c()), 1, 1000, ctypes.byref(t), vp(264), None, None) == \
+        binding.E_LAYOUT

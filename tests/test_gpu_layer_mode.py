@@ -1,0 +1,174 @@
+"""Layer-by-layer builder (spec_tree_layer / spec_tree_finish) on the GPU.
+
+The layer-mode tree must equal the one-shot spec_tree_build bit for bit (same
+draft rows, same draws), the support rows each call expands must equal the
+one-shot expansion, and the frontier each call names must equal the oracle's
+frontier of that layer (trees with a near-tie in the ranking exempt).
+"""
+import numpy as np
+import pytest
+import torch
+
+from dynamic_tree_speculative_gb300 import binding as B
+from dynamic_tree_speculative_gb300 import workloads as WL
+
+pytestmark = pytest.mark.gpu
+
+import parity  # noqa: E402  (loads the native library; fails loudly if absent)
+
+NODE_FIELDS = ("node_token", "node_parent", "node_depth", "node_kind", "node_slot", "node_exp_row")
+SUP_FIELDS = ("sup_id", "sup_q", "sup_qT", "sup_z", "sup_zT", "probe_pos")
+
+
+def _row0(wl, layer):
+    return 0 if layer == 0 else 1 + (layer - 1) * wl.W
+
+
+def _fresh_tree(params, wl):
+    tree = B.TreeBuffers(params, wl.B)
+    # rows that no call expands keep these values; none of them may reach a node
+    tree.sup_id.fill_(-5)
+    tree.probe_pos.fill_(-2)
+    for t in (tree.sup_q, tree.sup_qT, tree.sup_z, tree.sup_zT):
+        t.fill_(float("nan"))
+    return tree
+
+
+def run_layers(case, layers=None, state=None, tree=None, status=None):
+    wl = case.wl
+    params = B.Params.from_workload(wl)
+    tree = tree if tree is not None else _fresh_tree(params, wl)
+    state = state if state is not None else B.LayerState(params, wl.B)
+    status = status if status is not None else torch.zeros(1, dtype=torch.int32, device="cuda")
+    draft, u = case.draft.cuda(), case.u_probe.cuda()
+    fronts = []
+    for layer in (range(wl.depth) if layers is None else layers):
+        rows, r0 = B.spec_tree_layer_rows(params, layer), _row0(wl, layer)
+        B.spec_tree_layer(params, wl.V, layer, draft[:, r0:r0 + rows].contiguous(),
+                          u[:, r0:r0 + rows].contiguous(), tree, state, status)
+        fronts.append((state.frontier_token.cpu().numpy().copy(), state.frontier_parent.cpu().numpy().copy()))
+    return params, tree, state, status, fronts
+
+
+def _host(tree):
+    return {k: getattr(tree, k).cpu().numpy() for k in NODE_FIELDS + SUP_FIELDS + ("node_score", "n_nodes")}
+
+
+def _written_rows(params, wl):
+    out = []
+    for layer in range(wl.depth):
+        r0 = _row0(wl, layer)
+        out.extend(range(r0, r0 + B.spec_tree_layer_rows(params, layer)))
+    return out
+
+
+def check_layer_mode(wl, seed, sample=None, row_stride=None):
+    case = parity.make_case(wl, seed, row_stride)
+    one = parity.run_gpu(case)
+    params, tree, _, status, fronts = run_layers(case)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, status
+    lay = _host(tree)
+    # the tree: bit-exact against the one-shot build
+    assert np.array_equal(lay["n_nodes"], one["n_nodes"])
+    for b in range(wl.B):
+        n = int(one["n_nodes"][b])
+        for f in NODE_FIELDS:
+            assert np.array_equal(lay[f][b, :n], one[f][b, :n]), (b, f)
+        assert np.array_equal(lay["node_score"][b, :n].view(np.int32), one["node_score"][b, :n].view(np.int32)), b
+    # the support rows each call expanded
+    rows = _written_rows(params, wl)
+    S = min(wl.support, wl.V)
+    for f in SUP_FIELDS:
+        a, o = lay[f][:, rows], one[f][:, rows]
+        if f in ("sup_id", "sup_q", "sup_qT"):
+            a, o = a[..., :S], o[..., :S]
+        assert np.array_equal(a.view(np.int32), o.view(np.int32)), f
+    # the frontier of each call: the surviving frontier nodes of the one-shot tree
+    for b in range(wl.B):
+        n = int(one["n_nodes"][b])
+        for i in range(1, n):
+            er = int(one["node_exp_row"][b, i])
+            if er < 0:
+                continue
+            d = int(one["node_depth"][b, i])
+            r = er - _row0(wl, d)
+            assert fronts[d - 1][0][b, r] == one["node_token"][b, i], (b, i)
+    # ... and the oracle's frontiers, all of them (survivors or not)
+    idx = range(wl.B) if sample is None else sample
+    trees = parity.oracle_build(case, idx)
+    exact = exempt = 0
+    for b in idx:
+        t = trees[b]
+        ok = True
+        for layer in range(wl.depth):
+            tok, par = fronts[layer][0][b], fronts[layer][1][b]
+            ref = t.frontiers[layer] if layer < wl.depth - 1 else []
+            k = len(ref)
+            ok &= tok[:k].tolist() == [x for x, _ in ref] and par[:k].tolist() == [x for _, x in ref]
+            ok &= bool((tok[k:] == -1).all() and (par[k:] == -1).all())
+        if ok:
+            exact += 1
+        else:
+            assert t.margins.near > 0, f"tree {b}: frontier differs from the oracle without a near-tie"
+            exempt += 1
+    assert exempt <= 0.1 * len(idx) + 1
+    return exact, exempt
+
+
+LAYER_CASES = {
+    "tiny": ("tiny", dict(B=256), None),
+    "vicuna": ("vicuna", dict(B=4), None),
+    # frontiers below W in the first layers (2, 4, then 8 of W = 8)
+    "narrow": ("vicuna", dict(B=8, V=5000, K=2, W=8, depth=5, R=24), None),
+    "m0": ("vicuna", dict(B=8, V=3000, K=4, m=0, W=4, depth=4, R=16), None),
+    "topk_m_eq_K": ("vicuna", dict(B=8, V=3000, K=4, m=4, W=4, depth=4, R=16), None),
+    "f32_ragged": ("vicuna", dict(B=8, V=4099, K=6, W=3, depth=3, R=10, dtype="f32", stride=4100), None),
+    "depth1": ("vicuna", dict(B=8, V=3000, depth=1, R=8), None),
+    "llama3": ("llama3", dict(), [0, 5]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(LAYER_CASES))
+def test_layer_mode_equals_one_shot_and_oracle(name):
+    base, kw, sample = LAYER_CASES[name]
+    kw = dict(kw)
+    stride = kw.pop("stride", None)
+    wl = WL.WORKLOADS[base].with_(**kw)
+    exact, exempt = check_layer_mode(wl, 21, sample, stride)
+    print(f"{name}: frontier exact {exact} exempt {exempt}")
+
+
+def test_calls_out_of_order_set_status_and_recover():
+    wl = WL.WORKLOADS["vicuna"].with_(B=4, V=3000, K=4, W=4, depth=4, R=16)
+    case = parity.make_case(wl, 2)
+    # layer 2 right after layer 0: refused, frontier cleared, the state spoiled
+    params, tree, state, status, fronts = run_layers(case, layers=[0, 2])
+    assert int(status.item()) & B.S_LAYERS
+    assert (fronts[1][0] == -1).all() and (fronts[1][1] == -1).all()
+    B.spec_tree_finish(params, wl.V, tree, state, status)
+    assert (tree.n_nodes.cpu() == 1).all()
+    # finish before the last layer
+    status.zero_()
+    run_layers(case, layers=[0, 1], state=state, tree=tree, status=status)
+    assert int(status.item()) == 0
+    B.spec_tree_finish(params, wl.V, tree, state, status)
+    assert int(status.item()) & B.S_LAYERS and (tree.n_nodes.cpu() == 1).all()
+    # a zeroed state
+    state.state.zero_()
+    status.zero_()
+    B.spec_tree_finish(params, wl.V, tree, state, status)
+    assert int(status.item()) & B.S_LAYERS and (tree.n_nodes.cpu() == 1).all()
+    # a fresh layer 0 starts over: the full sequence gives the one-shot tree
+    status.zero_()
+    run_layers(case, state=state, tree=tree, status=status)
+    B.spec_tree_finish(params, wl.V, tree, state, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    one = parity.run_gpu(case)
+    lay = _host(tree)
+    assert np.array_equal(lay["n_nodes"], one["n_nodes"])
+    for b in range(wl.B):
+        n = int(one["n_nodes"][b])
+        for f in NODE_FIELDS:
+            assert np.array_equal(lay[f][b, :n], one[f][b, :n]), (b, f)

@@ -565,3 +565,32 @@ def test_losslessness_chi_square_two_levels(seed):
     v, c = max(second.items(), key=lambda kv: kv[1].sum())
     pv2 = _chi2_pvalue(c, O.target_probs(row_for((v,)), 1.0), int(c.sum()))
     assert pv2 > 1e-3
+
+
+def test_topr_frontiers_are_the_expanded_nodes():
+    """Each recorded frontier has min(W, layer size) entries; every kept node expanded from
+    draft row 1 + (d-1)W + r is entry r of the frontier of layer d, with its parent's rank."""
+    rng = np.random.default_rng(3)
+    p = O.Params(K=3, m=1, W=4, depth=4, R=200)
+    n_rows = 1 + (p.depth - 1) * p.W
+    rows = rng.normal(size=(n_rows, 50)) * 2.0
+    t = O.build(rows, rng.random(n_rows), p)
+    sizes, ln = [], p.K
+    for _ in range(1, p.depth):
+        sizes.append(min(ln, p.W))
+        ln = min(ln, p.W) * p.K
+    assert [len(f) for f in t.frontiers] == sizes
+    # R covers every candidate, so every frontier node is kept
+    assert t.n_nodes == 1 + t.n_candidates
+    seen = 0
+    for i in range(1, t.n_nodes):
+        if t.exp_row[i] < 0:
+            continue
+        d = int(t.depth[i])
+        r = int(t.exp_row[i]) - (1 + (d - 1) * p.W)
+        tok, prank = t.frontiers[d - 1][r]
+        assert tok == t.token[i]
+        par = int(t.parent[i])
+        assert prank == (-1 if d == 1 else int(t.exp_row[par]) - (1 + (d - 2) * p.W))
+        seen += 1
+    assert seen == sum(sizes)
