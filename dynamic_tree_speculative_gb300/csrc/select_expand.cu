@@ -4,32 +4,39 @@
 // logits) and Key design 2 (top-m deterministic children, probe sampled from
 // the renormalised tempered tail, tail masses).
 //
-// A persistent CTA owns rows; one producer warp streams every row twice
+// A persistent CTA owns rows; one producer warp streams every row once
 // through a ring of shared-memory stages filled by the TMA engine
 // (cp.async.bulk, "full" mbarriers with transaction counts, "empty" mbarriers
 // released by the consumer warps), so the consumers never wait on a CTA-wide
-// barrier per chunk and the next row is already landing while a row's
-// selection runs.
+// barrier per chunk and the next row is already landing while a row's tail
+// work runs.
 //
-//   pass 1 (HBM, kept in L2 with an evict-last hint): every consumer thread
-//     folds its elements into a running maximum (four bf16x2 max per 16-byte
-//     vector).  Thread maxima are distinct elements of the row, so if warp w's
+//   pass (HBM, kept in L2 with an evict-last hint): each consumer thread
+//     reduces its four vectors of every chunk to their maximum with one
+//     packed bf16x2 tree and writes it, as a 16-bit order key, to a table
+//     in shared memory (thread x chunk); it also keeps its running maximum.
+//   bound: thread maxima are distinct elements of the row, so if warp w's
 //     j-th largest thread maximum is b_w, with j * (consumer warps) >= |S|,
 //     then min_w b_w is a lower bound of the |S|-th largest logit.
-//   pass 2 (L2, evict-first): a vector's maximum is tested against the bound
-//     with packed bf16x2 compares; only vectors that reach it build an element
-//     mask (four more packed compares) and append their elements, with one
-//     shared atomic per lane, to a candidate buffer of 64-bit
-//     (order key, ~token id) composites -- typically ~250 per 128K-token row.
-//   select: an exact radix select over the composites gives the top-|S| by
-//     (logit desc, id asc); a rank count sorts them; warps 0..3 turn them into
-//     q, q_T, z, z_T and the probe (one support rank per thread).
+//   gather: only the (chunk, thread) pairs whose table entry reaches the
+//     bound can hold a candidate -- typically ~250 of 4096 per 128K-token
+//     row.  They are listed, the list's vectors are re-read with plain loads
+//     spread over the whole CTA (one round of loads in flight), and every
+//     element that reaches the bound is appended to a candidate buffer of
+//     64-bit (order key, ~token id) composites and counted in a histogram of
+//     key offsets above the bound.
+//   select (one warp, overlapped with the next row): the histogram gives the
+//     |S|-th largest key and the count above it; the candidates are cut to
+//     the exact top-|S| by (logit desc, id asc), ranked by a count, and turned
+//     into q, q_T, z, z_T and the probe.
 //
-// Rows whose candidates overflow the buffer (massive ties at the bound) are
-// redone by a robust path that streams the row from global memory in id
-// order, keeping the exact top-|S| of the prefix seen and a strict threshold.
+// Rows whose candidates overflow the buffer (massive ties at the bound), whose
+// bound has no value (NaN), or that are longer than the table are redone by a
+// robust path that streams the row from global memory in id order, keeping
+// the exact top-|S| of the prefix seen and a strict threshold.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "st_common.cuh"
@@ -47,31 +54,47 @@ constexpr int SX_CHUNK = SX_CONS * 16 * SX_VPT;  // 16 KB per stage
 constexpr int SX_STAGES = 5;
 constexpr int SX_FB_THREADS = 128;               // robust path: threads reading per step
 constexpr int SX_CAP = 640;                      // candidates of one row (64-bit composites)
-constexpr int SX_QCAP = 896;                     // pass-2 queue of vectors that reach the bound
-constexpr int SX_QW = SX_QCAP / SX_CWARPS;       // queue slots owned by each consumer warp
 constexpr int SX_FB_STEP = SX_FB_THREADS * 8;    // robust path: at most this many appends per step
-constexpr int SX_FB_CAP = SX_QCAP * 2;           // robust path: candidates live in the queue's storage
+constexpr int SX_FB_CAP = 1792;                  // robust path: candidate storage
 constexpr int SX_FB_HIGH = SX_FB_CAP - SX_FB_STEP;
+constexpr int SX_TBL = 32;                       // chunk maxima kept per thread: rows of up to 32 chunks
+constexpr int SX_GLIST = 1024;                   // gather list: (chunk, thread) pairs whose maximum reaches the bound
+// what the selector receives with a row's candidates
+constexpr int SX_HIST = 1;     // every element >= hbase, with its key histogram khist
+constexpr int SX_SORTED = 2;   // exactly the top-|S|, in order
+
+// Storage of the robust path (consumer threads), used only after the
+// table of chunk maxima, so the two share it.
+struct RobustScratch {
+  uint64_t fbuf[SX_FB_CAP];
+  uint64_t sel[SPEC_TREE_MAX_SUPPORT];
+  uint64_t tie[32];
+  uint32_t hist[256];
+};
 
 struct SelShared {
   alignas(128) uint8_t ring[SX_STAGES][SX_CHUNK];
   uint64_t cand[2][SX_CAP];  // double-buffered candidates: streamers fill one, the selector drains the other
-  uint4 qvec[SX_QCAP];
-  uint32_t qid[SX_QCAP];
-  uint64_t sel[SPEC_TREE_MAX_SUPPORT];   // streamers' scratch (robust path)
-  uint64_t ssel[SPEC_TREE_MAX_SUPPORT];  // selector's scratch
-  uint64_t tie[32];
+  union {
+    uint16_t tbl[SX_TBL][SX_CONS];  // order key of each consumer thread's maximum in each chunk
+    RobustScratch rb;
+  };
+  uint16_t glist[SX_GLIST];  // chunk << 8 | thread
+  alignas(16) uint64_t ssel[SPEC_TREE_MAX_SUPPORT];  // selector's scratch
+  uint64_t stie[32];                      // selector's ties
+  uint32_t khist[2][256];  // per candidate buffer: histogram of candidate keys above hbase
   uint64_t full[SX_STAGES];
   uint64_t empty[SX_STAGES];
   uint64_t cfull[2];   // candidates of a row ready for the selector
   uint64_t cempty[2];  // selector done with a candidate buffer
   int64_t cand_row[2];  // output row (support arrays) of the candidates
   int64_t cand_in[2];   // input row (logits, u_probe) of the candidates
-  uint32_t hist[256];
   uint32_t shist[256];
   uint32_t warp_bound[SX_CWARPS];
   int count[2];
-  int qn_warp[SX_CWARPS];
+  int mode[2];         // candidates handed over: SX_HIST or SX_SORTED
+  uint32_t hbase[2];   // SX_HIST: the bound the candidates reach (bin 0 of khist)
+  int glist_n;
   int sel_count;
   int tie_count;
   int radix_bin;
@@ -88,6 +111,9 @@ struct CandBuf {
   int* n;
   int cap;
 };
+
+// two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
+static_assert(sizeof(SelShared) <= 233472 / 2 - 1024, "select_expand needs two CTAs per SM");
 
 size_t select_expand_smem_bytes() { return sizeof(SelShared); }
 
@@ -295,7 +321,9 @@ struct Filter<__nv_bfloat16> {
     mx = __hmax2(mx, __lowhigh2highlow(mx));
     return __hbge2(mx, b2);
   }
-  __device__ __forceinline__ void emit(CandBuf cb, const uint4& v, uint32_t id0, bool& overflow) const {
+  // hist (or null): per key offset above hbase, the last bin collecting the rest
+  __device__ __forceinline__ void emit(CandBuf cb, const uint4& v, uint32_t id0, bool& overflow,
+                                       uint32_t* hist = nullptr, uint32_t hbase = 0) const {
     const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
     const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
     const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
@@ -309,8 +337,10 @@ struct Filter<__nv_bfloat16> {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (mask & (1u << j)) {
-        if (pos < cb.cap) cb.c[pos] = make_comp(elem_key<__nv_bfloat16>(v, j, nf), id0 + j);
+        const uint32_t key = elem_key<__nv_bfloat16>(v, j, nf);
+        if (pos < cb.cap) cb.c[pos] = make_comp(key, id0 + j);
         else overflow = true;
+        if (hist) atomicAdd(&hist[min(key - hbase, 255u)], 1u);
         ++pos;
       }
     }
@@ -341,7 +371,8 @@ struct Filter<float> {
     for (int j = 0; j < 4; ++j) k = max(k, elem_key<float>(v, j, nf));
     return k >= bound;
   }
-  __device__ __forceinline__ void emit(CandBuf cb, const uint4& v, uint32_t id0, bool& overflow) const {
+  __device__ __forceinline__ void emit(CandBuf cb, const uint4& v, uint32_t id0, bool& overflow,
+                                       uint32_t* hist = nullptr, uint32_t hbase = 0) const {
     bool nf = false;
     uint32_t keys[4], mask = 0;
 #pragma unroll
@@ -355,22 +386,27 @@ struct Filter<float> {
       if (mask & (1u << j)) {
         if (pos < cb.cap) cb.c[pos] = make_comp(keys[j], id0 + j);
         else overflow = true;
+        if (hist) atomicAdd(&hist[min(keys[j] - hbase, 255u)], 1u);
         ++pos;
       }
     }
   }
 };
 
-// j-th largest of the 32 lane values of a warp (binary search on key bits).
-template <int KEY_BITS>
+// j-th largest (1 <= j <= 32, with multiplicity) of the 32 lane values of a
+// warp: repeated warp maxima, each round retiring every lane that holds the
+// current maximum, so at most j rounds.  0 when fewer than j values are
+// nonzero.
 __device__ __forceinline__ uint32_t warp_kth_largest(uint32_t key, int j) {
-  uint32_t res = 0;
-#pragma unroll
-  for (int bit = KEY_BITS - 1; bit >= 0; --bit) {
-    const uint32_t cand = res | (1u << bit);
-    if (__popc(__ballot_sync(FULL, key >= cand)) >= j) res = cand;
+  uint32_t x = key;
+  for (int it = 0; it < 32; ++it) {
+    const uint32_t m = __reduce_max_sync(FULL, x);
+    const int c = __popc(__ballot_sync(FULL, x == m));
+    if (j <= c || m == 0u) return m;
+    j -= c;
+    if (x == m) x = 0u;
   }
-  return res;
+  return 0u;
 }
 
 // Exact top-k of cb.c[0..n) (distinct composites) sorted descending into
@@ -390,7 +426,7 @@ __device__ void select_topk(SelShared& s, CandBuf cb, int n, int k) {
 #pragma unroll 1
     for (int d = 0; d < NKD + 3; ++d) {
       const int sh = d < NKD ? 32 + KEY_BITS - 8 * (d + 1) : 8 * (NKD + 2 - d);
-      s.hist[tid] = 0;
+      s.rb.hist[tid] = 0;
       csync();
       for (int i = tid; i < n_round; i += SX_CONS) {
         bool valid = i < n;
@@ -399,14 +435,14 @@ __device__ void select_topk(SelShared& s, CandBuf cb, int n, int k) {
         const uint32_t bin = static_cast<uint32_t>(c >> sh) & 0xffu;
         const uint32_t tag = valid ? bin : (0x100u | lane);
         const unsigned peers = __match_any_sync(FULL, tag);
-        if (valid && lane == __ffs(peers) - 1) atomicAdd(&s.hist[bin], static_cast<uint32_t>(__popc(peers)));
+        if (valid && lane == __ffs(peers) - 1) atomicAdd(&s.rb.hist[bin], static_cast<uint32_t>(__popc(peers)));
       }
       csync();
       if (warp == 0) {
         uint32_t h[8], tot = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          h[j] = s.hist[255 - 8 * lane - j];
+          h[j] = s.rb.hist[255 - 8 * lane - j];
           tot += h[j];
         }
         uint32_t incl = tot;
@@ -453,34 +489,34 @@ __device__ void select_topk(SelShared& s, CandBuf cb, int n, int k) {
       const uint64_t m = c & pmask;
       if (tie_mode ? m > prefix : m >= prefix) {
         const int pos = atomicAdd(&s.sel_count, 1);
-        if (pos < SPEC_TREE_MAX_SUPPORT) s.sel[pos] = c;
+        if (pos < SPEC_TREE_MAX_SUPPORT) s.rb.sel[pos] = c;
       } else if (tie_mode && m == prefix) {
         const int pos = atomicAdd(&s.tie_count, 1);
-        if (pos < 32) s.tie[pos] = c;
+        if (pos < 32) s.rb.tie[pos] = c;
       }
     }
     csync();
     if (tie_mode && warp == 0) {
       const int nt = min(s.tie_count, 32);
-      const uint64_t c = lane < nt ? s.tie[lane] : 0ull;
+      const uint64_t c = lane < nt ? s.rb.tie[lane] : 0ull;
       int r = 0;
-      for (int j = 0; j < nt; ++j) r += s.tie[j] > c;
+      for (int j = 0; j < nt; ++j) r += s.rb.tie[j] > c;
       if (lane < nt && r < need) {
         const int pos = atomicAdd(&s.sel_count, 1);
-        if (pos < SPEC_TREE_MAX_SUPPORT) s.sel[pos] = c;
+        if (pos < SPEC_TREE_MAX_SUPPORT) s.rb.sel[pos] = c;
       }
     }
     csync();
   } else {
-    for (int i = tid; i < n; i += SX_CONS) s.sel[i] = cb.c[i];
+    for (int i = tid; i < n; i += SX_CONS) s.rb.sel[i] = cb.c[i];
     csync();
   }
   const int kk = n < k ? n : k;
   uint64_t c = 0;
   int r = 0;
   if (tid < kk) {
-    c = s.sel[tid];
-    for (int j = 0; j < kk; ++j) r += (s.sel[j] > c);
+    c = s.rb.sel[tid];
+    for (int j = 0; j < kk; ++j) r += (s.rb.sel[j] > c);
   }
   csync();
   if (tid < kk) cb.c[r] = c;
@@ -493,6 +529,56 @@ __device__ void select_topk(SelShared& s, CandBuf cb, int n, int k) {
     }
   }
   csync();
+}
+
+// Maximum of a consumer thread's four vectors of a chunk (vectors past the
+// row given as -inf) as a 16-bit order key for the table, and the full
+// order key for the thread's running maximum.  bf16: one packed tree of
+// NaN-propagating maxima; a NaN among the elements makes the table entry
+// 0xffff (the chunk is examined element by element) and sets nan.  f32: the
+// largest element key (NaN excluded, flagged); the table keeps its upper 16
+// bits, which order the same way and only ever let more chunks through.
+template <typename T>
+__device__ __forceinline__ uint32_t chunk_max(const uint4 (&v)[SX_VPT], bool& nan, uint32_t& full);
+
+template <>
+__device__ __forceinline__ uint32_t chunk_max<__nv_bfloat16>(const uint4 (&v)[SX_VPT], bool& nan, uint32_t& full) {
+  __nv_bfloat162 w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __nv_bfloat162 x0 = reinterpret_cast<const __nv_bfloat162*>(&v[0])[j];
+    const __nv_bfloat162 x1 = reinterpret_cast<const __nv_bfloat162*>(&v[1])[j];
+    const __nv_bfloat162 x2 = reinterpret_cast<const __nv_bfloat162*>(&v[2])[j];
+    const __nv_bfloat162 x3 = reinterpret_cast<const __nv_bfloat162*>(&v[3])[j];
+    w[j] = __hmax2_nan(__hmax2_nan(x0, x1), __hmax2_nan(x2, x3));
+  }
+  __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(w[0], w[1]), __hmax2_nan(w[2], w[3]));
+  m = __hmax2_nan(m, __lowhigh2highlow(m));
+  const uint32_t bits = __bfloat16_as_ushort(m.x);
+  if ((bits & 0x7fffu) > 0x7f80u) {
+    nan = true;
+    full = 0u;
+    return 0xffffu;
+  }
+  full = bf16_key(bits);
+  return full;
+}
+
+template <>
+__device__ __forceinline__ uint32_t chunk_max<float>(const uint4 (&v)[SX_VPT], bool& nan, uint32_t& full) {
+  uint32_t k = 0u;
+#pragma unroll
+  for (int q = 0; q < SX_VPT; ++q)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) k = max(k, elem_key<float>(v[q], j, nan));
+  full = k;
+  return k >> 16;
+}
+
+// Table threshold of a bound: entries at or above it may hold an element >= bound.
+template <typename T>
+__device__ __forceinline__ uint32_t table_bound(uint32_t bound) {
+  return sizeof(T) == 2 ? bound : bound >> 16;
 }
 
 struct SelArgs {
@@ -692,6 +778,111 @@ __device__ int warp_select_sort(SelShared& s, const uint64_t* c, int n, int k, u
   return kk;
 }
 
+// Exact top-k (k <= 128), sorted descending, of candidates that are every
+// element of the row with a key >= hbase, given their key histogram h (bin b:
+// key hbase + b; the last bin also takes every larger key), by one warp.
+// The histogram gives the k-th largest key t and the count above it; keys
+// above t are in, and of the keys equal to t the smallest ids fill the rest.
+// A rank count then orders the k.  Falls back to warp_select_sort when t
+// falls in the open last bin or more than 32 keys tie at t.
+template <int KEY_BITS>
+__device__ int warp_hist_select_sort(SelShared& s, const uint64_t* c, int n, int k, const uint32_t* h,
+                                     uint32_t hbase, uint64_t (&val)[4]) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  uint32_t hv[8], tot = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    hv[j] = h[255 - 8 * lane - j];
+    tot += hv[j];
+  }
+  uint32_t incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint32_t excl = incl - tot, kk = static_cast<uint32_t>(k);
+  int bin = -1, above = 0, nt = 0;
+  if (excl < kk && kk <= incl) {
+    uint32_t acc = excl;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (bin < 0 && kk <= acc + hv[j]) {
+        bin = 255 - 8 * lane - j;
+        above = static_cast<int>(acc);
+        nt = static_cast<int>(hv[j]);
+      }
+      acc += hv[j];
+    }
+  }
+  const int src = __ffs(__ballot_sync(FULL, bin >= 0)) - 1;
+  if (src < 0) return warp_select_sort<KEY_BITS>(s, c, n, k, val);
+  bin = __shfl_sync(FULL, bin, src);
+  above = __shfl_sync(FULL, above, src);
+  nt = __shfl_sync(FULL, nt, src);
+  const int need = k - above;
+  if (bin == 255 || (nt > 32 && nt != need)) return warp_select_sort<KEY_BITS>(s, c, n, k, val);
+  const uint32_t t = hbase + static_cast<uint32_t>(bin);
+  const bool all_ties = nt == need;
+  int base = 0, nties = 0;
+  for (int i0 = 0; i0 < n; i0 += 32) {
+    const int i = i0 + lane;
+    const uint64_t x = i < n ? c[i] : 0ull;
+    const uint32_t key = static_cast<uint32_t>(x >> 32);
+    const bool valid = i < n;
+    const bool take = valid && (key > t || (key == t && all_ties));
+    const bool tie = valid && key == t && !all_ties;
+    const unsigned tb = __ballot_sync(FULL, take);
+    if (take) s.ssel[base + __popc(tb & lt)] = x;
+    base += __popc(tb);
+    const unsigned eb = __ballot_sync(FULL, tie);
+    if (tie) s.stie[nties + __popc(eb & lt)] = x;
+    nties += __popc(eb);
+  }
+  __syncwarp();
+  if (!all_ties) {
+    // the `need` smallest ids among the keys equal to t (larger composite = smaller id)
+    const uint64_t x = lane < nties ? s.stie[lane] : 0ull;
+    int r = 0;
+    for (int j = 0; j < nties; ++j) r += s.stie[j] > x;
+    const bool take = lane < nties && r < need;
+    const unsigned tb = __ballot_sync(FULL, take);
+    if (take) s.ssel[base + __popc(tb & lt)] = x;
+    base += __popc(tb);
+    __syncwarp();
+  }
+  // rank of each of the k among them, then into rank order
+  uint64_t x[4];
+  int r[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    x[j] = j * 32 + lane < k ? s.ssel[j * 32 + lane] : 0ull;
+    r[j] = 0;
+  }
+  const uint4* s4 = reinterpret_cast<const uint4*>(s.ssel);
+  for (int i = 0; i < k / 2; ++i) {
+    const uint4 w = s4[i];
+    const uint64_t y0 = (static_cast<uint64_t>(w.y) << 32) | w.x;
+    const uint64_t y1 = (static_cast<uint64_t>(w.w) << 32) | w.z;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) r[j] += (y0 > x[j]) + (y1 > x[j]);
+  }
+  if (k & 1) {
+    const uint64_t y = s.ssel[k - 1];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) r[j] += y > x[j];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (j * 32 + lane < k) s.ssel[r[j]] = x[j];
+  __syncwarp();
+  warp_load<4>(s.ssel, k, val);
+  __syncwarp();
+  return k;
+}
+
 // Softmaxes, tail masses and the probe of one row from its sorted support,
 // by the selector warp (rank j*32 + lane in val[j]).  RheoSampling Key design
 // 2; the probe is the first tail rank k with u * z_T < sum_{j=m..k} q_T(j),
@@ -794,6 +985,7 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
     fence_mbar_init();
     s.timeout = 0;
   }
+  for (int i = tid; i < 2 * 256; i += SX_THREADS) s.khist[i >> 8][i & 255] = 0u;
   __syncthreads();  // the last CTA-wide barrier: the roles split below
   grid_dependency_wait();
   grid_dependents_launch();
@@ -809,8 +1001,20 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
       const int n = s.count[q];
       const int64_t out_row = s.cand_row[q], in_row = s.cand_in[q];
       uint64_t val[4];
-      const int n_sup = warp_select_sort<E::KEY_BITS>(s, s.cand[q], min(n, SX_CAP), a.S, val);
+      int n_sup;
+      const int mode = s.mode[q];
+      if (mode == SX_SORTED) {
+        n_sup = n;
+        warp_load<4>(s.cand[q], n, val);
+      } else if (mode == SX_HIST) {
+        n_sup = warp_hist_select_sort<E::KEY_BITS>(s, s.cand[q], min(n, SX_CAP), a.S, s.khist[q], s.hbase[q], val);
+      } else {
+        n_sup = warp_select_sort<E::KEY_BITS>(s, s.cand[q], min(n, SX_CAP), a.S, val);
+      }
       expand_epilogue<T>(val, a, out_row, in_row, n_sup);
+      // the histogram starts the buffer's next row at zero
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s.khist[q][j * 32 + lane] = 0u;
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.cempty[q]);
     }
@@ -821,8 +1025,7 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
   if (warp == SX_PROD_WARP) {
     // ------------------------------------------------------------ producer ---
     if (lane == 0 && nch > 0) {
-      const uint64_t keep = l2_evict_last_policy();
-      const uint64_t drop = l2_evict_first_policy();
+      const uint64_t keep = l2_evict_last_policy();  // the gather re-reads a few vectors from L2
       int st = 0;
       uint32_t phase = 0;
       int64_t g = 0;
@@ -830,18 +1033,16 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
       int64_t b = blockIdx.x / a.rows_used, e = blockIdx.x % a.rows_used;
       for (int64_t lr = 0; lr < my_rows; ++lr) {
         const uint8_t* row = a.logits + (b * a.in_rows + e) * a.row_bytes_stride;
-        for (int pass = 0; pass < 2; ++pass) {
-          for (int c = 0; c < nch; ++c, ++g) {
-            // stage reuse: wait until every consumer warp released its last use
-            if (g >= SX_STAGES && !mbar_wait(&s.empty[st], phase ^ 1u)) timed_out = true;
-            const int64_t off = static_cast<int64_t>(c) * SX_CHUNK;
-            const uint32_t bytes = static_cast<uint32_t>(min64(SX_CHUNK, tma_bytes - off));
-            mbar_expect_tx(&s.full[st], bytes);
-            bulk_g2s(s.ring[st], row + off, bytes, &s.full[st], pass == 0 ? keep : drop);
-            if (++st == SX_STAGES) {
-              st = 0;
-              phase ^= 1u;
-            }
+        for (int c = 0; c < nch; ++c, ++g) {
+          // stage reuse: wait until every consumer warp released its last use
+          if (g >= SX_STAGES && !mbar_wait(&s.empty[st], phase ^ 1u)) timed_out = true;
+          const int64_t off = static_cast<int64_t>(c) * SX_CHUNK;
+          const uint32_t bytes = static_cast<uint32_t>(min64(SX_CHUNK, tma_bytes - off));
+          mbar_expect_tx(&s.full[st], bytes);
+          bulk_g2s(s.ring[st], row + off, bytes, &s.full[st], keep);
+          if (++st == SX_STAGES) {
+            st = 0;
+            phase ^= 1u;
           }
         }
         e += gridDim.x;  // next row of this CTA, without dividing
@@ -861,145 +1062,154 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
   uint32_t phase = 0;
   int64_t b = blockIdx.x / a.rows_used, e = blockIdx.x % a.rows_used;
   const int jth = (a.S + SX_CWARPS - 1) / SX_CWARPS;
+  const bool tabled = nch <= SX_TBL;  // longer rows take the robust path
+  const bool has_vec = nch > 1 || tid < last_nvec;  // this thread sees at least one whole vector
   for (int64_t lr = 0; lr < my_rows; ++lr) {
     const int64_t out_row = b * a.n_rows + a.sup_row0 + e;
     const int64_t in_row = b * a.in_rows + e;
     const uint8_t* row = a.logits + in_row * a.row_bytes_stride;
+    // candidate buffer of this row (the selector may still drain it from two rows ago)
+    const int q = static_cast<int>(lr & 1);
+    const CandBuf cb{s.cand[q], &s.count[q], SX_CAP};
+    uint32_t* const kh = s.khist[q];  // zeroed by the selector once it is done with the buffer
 
-    // pass 1: running maximum of this thread's elements
-    RunMax<T> rm;
-    rm.init();
+    // the one pass over the row: each thread's maximum in every chunk goes
+    // to the table, and its running maximum is kept
+    uint32_t tkey = 0u;
+    bool row_nan = false;
     for (int c = 0; c < nch; ++c) {
       if (!mbar_wait(&s.full[st], phase)) s.timeout = 1;
+      const int nvec = c + 1 < nch ? SX_CHUNK / 16 : last_nvec;
       const uint4* src = reinterpret_cast<const uint4*>(s.ring[st]) + tid;
       uint4 v[SX_VPT];
-      if (c + 1 < nch) {  // full chunk
+      if (c + 1 < nch) {
 #pragma unroll
         for (int k = 0; k < SX_VPT; ++k) v[k] = src[k * SX_CONS];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.empty[st]);
-        rm.add4(v);
       } else {
+        const uint32_t ninf = sizeof(T) == 2 ? 0xff80ff80u : 0xff800000u;
 #pragma unroll
         for (int k = 0; k < SX_VPT; ++k)
-          v[k] = tid + k * SX_CONS < last_nvec ? src[k * SX_CONS] : make_uint4(0, 0, 0, 0);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.empty[st]);
-#pragma unroll
-        for (int k = 0; k < SX_VPT; ++k)
-          if (tid + k * SX_CONS < last_nvec) rm.add(v[k]);
+          v[k] = tid + k * SX_CONS < nvec ? src[k * SX_CONS] : make_uint4(ninf, ninf, ninf, ninf);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.empty[st]);
+      uint32_t full;
+      const uint32_t ck = chunk_max<T>(v, row_nan, full);
+      tkey = max(tkey, full);
+      if (tabled) s.tbl[c][tid] = static_cast<uint16_t>(ck);
       if (++st == SX_STAGES) {
         st = 0;
         phase ^= 1u;
       }
     }
     const int tail_id = tail_begin + tid;  // elements past the last whole vector
-    uint32_t tail_key = 0;
-    if (tail_id < a.V) {
-      tail_key = scalar_key<T>(row, tail_id, nonfinite);
-      rm.add_key(tail_key);
-    }
-    // candidate buffer of this row (the selector may still drain it from two rows ago)
-    const int q = static_cast<int>(lr & 1);
-    const CandBuf cb{s.cand[q], &s.count[q], SX_CAP};
-    // bound: min over consumer warps of the warp's jth-largest thread maximum
-    const uint32_t wb = warp_kth_largest<E::KEY_BITS>(rm.key(nonfinite), jth);
-    if (lane == 0) s.warp_bound[warp] = wb;
+    uint32_t tail_key = 0u;
+    if (tail_id < a.V) tail_key = scalar_key<T>(row, tail_id, row_nan);
+    nonfinite = nonfinite || row_nan;
+    // a thread's maximum as an order key; 0 (no value) for a thread that saw
+    // nothing, or a NaN among bf16 elements (its real maximum is unknown)
+    uint32_t tmax = has_vec ? tkey : 0u;
+    if (sizeof(T) == 2 && row_nan) tmax = 0u;
+    tmax = max(tmax, tail_key);
+    // the bound: the minimum over warps of each warp's jth-largest thread
+    // maximum.  Thread maxima are distinct elements of the row and
+    // jth * warps >= |S|, so at least |S| elements reach it.
+    const uint32_t wv = warp_kth_largest(tmax, jth);
+    if (lane == 0) s.warp_bound[warp] = wv;
     if (tid == 0) {
       if (lr >= 2 && !mbar_wait(&s.cempty[q], static_cast<uint32_t>(((lr >> 1) - 1) & 1))) s.timeout = 1;
       *cb.n = 0;
+      s.glist_n = 0;
     }
     csync();
     uint32_t bound = 0xffffffffu;
 #pragma unroll
     for (int w = 0; w < SX_CWARPS; ++w) bound = min(bound, s.warp_bound[w]);
-    // a bound of key 0 (a thread maximum was NaN) has no value to compare
-    // against: such rows take the robust path below
-    const bool robust = bound == 0u;
-    Filter<T> flt;
-    flt.init(robust ? 0xffffffffu : bound);
-
-    // pass 2: vectors that reach the bound go to this warp's queue slots
-    // (ballot-ranked, no atomics); their elements are examined after the
-    // pass with every lane busy instead of one lane per warp
-    uint32_t qn_w = 0;  // warp-uniform count of queued vectors
-    uint4* const wq = s.qvec + warp * SX_QW;
-    uint32_t* const wqid = s.qid + warp * SX_QW;
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int c = 0; c < nch; ++c) {
-      if (!mbar_wait(&s.full[st], phase)) s.timeout = 1;
-      const int nvec = c + 1 < nch ? SX_CHUNK / 16 : last_nvec;
-      const uint4* src = reinterpret_cast<const uint4*>(s.ring[st]) + tid;
-      uint4 v[SX_VPT];
-      const bool full_chunk = c + 1 < nch;
-      if (full_chunk) {
+    // a key-0 bound (NaN, or too few elements) has no value to compare against
+    bool robust = bound == 0u || !tabled;
+    if (!robust) {
+      // the gather list: every (chunk, thread) whose maximum reaches the
+      // bound (warp-aggregated appends)
+      const uint32_t tb = table_bound<T>(bound);
+      uint32_t hits = 0u;
+      for (int c = 0; c < nch; ++c) hits |= (static_cast<uint32_t>(s.tbl[c][tid]) >= tb ? 1u : 0u) << c;
+      const int nh = __popc(hits);
+      int incl = nh;
 #pragma unroll
-        for (int k = 0; k < SX_VPT; ++k) v[k] = src[k * SX_CONS];
-      } else {
-#pragma unroll
-        for (int k = 0; k < SX_VPT; ++k) v[k] = tid + k * SX_CONS < nvec ? src[k * SX_CONS] : make_uint4(0, 0, 0, 0);
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += y;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.empty[st]);
-      // one test for the thread's four vectors (their element-wise maximum)
-      // before testing them one by one
-      bool any = true;
-      if (tid + (SX_VPT - 1) * SX_CONS < nvec) any = flt.pass(Filter<T>::merge4(v));
-      if (__any_sync(FULL, any)) {
+      int gbase = 0;
+      if (lane == 31) gbase = atomicAdd(&s.glist_n, incl);
+      gbase = __shfl_sync(FULL, gbase, 31) + incl - nh;
+      while (hits) {
+        const int c = __ffs(hits) - 1;
+        hits &= hits - 1u;
+        if (gbase < SX_GLIST) s.glist[gbase] = static_cast<uint16_t>((c << 8) | tid);
+        ++gbase;
+      }
+      csync();
+      const int nlist = s.glist_n;
+      robust = nlist > SX_GLIST;  // more than the candidate buffer could hold anyway
+    }
+    if (!robust) {
+      // the gather: the listed vectors are re-read from L2 (each list entry
+      // is the four vectors of one thread in one chunk, spread over the CTA
+      // so that every load is in flight at once), and every element that
+      // reaches the bound is appended to the candidates and counted in the
+      // key histogram
+      Filter<T> flt;
+      flt.init(bound);
+      const int ntask = s.glist_n * SX_VPT;
+      for (int i0 = 0; i0 < ntask; i0 += SX_CONS * SX_VPT) {
+        uint4 v[SX_VPT];
+        uint32_t vid[SX_VPT];
+        bool ok[SX_VPT];
 #pragma unroll
-        for (int k = 0; k < SX_VPT; ++k) {
-          const int vi = tid + k * SX_CONS;
-          const bool hit = any && vi < nvec && flt.pass(v[k]);
-          const unsigned bal = __ballot_sync(FULL, hit);
-          if (bal) {
-            const uint32_t pos = qn_w + __popc(bal & lt_mask);
-            if (hit && pos < SX_QW) {
-              wq[pos] = v[k];
-              wqid[pos] = static_cast<uint32_t>(c * CHUNK_ELEMS + vi * VEC);
-            }
-            qn_w += __popc(bal);
+        for (int u = 0; u < SX_VPT; ++u) {
+          const int i = i0 + u * SX_CONS + tid;
+          ok[u] = false;
+          vid[u] = 0u;
+          v[u] = make_uint4(0, 0, 0, 0);
+          if (i < ntask) {
+            const uint32_t ent = s.glist[i / SX_VPT];
+            const int c = static_cast<int>(ent >> 8);
+            const int vi = static_cast<int>(ent & 0xffu) + (i % SX_VPT) * SX_CONS;
+            const int nvec = c + 1 < nch ? SX_CHUNK / 16 : last_nvec;
+            ok[u] = vi < nvec;
+            vid[u] = static_cast<uint32_t>(c * CHUNK_ELEMS + vi * VEC);
+            if (ok[u]) v[u] = ldg_stream(row + static_cast<int64_t>(c) * SX_CHUNK + static_cast<int64_t>(vi) * 16);
           }
         }
-      }
-      if (++st == SX_STAGES) {
-        st = 0;
-        phase ^= 1u;
-      }
-    }
-    if (lane == 0) s.qn_warp[warp] = static_cast<int>(qn_w);
-    csync();
-    bool q_over = false;
-    int qtot = 0;
 #pragma unroll
-    for (int w = 0; w < SX_CWARPS; ++w) {
-      q_over = q_over || s.qn_warp[w] > SX_QW;
-      qtot += min(s.qn_warp[w], SX_QW);
-    }
-    if (!q_over) {
-      for (int i = tid; i < qtot; i += SX_CONS) {
-        // flat index -> (warp region, slot)
-        int w = 0, rem = i;
-        while (rem >= s.qn_warp[w]) {
-          rem -= s.qn_warp[w];
-          ++w;
-        }
-        flt.emit(cb, s.qvec[w * SX_QW + rem], s.qid[w * SX_QW + rem], p2over);
+        for (int u = 0; u < SX_VPT; ++u)
+          if (ok[u] && flt.pass(v[u])) flt.emit(cb, v[u], vid[u], p2over, kh, bound);
       }
-      if (tail_id < a.V && tail_key >= bound && !robust) {
+      if (tail_id < a.V && tail_key >= bound) {
         const int pos = atomicAdd(cb.n, 1);
         if (pos < cb.cap) cb.c[pos] = make_comp(tail_key, static_cast<uint32_t>(tail_id));
+        atomicAdd(&kh[min(tail_key - bound, 255u)], 1u);
+      }
+      csync();
+      if (*cb.n <= SX_CAP) {
+        // the selector cuts them to the top-|S| with the histogram
+        if (tid == 0) {
+          s.mode[q] = SX_HIST;
+          s.hbase[q] = bound;
+        }
+      } else {
+        robust = true;  // massive ties at the bound
       }
     }
-    csync();
-    if (*cb.n > SX_CAP || robust || q_over) {
-      // massive ties at the bound: redo the row in id order from global
-      // memory, with the (now idle) queue storage as the candidate buffer,
-      // then hand the selector the exact top-|S|
-      const CandBuf fb{reinterpret_cast<uint64_t*>(s.qvec), &s.count[q], SX_FB_CAP};
+    if (robust) {
+      // redo the row in id order from global memory with the robust path's
+      // own candidate storage, then hand the selector the exact top-|S|
+      const CandBuf fb{s.rb.fbuf, &s.count[q], SX_FB_CAP};
       select_row_fallback<T>(s, fb, row, a.V, a.S, nonfinite, overflow);
       select_topk<E::KEY_BITS>(s, fb, *fb.n, a.S);
       for (int i = tid; i < *fb.n; i += SX_CONS) cb.c[i] = fb.c[i];
+      if (tid == 0) s.mode[q] = SX_SORTED;  // select_topk leaves them in order
       csync();
     }
     // hand the candidates to the selector warp and move on to the next row
