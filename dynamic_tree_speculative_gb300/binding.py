@@ -28,7 +28,7 @@ MAX_SUPPORT = 128
 
 EXPORTS = ("spec_tree_rows_needed", "spec_tree_check_params", "spec_tree_select_expand", "spec_tree_rank",
            "spec_tree_build", "spec_tree_verify", "spec_tree_layer_state_bytes", "spec_tree_layer_rows",
-           "spec_tree_layer", "spec_tree_finish", "spec_tree_strerror")
+           "spec_tree_layer", "spec_tree_finish", "spec_tree_smart_fit", "spec_tree_strerror")
 
 
 class SpecTreeError(RuntimeError):
@@ -66,6 +66,8 @@ def _load():
     lib.spec_tree_layer_rows.argtypes = [P, i32]
     lib.spec_tree_layer.argtypes = [P, i32, i32, i32, i32, vp, i64, vp, T, vp, vp, vp, vp, vp]
     lib.spec_tree_finish.argtypes = [P, i32, i32, T, vp, vp, vp]
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.spec_tree_smart_fit.argtypes = [i32, dp, dp, dp, ctypes.c_double, dp, P, dp, dp]
     lib.spec_tree_strerror.argtypes = [i32]
     lib.spec_tree_strerror.restype = ctypes.c_char_p
     for name in EXPORTS:
@@ -242,6 +244,40 @@ def spec_tree_finish(params: Params, V: int, tree: TreeBuffers, state: LayerStat
                      stream=None):
     _check(_lib.spec_tree_finish(ctypes.byref(_cp(params)), tree.B, V, ctypes.byref(tree.c()), _ptr(state.state),
                                  _ptr(status), _stream(stream)))
+
+
+@dataclasses.dataclass
+class CostFit:
+    lam: float
+    gamma: float
+    delta: float
+    rho: float
+    rms_draft: float
+    rms_verify: float
+
+    def apply(self, params: Params) -> Params:
+        """params with the fitted SMART cost coefficients (beta = eta = 0)."""
+        return dataclasses.replace(params, lam=self.lam, beta=0.0, gamma=self.gamma, delta=self.delta,
+                                   rho=self.rho, eta=0.0)
+
+
+def spec_tree_smart_fit(sizes, t_draft, t_verify, t_base: float, weights=None) -> CostFit:
+    """Fit the SMART cost model to profiled step times (host only, no GPU)."""
+    def arr(x):
+        a = (ctypes.c_double * len(x))(*[float(v) for v in x])
+        return ctypes.cast(a, ctypes.POINTER(ctypes.c_double)), a
+
+    n = len(sizes)
+    if len(t_draft) != n or len(t_verify) != n or (weights is not None and len(weights) != n):
+        raise SpecTreeError("sizes, timings and weights must have the same length")
+    (pn, _an), (pd, _ad), (pv, _av) = arr(sizes), arr(t_draft), arr(t_verify)
+    pw, _aw = arr(weights) if weights is not None else (None, None)
+    coef = (ctypes.c_double * 4)()
+    rms = (ctypes.c_double * 2)()
+    _check(_lib.spec_tree_smart_fit(n, pn, pd, pv, float(t_base), pw, None,
+                                    ctypes.cast(coef, ctypes.POINTER(ctypes.c_double)),
+                                    ctypes.cast(rms, ctypes.POINTER(ctypes.c_double))))
+    return CostFit(lam=coef[0], gamma=coef[1], delta=coef[2], rho=coef[3], rms_draft=rms[0], rms_verify=rms[1])
 
 
 class VerifyOutputs:

@@ -29,6 +29,7 @@ import dataclasses
 import hashlib
 from typing import Optional, Sequence
 
+import numpy as np
 import torch
 
 
@@ -219,3 +220,22 @@ def bf16_bits(x: torch.Tensor):
 def to_numpy_f64(x: torch.Tensor):
     """Exact float64 copy of a bf16/f32 tensor."""
     return x.detach().to("cpu").to(torch.float64).numpy()
+
+
+def profile_timings(seed: int, sizes: Sequence[float], t_base: float = 1.0e-3, draft_per_token: float = 2.0e-5,
+                    slope: float = 2.0e-3, knee: float = 96.0, curvature: float = 6.0e-5, noise: float = 0.02):
+    """Synthetic profiled step times (seconds) of a device, standing in for timed model forward passes.
+
+    A plain target step takes t_base; drafting a tree of n tokens takes about
+    draft_per_token * n; verifying it takes t_base * (1 + slope * n +
+    curvature * max(0, n - knee)^2): nearly flat while the target pass is
+    memory-bound, growing faster past a compute knee.  Each time carries
+    relative Gaussian noise of the given size.  Returns (t_draft, t_verify)
+    as float64 numpy arrays.
+    """
+    rng = np.random.default_rng(_seed_of("profile", seed))
+    n = np.asarray(sizes, dtype=np.float64)
+    t_draft = draft_per_token * n * (1.0 + noise * rng.standard_normal(n.shape))
+    t_verify = t_base * (1.0 + slope * n + curvature * np.maximum(0.0, n - knee) ** 2)
+    t_verify = t_verify * (1.0 + noise * rng.standard_normal(n.shape))
+    return np.maximum(t_draft, 0.0), np.maximum(t_verify, 0.0)

@@ -278,6 +278,30 @@ int spec_tree_layer(const spec_tree_params* p, int B, int V, int layer, int dtyp
 int spec_tree_finish(const spec_tree_params* p, int B, int V, const spec_tree_t* tree,
                      const void* state, uint32_t* status, spec_tree_stream_t stream);
 
+/*
+ * SMART cost-model fit from profiled steps (SMART notes, Key design 2:
+ * device profiling, least squares over a few forward passes, the biases
+ * fixed at zero so that both curves pass through the origin).  Host only, no
+ * CUDA call.
+ *   n[i] > 0:        tree size (tokens) of profiled step i, i < npts, 3 <= npts <= 1024;
+ *   t_draft[i] >= 0: its drafting time;  t_verify[i] >= 0: its verification time;
+ *   t_base > 0:      the time of a plain target step (no tree), same unit;
+ *   w[i] >= 0:       weights (NULL: all 1), e.g. decaying with age for an online refit.
+ * In units of t_base it fits, by weighted least squares,
+ *   lambda * n                      to t_draft / t_base            (beta = 0),
+ *   gamma * (exp(delta * n^rho) - 1) to (t_verify - t_base) / t_base (eta = 0),
+ * lambda and gamma >= 0 in closed form, (delta, rho) by a refined grid search
+ * over rho in [1, 4] and delta * max(n)^rho in [1e-6, 30].
+ *   p (or NULL):    lambda, gamma, delta, rho set, beta = eta = 0, other fields untouched;
+ *   coef (or NULL): double[4] = lambda, gamma, delta, rho;
+ *   rms (or NULL):  double[2] = weighted root-mean-square residual of the draft and of the
+ *                   verification fit, in units of t_base.
+ * Returns SPEC_TREE_E_PARAM for a null input, npts out of range, a non-finite
+ * or negative value, a size <= 0, t_base <= 0 or all weights zero.
+ */
+int spec_tree_smart_fit(int npts, const double* n, const double* t_draft, const double* t_verify,
+                        double t_base, const double* w, spec_tree_params* p, double* coef, double* rms);
+
 /* Message for a return code (static string). */
 const char* spec_tree_strerror(int code);
 

@@ -55,6 +55,21 @@ def test_smart_parity(seed):
     _report("smart", parity.run_parity(wl, seed))
 
 
+def test_smart_parity_with_fitted_costs():
+    """SMART trees whose cost coefficients come from spec_tree_smart_fit on profiled step times."""
+    from dynamic_tree_speculative_gb300 import binding as B
+    sizes = [16, 64, 128, 256, 384]
+    td, tv = WL.profile_timings(7, sizes)
+    f = B.spec_tree_smart_fit(sizes, td, tv, 1.0e-3)
+    wl = WL.WORKLOADS["sweep_smart"].with_(B=8, V=32000, lam=f.lam, beta=0.0, gamma=f.gamma, delta=f.delta,
+                                           rho=f.rho, eta=0.0)
+    out = parity.run_parity(wl, 13)
+    sizes_built = out["gpu"]["n_nodes"] - 1
+    print(f"fitted lam {f.lam:.4g} gamma {f.gamma:.4g} delta {f.delta:.4g} rho {f.rho:.4g}; "
+          f"tree sizes {sizes_built.tolist()}")
+    _report("smart_fitted", out)
+
+
 def test_smart_parity_llama_vocab():
     wl = WL.WORKLOADS["sweep_smart"].with_(B=4)
     _report("smart128k", parity.run_parity(wl, 9))
