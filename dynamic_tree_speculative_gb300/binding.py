@@ -24,7 +24,8 @@ ROOT, DET, PROBE, FILL = 0, 1, 2, 3
 OK, E_PARAM, E_LAYOUT, E_CUDA = 0, -1, -3, -4
 S_NONFINITE_DRAFT, S_NONFINITE_TARGET, S_RESIDUAL_EMPTY = 1, 2, 4
 S_OVERFLOW, S_TIMEOUT, S_ROWS, S_LAYERS = 8, 16, 32, 64
-MAX_SUPPORT = 128
+MAX_SUPPORT = 1024
+DEFAULT_SUPPORT = 128
 
 EXPORTS = ("spec_tree_rows_needed", "spec_tree_check_params", "spec_tree_select_expand", "spec_tree_rank",
            "spec_tree_build", "spec_tree_verify", "spec_tree_layer_state_bytes", "spec_tree_layer_rows",
@@ -139,7 +140,8 @@ class TreeBuffers:
         self.B = B
         self.n_rows = n_rows if n_rows is not None else rows_needed(params)
         self.max_nodes = params.R + 1
-        self.sup_stride = MAX_SUPPORT
+        # support arrays hold |S| = min(support, V) ranks per row; at least 128 wide
+        self.sup_stride = max(DEFAULT_SUPPORT, params.support or DEFAULT_SUPPORT)
         mk = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)  # noqa: E731
         n = (B, self.max_nodes)
         self.node_token, self.node_parent, self.node_depth = mk(n, i32), mk(n, i32), mk(n, i32)

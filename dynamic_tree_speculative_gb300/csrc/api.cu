@@ -61,6 +61,11 @@ int check_tree(const spec_tree_params* p, const spec_tree_t* t, int V, bool need
 
 cudaStream_t as_stream(spec_tree_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// the streaming kernel for supports of up to 128 tokens, else one CTA per row
+cudaError_t launch_select(int dtype, const st::SelLaunch& L, cudaStream_t stream) {
+  return L.S <= 128 ? st::launch_select_expand(dtype, L, stream) : st::launch_select_wide(dtype, L, stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -131,7 +136,7 @@ int spec_tree_select_expand(const spec_tree_params* p, int B, int V, int dtype, 
   L.num_sms = num_sms_of_current_device();
   L.ctas_per_sm = 2;
   if (L.num_sms <= 0) return SPEC_TREE_E_CUDA;
-  return st::launch_select_expand(dtype, L, as_stream(stream)) == cudaSuccess ? SPEC_TREE_OK : SPEC_TREE_E_CUDA;
+  return launch_select(dtype, L, as_stream(stream)) == cudaSuccess ? SPEC_TREE_OK : SPEC_TREE_E_CUDA;
 }
 
 int spec_tree_rank(const spec_tree_params* p, int B, int V, const spec_tree_t* tree, uint32_t* status,
@@ -218,7 +223,7 @@ int spec_tree_layer(const spec_tree_params* p, int B, int V, int layer, int dtyp
   S.num_sms = num_sms_of_current_device();
   S.ctas_per_sm = 2;
   if (S.num_sms <= 0) return SPEC_TREE_E_CUDA;
-  if (st::launch_select_expand(dtype, S, as_stream(stream)) != cudaSuccess) return SPEC_TREE_E_CUDA;
+  if (launch_select(dtype, S, as_stream(stream)) != cudaSuccess) return SPEC_TREE_E_CUDA;
   st::RankLaunch L;
   L.p = *p;
   L.B = B;

@@ -40,10 +40,12 @@
 #include <stdint.h>
 
 #include "st_common.cuh"
+#include "st_keys.cuh"
 #include "st_kernels.h"
 
 namespace st {
 
+constexpr int SX_MAX_S = 128;                    // supports of up to 128 tokens (larger: select_wide.cu)
 constexpr int SX_CONS = 256;                     // streaming consumer threads (8 warps)
 constexpr int SX_CWARPS = SX_CONS / 32;
 constexpr int SX_SEL_WARP = SX_CWARPS;           // warp 8: exact selection + epilogue
@@ -67,7 +69,7 @@ constexpr int SX_SORTED = 2;   // exactly the top-|S|, in order
 // table of chunk maxima, so the two share it.
 struct RobustScratch {
   uint64_t fbuf[SX_FB_CAP];
-  uint64_t sel[SPEC_TREE_MAX_SUPPORT];
+  uint64_t sel[SX_MAX_S];
   uint64_t tie[32];
   uint32_t hist[256];
 };
@@ -80,7 +82,7 @@ struct SelShared {
     RobustScratch rb;
   };
   uint16_t glist[SX_GLIST];  // chunk << 8 | thread
-  alignas(16) uint64_t ssel[SPEC_TREE_MAX_SUPPORT];  // selector's scratch
+  alignas(16) uint64_t ssel[SX_MAX_S];  // selector's scratch
   uint64_t stie[32];                      // selector's ties
   uint32_t khist[2][256];  // per candidate buffer: histogram of candidate keys above hbase
   uint64_t full[SX_STAGES];
@@ -122,48 +124,6 @@ __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(S
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-template <typename T>
-struct Elem;
-template <>
-struct Elem<__nv_bfloat16> {
-  static constexpr int VEC = 8;
-  static constexpr int KEY_BITS = 16;
-  static constexpr int ES = 2;
-};
-template <>
-struct Elem<float> {
-  static constexpr int VEC = 4;
-  static constexpr int KEY_BITS = 32;
-  static constexpr int ES = 4;
-};
-
-// Order key of element j of a 16-byte vector; flags NaN / +inf.
-template <typename T>
-__device__ __forceinline__ uint32_t elem_key(const uint4& v, int j, bool& nonfinite);
-
-template <>
-__device__ __forceinline__ uint32_t elem_key<__nv_bfloat16>(const uint4& v, int j, bool& nonfinite) {
-  const uint32_t w = (j < 2) ? v.x : (j < 4) ? v.y : (j < 6) ? v.z : v.w;
-  const uint32_t bits = (w >> (16 * (j & 1))) & 0xffffu;
-  if ((bits & 0x7fffu) >= 0x7f80u && bits != 0xff80u) nonfinite = true;  // NaN or +inf
-  return bf16_key(bits);
-}
-
-template <>
-__device__ __forceinline__ uint32_t elem_key<float>(const uint4& v, int j, bool& nonfinite) {
-  const uint32_t bits = (j == 0) ? v.x : (j == 1) ? v.y : (j == 2) ? v.z : v.w;
-  if ((bits & 0x7fffffffu) >= 0x7f800000u && bits != 0xff800000u) nonfinite = true;
-  return f32_key(bits);
-}
-
-template <typename T>
-__device__ __forceinline__ uint32_t scalar_key(const uint8_t* row, int v, bool& nonfinite) {
-  uint4 x = make_uint4(0, 0, 0, 0);
-  if (sizeof(T) == 2) x.x = reinterpret_cast<const uint16_t*>(row)[v];
-  else x.x = reinterpret_cast<const uint32_t*>(row)[v];
-  return elem_key<T>(x, 0, nonfinite);
 }
 
 // Running maximum of pass 1, as an order key (0 when the thread saw nothing).
@@ -241,17 +201,6 @@ struct RunMax<float> {
     return k;
   }
 };
-
-template <typename T>
-__device__ __forceinline__ float key_value(uint32_t key);
-template <>
-__device__ __forceinline__ float key_value<__nv_bfloat16>(uint32_t key) { return bf16_key_value(key); }
-template <>
-__device__ __forceinline__ float key_value<float>(uint32_t key) { return __uint_as_float(f32_from_key(key)); }
-
-__device__ __forceinline__ uint64_t make_comp(uint32_t key, uint32_t id) {
-  return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~id);
-}
 
 // Warp-aggregated append of the elements selected by `mask` (bit j: key
 // keys[j], id id0 + j).  All 32 lanes of the warp call it.
@@ -489,7 +438,7 @@ __device__ void select_topk(SelShared& s, CandBuf cb, int n, int k) {
       const uint64_t m = c & pmask;
       if (tie_mode ? m > prefix : m >= prefix) {
         const int pos = atomicAdd(&s.sel_count, 1);
-        if (pos < SPEC_TREE_MAX_SUPPORT) s.rb.sel[pos] = c;
+        if (pos < SX_MAX_S) s.rb.sel[pos] = c;
       } else if (tie_mode && m == prefix) {
         const int pos = atomicAdd(&s.tie_count, 1);
         if (pos < 32) s.rb.tie[pos] = c;
@@ -503,7 +452,7 @@ __device__ void select_topk(SelShared& s, CandBuf cb, int n, int k) {
       for (int j = 0; j < nt; ++j) r += s.rb.tie[j] > c;
       if (lane < nt && r < need) {
         const int pos = atomicAdd(&s.sel_count, 1);
-        if (pos < SPEC_TREE_MAX_SUPPORT) s.rb.sel[pos] = c;
+        if (pos < SX_MAX_S) s.rb.sel[pos] = c;
       }
     }
     csync();

@@ -1,0 +1,554 @@
+// Support selection + dual-identity expansion for supports of 129 to 1024
+// tokens (sm_103a): one CTA of 1024 threads per draft row.
+//
+// RheoSampling notes, Method / Key design 1 (the support-size ablation:
+// top-128, 256, 512, 1024, and the dense support when it is the whole
+// vocabulary) and Key design 2 (softmaxes over the support, tail masses, the
+// probe by inverse CDF over the tempered tail in rank order).
+//
+//   select: an exact radix select on the elements' order keys, one 8-bit
+//     digit at a time from the top (two passes over the row for bf16, at most
+//     four for f32), each pass counting the elements that match the digits
+//     fixed so far into per-warp histograms.  It ends with the |S|-th largest
+//     key t and the number of elements equal to t still needed.
+//   collect: one more pass, in rounds of 1024 consecutive vectors (token-id
+//     order), appends every element above t and, of the elements equal to t,
+//     the smallest ids (a block scan ranks them within the round): exactly
+//     |S| (key, ~id) composites.
+//   sort: a bitonic sort in shared memory, descending, so rank r is thread r.
+//   epilogue: q, q_T, z, z_T by block reductions and the probe by a block
+//     scan of the tempered tail weights in rank order.
+//
+// The rows are read from global memory (the first pass from HBM, the others
+// mostly from L2); the streaming kernel for supports of up to 128 tokens is
+// the fast path.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "st_common.cuh"
+#include "st_keys.cuh"
+#include "st_kernels.h"
+
+namespace st {
+
+constexpr int SW_THREADS = 1024;
+constexpr int SW_WARPS = SW_THREADS / 32;
+constexpr int SW_MAX_S = SPEC_TREE_MAX_SUPPORT;
+constexpr int SW_TBL = 32768;  // table path: rows of up to 32768 vectors (256K bf16 / 128K f32 tokens)
+constexpr int SW_CAP = 2048;   // table path: candidates
+
+struct WideShared {
+  union {
+    uint16_t tbl[SW_TBL];           // table path: 16-bit order key of each vector's maximum
+    uint32_t whist[SW_WARPS][256];  // radix path: per-warp digit histograms
+  };
+  uint64_t cand[SW_CAP];            // candidates; at the end the top-|S| in rank order
+  uint32_t list[SW_CAP];            // table path: vectors to gather
+  uint32_t sample[SW_THREADS];      // table path: a sorted sample of the table
+  uint32_t hist[256];
+  float red[4][SW_WARPS];         // block reductions
+  float scan[SW_WARPS];           // block scan of the tail weights
+  int tie_scan[SW_WARPS];         // block scan of tie counts
+  int n_cand;
+  int n_list;
+  int count;
+  int bin;
+  int above;
+  int cnt;
+  int probe;
+  int last_pos;
+};
+
+// Calls f(key, id) for every element of the row that thread tid owns: the
+// 16-byte vectors tid, tid + 1024, ... (loaded eight at a time, so that eight
+// loads are in flight) and then the scalar tail element nvec * VEC + tid, if
+// any.
+template <typename T, typename F>
+__device__ __forceinline__ void for_each_elem(const uint8_t* row, int V, int nvec, bool& nonfinite, F f) {
+  using E = Elem<T>;
+  constexpr int VEC = E::VEC, U = 8;
+  const int tid = threadIdx.x;
+  for (int v0 = tid; v0 < nvec; v0 += U * SW_THREADS) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int vi = v0 + u * SW_THREADS;
+      if (vi < nvec) v[u] = ldg_stream(row + static_cast<int64_t>(vi) * 16);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int vi = v0 + u * SW_THREADS;
+      if (vi < nvec)
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) f(elem_key<T>(v[u], j, nonfinite), static_cast<uint32_t>(vi * VEC + j));
+    }
+  }
+  const int id = nvec * VEC + tid;
+  if (id < V) f(scalar_key<T>(row, id, nonfinite), static_cast<uint32_t>(id));
+}
+
+// Radix select of the k-th largest key of the row (k >= 1): returns the
+// digits fixed (prefix under pmask) and how many elements matching them are
+// still needed; *exact is set when every element matching the prefix is in
+// (the count of the last bin equalled the need).
+template <typename T>
+__device__ void radix_select_row(WideShared& s, const uint8_t* row, int V, int nvec, int k, bool& nonfinite,
+                                 uint32_t& prefix, uint32_t& pmask, int& need, bool& exact) {
+  constexpr int KEY_BITS = Elem<T>::KEY_BITS;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  prefix = 0u;
+  pmask = 0u;
+  need = k;
+  exact = false;
+  for (int d = 0; d < KEY_BITS / 8; ++d) {
+    const int shift = KEY_BITS - 8 * (d + 1);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) (&s.whist[0][0])[tid * 8 + i] = 0u;
+    __syncthreads();
+    uint32_t* wh = s.whist[warp];
+    const uint32_t pf = prefix, pm = pmask;
+    for_each_elem<T>(row, V, nvec, nonfinite, [&](uint32_t key, uint32_t) {
+      if ((key & pm) == pf) atomicAdd(&wh[(key >> shift) & 0xffu], 1u);
+    });
+    __syncthreads();
+    if (tid < 256) {
+      uint32_t c = 0;
+#pragma unroll 8
+      for (int w = 0; w < SW_WARPS; ++w) c += s.whist[w][tid];
+      s.hist[tid] = c;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // bins from the top: lane l holds bins 255 - 8l - j
+      uint32_t h[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        h[j] = s.hist[255 - 8 * lane - j];
+        tot += h[j];
+      }
+      uint32_t incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t excl = incl - tot, nd = static_cast<uint32_t>(need);
+      if (excl < nd && nd <= incl) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (acc < nd && nd <= acc + h[j]) {
+            s.bin = 255 - 8 * lane - j;
+            s.above = static_cast<int>(acc);
+            s.cnt = static_cast<int>(h[j]);
+          }
+          acc += h[j];
+        }
+      }
+    }
+    __syncthreads();
+    need -= s.above;
+    prefix |= static_cast<uint32_t>(s.bin) << shift;
+    pmask |= 0xffu << shift;
+    const bool done = s.cnt == need;
+    __syncthreads();  // every thread has read bin, above, cnt
+    if (done) {
+      exact = true;
+      return;
+    }
+  }
+}
+
+// Exclusive block scan of one int per thread; returns the prefix and writes
+// the block total to *total.  All threads call it.
+__device__ __forceinline__ int block_excl_scan(WideShared& s, int x, int* total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s.tie_scan[warp] = incl;
+  __syncthreads();
+  int before = 0, tot = 0;
+  for (int w = 0; w < SW_WARPS; ++w) {
+    const int c = s.tie_scan[w];
+    if (w < warp) before += c;
+    tot += c;
+  }
+  __syncthreads();  // tie_scan may be reused
+  *total = tot;
+  return before + incl - x;
+}
+
+// Appends to s.cand every element above the prefix and, unless exact, the
+// `need` smallest ids among the elements equal to it (exact: every element
+// equal to it).  Rounds of 1024 consecutive vectors keep id order for ties.
+template <typename T>
+__device__ void collect_row(WideShared& s, const uint8_t* row, int V, int nvec, uint32_t prefix, uint32_t pmask,
+                            int need, bool exact, bool& nonfinite) {
+  using E = Elem<T>;
+  constexpr int VEC = E::VEC;
+  const int tid = threadIdx.x;
+  if (tid == 0) s.n_cand = 0;
+  __syncthreads();
+  auto push = [&](uint32_t key, uint32_t id) {
+    const int pos = atomicAdd(&s.n_cand, 1);
+    if (pos < SW_MAX_S) s.cand[pos] = make_comp(key, id);
+  };
+  if (exact) {
+    for_each_elem<T>(row, V, nvec, nonfinite, [&](uint32_t key, uint32_t id) {
+      if ((key & pmask) >= prefix) push(key, id);
+    });
+    __syncthreads();
+    return;
+  }
+  // ties: key == prefix (every digit fixed); ranked in id order round by round
+  int taken = 0;  // ties taken in earlier rounds (block-uniform)
+  const int rounds = (nvec + SW_THREADS - 1) / SW_THREADS + 1;  // the last round: the scalar tail
+  for (int r = 0; r < rounds; ++r) {
+    uint32_t keys[VEC];
+    uint32_t id0;
+    int nel = 0;
+    if (r + 1 < rounds) {
+      const int vi = r * SW_THREADS + tid;
+      id0 = static_cast<uint32_t>(vi * VEC);
+      if (vi < nvec) {
+        const uint4 v = ldg_stream(row + static_cast<int64_t>(vi) * 16);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) keys[j] = elem_key<T>(v, j, nonfinite);
+        nel = VEC;
+      }
+    } else {
+      const int id = nvec * VEC + tid;
+      id0 = static_cast<uint32_t>(id);
+      if (id < V) {
+        keys[0] = scalar_key<T>(row, id, nonfinite);
+        nel = 1;
+      }
+    }
+    int ties = 0;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j)
+      if (j < nel) {
+        if (keys[j] > prefix) push(keys[j], id0 + j);
+        else if (keys[j] == prefix) ++ties;
+      }
+    int total;
+    int rank = block_excl_scan(s, ties, &total) + taken;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j)
+      if (j < nel && keys[j] == prefix) {
+        if (rank < need) push(keys[j], id0 + j);
+        ++rank;
+      }
+    taken += total;
+    if (taken >= need) {
+      // every tie needed is in; the rest of the row is only above-t elements
+      for (int r2 = r + 1; r2 + 1 < rounds; ++r2) {
+        const int vi = r2 * SW_THREADS + tid;
+        if (vi < nvec) {
+          const uint4 v = ldg_stream(row + static_cast<int64_t>(vi) * 16);
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) {
+            const uint32_t key = elem_key<T>(v, j, nonfinite);
+            if (key > prefix) push(key, static_cast<uint32_t>(vi * VEC + j));
+          }
+        }
+      }
+      if (r + 1 < rounds) {
+        const int id = nvec * VEC + tid;
+        if (id < V) {
+          const uint32_t key = scalar_key<T>(row, id, nonfinite);
+          if (key > prefix) push(key, static_cast<uint32_t>(id));
+        }
+      }
+      break;
+    }
+  }
+  __syncthreads();
+}
+
+// Bitonic sort of s.cand[0..n) descending, padded with 0 (below every
+// composite) to the next power of two P <= SW_CAP.
+__device__ void sort_cand_desc(WideShared& s, int n) {
+  const int tid = threadIdx.x;
+  int P = 1;
+  while (P < n) P <<= 1;
+  for (int i = n + tid; i < P; i += SW_THREADS) s.cand[i] = 0ull;
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      for (int i = tid; i < P / 2; i += SW_THREADS) {
+        const int pos = 2 * i - (i & (stride - 1));
+        const uint64_t a = s.cand[pos], b = s.cand[pos + stride];
+        const bool desc = (pos & size) == 0;
+        if ((a < b) == desc) {
+          s.cand[pos] = b;
+          s.cand[pos + stride] = a;
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Bitonic sort of a[0..P) descending (P a power of two <= 2048).
+__device__ void sort_u32_desc(uint32_t* a, int P) {
+  const int tid = threadIdx.x;
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      for (int i = tid; i < P / 2; i += SW_THREADS) {
+        const int pos = 2 * i - (i & (stride - 1));
+        const uint32_t x = a[pos], y = a[pos + stride];
+        const bool desc = (pos & size) == 0;
+        if ((x < y) == desc) {
+          a[pos] = y;
+          a[pos + stride] = x;
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// 16-bit order key of the maximum of one 16-byte vector, for the table:
+// bf16: its key (0xffff, so that the vector is examined, when a NaN is among
+// the elements); f32: the upper 16 bits of the largest element key, which
+// order the same way and only ever let more vectors through.
+template <typename T>
+__device__ __forceinline__ uint32_t vec_max_key16(const uint4& v, bool& nan);
+
+template <>
+__device__ __forceinline__ uint32_t vec_max_key16<__nv_bfloat16>(const uint4& v, bool& nan) {
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
+  const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
+  const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&v.w);
+  __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+  m = __hmax2_nan(m, __lowhigh2highlow(m));
+  const uint32_t bits = __bfloat16_as_ushort(m.x);
+  if ((bits & 0x7fffu) > 0x7f80u) {
+    nan = true;
+    return 0xffffu;
+  }
+  return bf16_key(bits);
+}
+
+template <>
+__device__ __forceinline__ uint32_t vec_max_key16<float>(const uint4& v, bool& nan) {
+  uint32_t k = 0u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) k = max(k, elem_key<float>(v, j, nan));
+  return k >> 16;
+}
+
+// Table path: one pass stores every vector's maximum key; the bound is a rank
+// of a sorted sample of the table expected to leave about 1.5 |S| entries at
+// or above it, accepted once an exact count shows between |S| and SW_CAP
+// entries there (each entry is a distinct element, so at least |S| elements
+// reach the bound); the listed vectors are re-read and every element that
+// reaches the bound becomes a candidate; the candidates are sorted, so the
+// first |S| are the top-|S|.  Returns false (nothing decided) when no sample
+// rank passes the count, or the candidates are too few (NaN) or too many
+// (ties); block-uniform.
+template <typename T>
+__device__ bool table_select(WideShared& s, const uint8_t* row, int V, int nvec, int S, bool& nonfinite) {
+  constexpr int VEC = Elem<T>::VEC, U = 8;
+  const int tid = threadIdx.x;
+  for (int v0 = tid; v0 < nvec; v0 += U * SW_THREADS) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int vi = v0 + u * SW_THREADS;
+      if (vi < nvec) v[u] = ldg_stream(row + static_cast<int64_t>(vi) * 16);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int vi = v0 + u * SW_THREADS;
+      if (vi < nvec) s.tbl[vi] = static_cast<uint16_t>(vec_max_key16<T>(v[u], nonfinite));
+    }
+  }
+  __syncthreads();
+  s.sample[tid] = s.tbl[static_cast<int64_t>(tid) * nvec / SW_THREADS];
+  sort_u32_desc(s.sample, SW_THREADS);
+  int r = static_cast<int>(ceilf(1.5f * S * SW_THREADS / nvec)) - 1;
+  r = r < 0 ? 0 : (r > SW_THREADS - 1 ? SW_THREADS - 1 : r);
+  uint32_t b16 = 0u;
+  bool ok = false;
+  for (int attempt = 0; attempt < 4 && !ok; ++attempt) {
+    b16 = s.sample[r];
+    int c = 0;
+    for (int vi = tid; vi < nvec; vi += SW_THREADS) c += s.tbl[vi] >= b16;
+    int total;
+    block_excl_scan(s, c, &total);
+    if (total >= S && total <= SW_CAP) ok = true;
+    else r = total < S ? min(SW_THREADS - 1, 2 * r + 1) : r / 2;
+  }
+  if (!ok) return false;
+  const uint32_t bound = sizeof(T) == 2 ? b16 : (b16 << 16);
+  if (tid == 0) {
+    s.n_list = 0;
+    s.n_cand = 0;
+  }
+  __syncthreads();
+  for (int vi = tid; vi < nvec; vi += SW_THREADS)
+    if (s.tbl[vi] >= b16) {
+      const int pos = atomicAdd(&s.n_list, 1);
+      if (pos < SW_CAP) s.list[pos] = static_cast<uint32_t>(vi);
+    }
+  __syncthreads();
+  const int nl = min(s.n_list, SW_CAP);
+  auto push = [&](uint32_t key, uint32_t id) {
+    const int pos = atomicAdd(&s.n_cand, 1);
+    if (pos < SW_CAP) s.cand[pos] = make_comp(key, id);
+  };
+  // the listed vectors, two per thread with both loads in flight
+  for (int i0 = 0; i0 < nl; i0 += 2 * SW_THREADS) {
+    uint4 v[2];
+    int vi[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int i = i0 + u * SW_THREADS + tid;
+      vi[u] = i < nl ? static_cast<int>(s.list[i]) : -1;
+      if (vi[u] >= 0) v[u] = ldg_stream(row + static_cast<int64_t>(vi[u]) * 16);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (vi[u] >= 0)
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+          const uint32_t key = elem_key<T>(v[u], j, nonfinite);
+          if (key >= bound) push(key, static_cast<uint32_t>(vi[u] * VEC + j));
+        }
+  }
+  const int id = nvec * VEC + tid;  // elements past the last whole vector
+  if (id < V) {
+    const uint32_t key = scalar_key<T>(row, id, nonfinite);
+    if (key >= bound) push(key, static_cast<uint32_t>(id));
+  }
+  __syncthreads();
+  const int n = s.n_cand;
+  if (n < S || n > SW_CAP) return false;
+  sort_cand_desc(s, n);
+  return true;
+}
+
+// Softmaxes, tail masses and the probe of a row from its sorted support
+// s.cand[0..n): thread r owns support rank r.  RheoSampling Key design 2; the
+// probe is the first tail rank k with u * z_T < sum_{j=m..k} q_T(j), on
+// unnormalised weights (the last tail rank with weight if rounding leaves
+// none).
+template <typename T>
+__device__ void wide_epilogue(WideShared& s, const SelLaunch& a, int64_t out_row, int64_t in_row, int n) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool valid = tid < n;
+  const uint64_t x = valid ? s.cand[tid] : 0ull;
+  const float lmax = key_value<T>(static_cast<uint32_t>(s.cand[0] >> 32));
+  if (tid == 0 && !(lmax < INFINITY)) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
+  const float l = key_value<T>(static_cast<uint32_t>(x >> 32));
+  const float dd = l - lmax;
+  const float e = valid ? expf(dd) : 0.0f;
+  const float eT = valid ? expf(dd / a.temperature) : 0.0f;
+  const bool tail = valid && tid >= a.m;
+  float v4[4] = {e, eT, tail ? e : 0.0f, tail ? eT : 0.0f};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    v4[k] = warp_sum(v4[k]);
+    if (lane == 0) s.red[k][warp] = v4[k];
+  }
+  if (tid == 0) {
+    s.probe = 0x7fffffff;
+    s.last_pos = -1;
+  }
+  __syncthreads();
+  float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int w = 0; w < SW_WARPS; ++w)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sum[k] += s.red[k][w];
+  const float se = sum[0], seT = sum[1], te = sum[2], teT = sum[3];
+  if (valid) {
+    a.sup_id[out_row * a.sup_stride + tid] = static_cast<int32_t>(~static_cast<uint32_t>(x));
+    a.sup_q[out_row * a.sup_stride + tid] = e / se;
+    a.sup_qT[out_row * a.sup_stride + tid] = eT / seT;
+  }
+  const bool draw = a.draw_probe && a.m < n && teT > 0.0f;  // block-uniform
+  if (draw) {
+    // inclusive scan of the tail weights in rank order
+    const float w = tail ? eT : 0.0f;
+    float incl = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s.scan[warp] = incl;
+    __syncthreads();
+    float before = 0.0f;
+    for (int k = 0; k < warp; ++k) before += s.scan[k];
+    const float target = a.u_probe[in_row] * teT;
+    if (tail && target < before + incl) atomicMin(&s.probe, tid);
+    if (tail && w > 0.0f) atomicMax(&s.last_pos, tid);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int probe = -1;
+    if (draw) probe = s.probe != 0x7fffffff ? s.probe : s.last_pos;
+    a.sup_z[out_row] = te / se;
+    a.sup_zT[out_row] = teT / seT;
+    a.probe_pos[out_row] = probe;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(SW_THREADS) select_wide_kernel(SelLaunch a, int64_t row_bytes) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  WideShared& s = *reinterpret_cast<WideShared*>(smem_raw);
+  const int64_t g = blockIdx.x;
+  const int64_t b = g / a.rows_used, e = g % a.rows_used;
+  const int64_t out_row = b * a.n_rows + a.sup_row0 + e;
+  const int64_t in_row = b * a.in_rows + e;
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const uint8_t* row = static_cast<const uint8_t*>(a.logits) + in_row * row_bytes;
+  const int nvec = static_cast<int>((static_cast<int64_t>(a.V) * Elem<T>::ES) / 16);
+  bool nonfinite = false;
+  // rows of 2048 to SW_TBL vectors: the table path; otherwise, or when it
+  // declines, the exact radix select
+  bool done = nvec >= 2 * SW_THREADS && nvec <= SW_TBL && table_select<T>(s, row, a.V, nvec, a.S, nonfinite);
+  if (!done) {
+    __syncthreads();  // the table shares its storage with the radix histograms
+    uint32_t prefix, pmask;
+    int need;
+    bool exact;
+    radix_select_row<T>(s, row, a.V, nvec, a.S, nonfinite, prefix, pmask, need, exact);
+    collect_row<T>(s, row, a.V, nvec, prefix, pmask, need, exact, nonfinite);
+    sort_cand_desc(s, min(s.n_cand, a.S));
+  }
+  const int n = min(s.n_cand, a.S);
+  wide_epilogue<T>(s, a, out_row, in_row, n);
+  if (nonfinite) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
+}
+
+cudaError_t launch_select_wide(int dtype, const SelLaunch& L, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(L.B) * L.rows_used;
+  if (rows == 0) return cudaSuccess;
+  const int smem = static_cast<int>(sizeof(WideShared));
+  if (dtype == SPEC_TREE_BF16) {
+    cudaError_t err = cudaFuncSetAttribute(select_wide_kernel<__nv_bfloat16>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(select_wide_kernel<__nv_bfloat16>, dim3(static_cast<unsigned>(rows)), dim3(SW_THREADS),
+                      static_cast<size_t>(smem), stream, L, L.row_stride * static_cast<int64_t>(2));
+  }
+  cudaError_t err = cudaFuncSetAttribute(select_wide_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(select_wide_kernel<float>, dim3(static_cast<unsigned>(rows)), dim3(SW_THREADS),
+                    static_cast<size_t>(smem), stream, L, L.row_stride * static_cast<int64_t>(4));
+}
+
+}  // namespace st

@@ -63,6 +63,8 @@ struct VerifyLaunch {
 
 size_t select_expand_smem_bytes();
 cudaError_t launch_select_expand(int dtype, const SelLaunch& L, cudaStream_t stream);
+// supports of 129 to 1024 tokens
+cudaError_t launch_select_wide(int dtype, const SelLaunch& L, cudaStream_t stream);
 cudaError_t launch_rank_topr(const RankLaunch& L, cudaStream_t stream);
 cudaError_t launch_rank_smart(const RankLaunch& L, cudaStream_t stream);
 size_t layer_state_bytes();

@@ -84,7 +84,7 @@ typedef struct CUstream_st* spec_tree_stream_t;
 #define SPEC_TREE_S_LAYERS 64u           /* layer mode: a call out of order, or finish before the last layer */
 
 /* Limits of this build. */
-#define SPEC_TREE_MAX_SUPPORT 128
+#define SPEC_TREE_MAX_SUPPORT 1024
 #define SPEC_TREE_MAX_CAND 2048 /* K + (depth-1)*W*K for the top-R builder; K*R for SMART */
 #define SPEC_TREE_MAX_NODES 512 /* R + 1 */
 
@@ -98,7 +98,9 @@ typedef struct CUstream_st* spec_tree_stream_t;
  *   depth    D >= 1: layers of draft nodes.
  *   R        pruned tree size in draft nodes, root excluded (top-R builder);
  *            node budget (SMART).  Node arrays hold R + 1 entries.
- *   support  |S| = min(support, V); 0 means 128.  1 <= support <= 128.
+ *   support  |S| = min(support, V); 0 means 128.  1 <= support <= 1024 (the
+ *            pages' ablation: 128, 256, 512, 1024; support >= V is the dense
+ *            support of a vocabulary of at most 1024 tokens).
  *   temperature T > 0: probe sampling and verification use q_T and
  *            p = softmax(t / T); ranking uses untempered q.
  *   builder  SPEC_TREE_BUILDER_TOPR or SPEC_TREE_BUILDER_SMART.

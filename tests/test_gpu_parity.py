@@ -96,6 +96,21 @@ EDGE = {
     "rrsw": dict(V=3000, K=4, m=1, W=4, depth=4, R=16, verify_order="rrsw"),
     "rrsw_no_fillers": dict(V=3000, K=2, m=1, W=2, depth=5, R=14, verify_order="rrsw"),
     "rrsw_m0": dict(V=3000, K=3, m=0, W=3, depth=4, R=14, verify_order="rrsw"),
+    # the pages' support-size ablation (one CTA per row past 128 tokens)
+    "support_256": dict(V=32000, K=8, m=1, W=4, depth=4, R=20, support=256),
+    "support_512": dict(V=32000, K=8, m=1, W=4, depth=4, R=20, support=512),
+    "support_1024": dict(V=32000, K=8, m=1, W=4, depth=4, R=20, support=1024),
+    "support_1024_m0": dict(V=9000, K=4, m=0, W=4, depth=4, R=16, support=1024),
+    "support_1024_rrsw": dict(V=9000, K=2, m=1, W=2, depth=5, R=14, support=1024, verify_order="rrsw"),
+    "support_1024_f32": dict(V=5003, K=6, m=1, W=3, depth=3, R=10, dtype="f32", stride=5004, support=1024),
+    "support_300_ragged": dict(V=4097, K=6, m=2, W=3, depth=3, R=12, stride=4104, support=300),
+    # support >= V: the dense support of a small vocabulary
+    "dense_small_vocab": dict(V=700, K=8, m=1, W=4, depth=4, R=20, stride=704, support=1024),
+    # the cold limit: m = 0 reduces to Top-K (its tail starts at the top token, so
+    # its tempered weight never underflows); m = 1 keeps its proxy, at a temperature
+    # above the float32 underflow of exp((l_2 - l_1) / T) for these rows
+    "cold_m0": dict(V=3000, K=4, m=0, W=4, depth=4, R=16, temperature=0.02),
+    "cold_m1": dict(V=3000, K=4, m=1, W=4, depth=4, R=16, temperature=0.1),
 }
 
 
@@ -106,6 +121,23 @@ def test_edge_cases(name):
     base = WL.WORKLOADS["vicuna"].with_(B=16)
     wl = base.with_(**kw)
     _report(name, parity.run_parity(wl, 11, row_stride=stride))
+
+
+def test_wide_support_llama_vocab():
+    """Support 1024 at the LLaMA-3 vocabulary (V = 128256), every tree of a small batch."""
+    wl = WL.WORKLOADS["llama3"].with_(B=4, support=1024)
+    _report("llama3_support1024", parity.run_parity(wl, 17))
+
+
+def test_heavy_ties_wide_support():
+    """Integer-valued bf16 logits with support 512: ties at the |S|-th key take the smallest ids."""
+    wl = WL.WORKLOADS["vicuna"].with_(B=4, V=20000, depth=3, R=12, K=6, W=3, support=512)
+    n_rows = 1 + (wl.depth - 1) * wl.W
+    g = torch.Generator().manual_seed(6)
+    draft = torch.randint(-6, 3, (wl.B, n_rows, wl.V), generator=g).to(torch.bfloat16)
+    draft[1] = 0.25
+    ex, exm = _parity_on_draft(wl, draft)
+    assert ex + exm == wl.B
 
 
 def _parity_on_draft(wl, draft, seed=0):

@@ -594,3 +594,62 @@ def test_topr_frontiers_are_the_expanded_nodes():
         assert prank == (-1 if d == 1 else int(t.exp_row[par]) - (1 + (d - 2) * p.W))
         seen += 1
     assert seen == sum(sizes)
+
+
+def _separated_rows(seed, n_rows, V=40, gap=0.6):
+    """Rows whose sorted logits are gap apart (a random permutation of 0, gap, 2 gap, ...)."""
+    rng = np.random.default_rng(seed)
+    return np.stack([rng.permutation(V).astype(np.float64) * gap for _ in range(n_rows)])
+
+
+def _tree_sig(t):
+    return t.token.tolist(), t.parent.tolist(), t.depth.tolist()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_cold_limit_m0_is_the_topk_tree(seed):
+    """T -> 0 with m = 0: the probe is always the top token (the tempered tail
+    collapses on rank 0), so sampling and structure both reduce to Top-K."""
+    kw = dict(K=4, W=3, depth=3, R=10)
+    n_rows = 1 + (kw["depth"] - 1) * kw["W"]
+    rows = _separated_rows(seed, n_rows)
+    topk = O.build_topr(rows, np.full(n_rows, 0.5), O.Params(m=4, temperature=0.02, **kw))
+    for u in (0.0, 0.37, 0.999):
+        t = O.build_topr(rows, np.full(n_rows, u), O.Params(m=0, temperature=0.02, **kw))
+        for ex in t.expansions.values():
+            assert ex.probe_pos == 0
+        assert _tree_sig(t) == _tree_sig(topk)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_cold_limit_m1_keeps_a_proxy_difference(seed):
+    """T -> 0 with m = 1: the probe is always the second token, so the children are
+    Top-K's tokens, but the probe carries min(q(x_1), z) instead of q(x_2): the
+    small structural difference from Top-K that the pages describe."""
+    kw = dict(K=4, W=3, depth=3, R=10)
+    n_rows = 1 + (kw["depth"] - 1) * kw["W"]
+    rows = _separated_rows(seed, n_rows)
+    p = O.Params(m=1, temperature=0.02, **kw)
+    t = O.build_topr(rows, np.full(n_rows, 0.5), p)
+    for e, ex in t.expansions.items():
+        assert ex.probe_pos == 1
+        order = np.argsort(-rows[e], kind="stable")
+        assert [tok for _, _, _, tok, _ in ex.children] == order[:kw["K"]].tolist()
+        lp_probe = [lp for _, kind, _, _, lp in ex.children if kind == O.PROBE][0]
+        assert lp_probe == pytest.approx(min(ex.q[0], ex.z), rel=1e-15)
+        assert lp_probe > ex.q[1]
+
+
+def test_cold_limit_underflow_draws_no_probe():
+    """Reading: once the tempered tail weight underflows (T = 1e-4 with gaps of
+    0.6), there is no tail mass to sample, no probe is drawn, and m = 1 builds
+    exactly the Top-K tree."""
+    kw = dict(K=4, W=3, depth=3, R=10)
+    n_rows = 1 + (kw["depth"] - 1) * kw["W"]
+    rows = _separated_rows(9, n_rows)
+    t1 = O.build_topr(rows, np.full(n_rows, 0.5), O.Params(m=1, temperature=1e-4, **kw))
+    tk = O.build_topr(rows, np.full(n_rows, 0.5), O.Params(m=4, temperature=1e-4, **kw))
+    for ex in t1.expansions.values():
+        assert ex.zT == 0.0 and ex.probe_pos == -1
+    assert _tree_sig(t1) == _tree_sig(tk)
+    assert np.array_equal(t1.score, tk.score)
