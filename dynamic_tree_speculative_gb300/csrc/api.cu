@@ -26,8 +26,11 @@ int num_sms_of_current_device() {
   return cache[dev];
 }
 
+// |S| = min(support, V); support 0 selects the pages' default of 128 tokens
+constexpr int DEFAULT_SUPPORT = 128;
+
 int support_size(const spec_tree_params* p, int V) {
-  const int s = p->support == 0 ? SPEC_TREE_MAX_SUPPORT : p->support;
+  const int s = p->support == 0 ? DEFAULT_SUPPORT : p->support;
   return s < V ? s : V;
 }
 

@@ -50,6 +50,9 @@ def test_rows_needed(binding):
     (dict(K=8, m=1, W=8, depth=8, R=60, support=129), 1000, True),    # wide supports: 129 .. 1024
     (dict(K=8, m=1, W=8, depth=8, R=60, support=1024), 128256, True),
     (dict(K=8, m=1, W=8, depth=8, R=60, support=1025), 128256, False),
+    (dict(K=128, m=1, W=1, depth=2, R=8, support=0), 128256, True),   # support 0 means 128 ...
+    (dict(K=129, m=1, W=1, depth=2, R=8, support=0), 128256, False),  # ... so K = 129 > |S|
+    (dict(K=100, m=1, W=1, depth=2, R=8, support=0), 100, True),      # |S| = min(128, V)
     (dict(K=16, m=1, W=16, depth=9, R=60), 1000, False),    # candidates > 2048
     (dict(K=8, m=1, W=8, depth=8, R=600), 1000, False),     # R + 1 > 512
     (dict(K=2, m=0, W=1, depth=1, R=1), 2, True),
