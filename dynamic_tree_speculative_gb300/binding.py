@@ -25,11 +25,13 @@ OK, E_PARAM, E_LAYOUT, E_CUDA = 0, -1, -3, -4
 S_NONFINITE_DRAFT, S_NONFINITE_TARGET, S_RESIDUAL_EMPTY = 1, 2, 4
 S_OVERFLOW, S_TIMEOUT, S_ROWS, S_LAYERS = 8, 16, 32, 64
 MAX_SUPPORT = 1024
+STATIC_MAX_TREES = 64
 DEFAULT_SUPPORT = 128
 
 EXPORTS = ("spec_tree_rows_needed", "spec_tree_check_params", "spec_tree_select_expand", "spec_tree_rank",
            "spec_tree_build", "spec_tree_verify", "spec_tree_layer_state_bytes", "spec_tree_layer_rows",
-           "spec_tree_layer", "spec_tree_finish", "spec_tree_smart_fit", "spec_tree_strerror")
+           "spec_tree_layer", "spec_tree_finish", "spec_tree_layer_static", "spec_tree_smart_fit",
+           "spec_tree_strerror")
 
 
 class SpecTreeError(RuntimeError):
@@ -67,6 +69,7 @@ def _load():
     lib.spec_tree_layer_rows.argtypes = [P, i32]
     lib.spec_tree_layer.argtypes = [P, i32, i32, i32, i32, vp, i64, vp, T, vp, vp, vp, vp, vp]
     lib.spec_tree_finish.argtypes = [P, i32, i32, T, vp, vp, vp]
+    lib.spec_tree_layer_static.argtypes = [P, i32, i32, i32, i32, vp, i64, vp, T, vp, vp, vp, vp]
     dp = ctypes.POINTER(ctypes.c_double)
     lib.spec_tree_smart_fit.argtypes = [i32, dp, dp, dp, ctypes.c_double, dp, P, dp, dp]
     lib.spec_tree_strerror.argtypes = [i32]
@@ -246,6 +249,19 @@ def spec_tree_finish(params: Params, V: int, tree: TreeBuffers, state: LayerStat
                      stream=None):
     _check(_lib.spec_tree_finish(ctypes.byref(_cp(params)), tree.B, V, ctypes.byref(tree.c()), _ptr(state.state),
                                  _ptr(status), _stream(stream)))
+
+
+def spec_tree_layer_static(params: Params, V: int, layer: int, layer_draft: torch.Tensor, u_probe: torch.Tensor,
+                           tree: TreeBuffers, frontier_token: Optional[torch.Tensor],
+                           frontier_parent: Optional[torch.Tensor], status: torch.Tensor, stream=None):
+    """spec_tree_layer with the builder's state inside the library (no state buffer to allocate); the
+    last layer's call also writes the node arrays.  At most STATIC_MAX_TREES trees; builds must not
+    overlap on the GPU."""
+    rows = spec_tree_layer_rows(params, layer)
+    _check(_lib.spec_tree_layer_static(ctypes.byref(_cp(params)), tree.B, V, layer, _dtype_code(layer_draft),
+                                       _ptr(layer_draft), _row_stride(layer_draft, rows), _ptr(u_probe),
+                                       ctypes.byref(tree.c()), _ptr(frontier_token), _ptr(frontier_parent),
+                                       _ptr(status), _stream(stream)))
 
 
 @dataclasses.dataclass

@@ -20,7 +20,8 @@
  *
  * General contract of every entry point:
  *   - Pointers named "device" are device pointers owned by the caller; the
- *     library allocates nothing, keeps no state between calls and never
+ *     library allocates nothing, keeps no state between calls (except
+ *     spec_tree_layer_static, whose state lives in the library) and never
  *     synchronises the host.  Every call is asynchronous on `stream`
  *     (0 = the legacy default stream).
  *   - Return value: SPEC_TREE_OK (0) or a negative SPEC_TREE_E_* code.
@@ -279,6 +280,47 @@ int spec_tree_layer(const spec_tree_params* p, int B, int V, int layer, int dtyp
 
 int spec_tree_finish(const spec_tree_params* p, int B, int V, const spec_tree_t* tree,
                      const void* state, uint32_t* status, spec_tree_stream_t stream);
+
+/*
+ * spec_tree_layer_static: spec_tree_layer for callers that cannot allocate
+ * device memory.  The pages have no counterpart: this is an interface
+ * variant of the layer-by-layer builder, not a step of the method.
+ *
+ * Who needs it: a draft loop embedded in a host runtime that reserves all
+ * device memory up front and gives its plugins no allocator, and decode
+ * loops that must not call cudaMalloc or cudaFree because those can
+ * synchronise the device in the middle of a step.  Such a caller still owns
+ * the logits, draws, tree and frontier buffers, but cannot provide the
+ * builder's per-tree state (spec_tree_layer_state_bytes() per tree).
+ *
+ * What differs from spec_tree_layer:
+ *   - the state lives in a device array inside this library, sized for
+ *     SPEC_TREE_STATIC_MAX_TREES trees (3.5 MiB, held on every GPU that loads
+ *     the library until the process exits); B > SPEC_TREE_STATIC_MAX_TREES
+ *     returns SPEC_TREE_E_PARAM before anything is launched;
+ *   - the call of the last layer (layer = depth - 1) also performs
+ *     spec_tree_finish, so it writes the node arrays and n_nodes of `tree`
+ *     (its arguments are checked before the first launch);
+ *   - the array is shared by every call in the process and keeps the last
+ *     call's contents.  Layer 0 rewrites everything later calls read, so
+ *     nothing needs clearing, but two builds whose calls overlap on the GPU
+ *     (on different streams, or from different host threads) race on it:
+ *     finish one batch's layers before another batch's layer 0 starts;
+ *   - the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.  A failed lookup returns
+ *     SPEC_TREE_E_CUDA.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.  Everything
+ * else (arguments, rows, frontier outputs, status bits, results bit for bit)
+ * is as for spec_tree_layer followed, after the last layer, by
+ * spec_tree_finish.
+ */
+#define SPEC_TREE_STATIC_MAX_TREES 64
+
+int spec_tree_layer_static(const spec_tree_params* p, int B, int V, int layer, int dtype,
+                           const void* layer_logits, int64_t row_stride, const float* u_probe,
+                           const spec_tree_t* tree, int32_t* frontier_token, int32_t* frontier_parent,
+                           uint32_t* status, spec_tree_stream_t stream);
 
 /*
  * SMART cost-model fit from profiled steps (SMART notes, Key design 2:

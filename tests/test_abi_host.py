@@ -134,3 +134,30 @@ def test_layer_mode_bad_arguments(binding):
         binding.E_PARAM
     assert lib.spec_tree_finish(ctypes.byref(p.c()), 1, 1000, ctypes.byref(t), vp(264), None, None) == \
         binding.E_LAYOUT
+
+
+def test_layer_static_host_checks(binding):
+    """The allocation-free layer call refuses batches above its array and checks arguments before any
+    CUDA call (B = 0 runs the checks alone)."""
+    lib = binding._lib
+    t = binding.c_tree()
+    for name, _ in binding.c_tree._fields_[:14]:
+        setattr(t, name, 256)
+    t.n_rows, t.max_nodes, t.sup_stride = 57, 61, 128
+    vp = ctypes.c_void_p
+    p = binding.Params(K=8, m=1, W=8, depth=8, R=60)
+
+    def call(B, layer, tree=t, params=p):
+        return lib.spec_tree_layer_static(ctypes.byref(params.c()), B, 1000, layer, binding.BF16, vp(256), 1008,
+                                          vp(256), ctypes.byref(tree), None, None, None, None)
+
+    assert call(binding.STATIC_MAX_TREES + 1, 0) == binding.E_PARAM
+    assert call(-1, 0) == binding.E_PARAM
+    assert call(0, 0) == binding.OK and call(0, 7) == binding.OK
+    assert call(0, 8) == binding.E_PARAM                                  # past the last layer
+    t.max_nodes = 60                                                      # node arrays too small for R + 1
+    assert call(0, 6) == binding.OK and call(0, 7) == binding.E_PARAM     # only the last layer writes nodes
+    t.max_nodes = 61
+    smart = binding.Params(K=8, m=1, W=8, depth=8, R=60, builder=binding.BUILDER_SMART)
+    t.n_rows = 61
+    assert call(0, 0, params=smart) == binding.E_PARAM                    # top-R builder only
