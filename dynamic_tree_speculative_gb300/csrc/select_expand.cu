@@ -25,6 +25,17 @@
 //     element that reaches the bound is appended to a candidate buffer of
 //     64-bit (order key, ~token id) composites and counted in a histogram of
 //     key offsets above the bound.
+//   queue (bf16 rows of up to 16 chunks): the cut of the support is nearly
+//     the same from row to row, so a threshold a margin below a recent
+//     row's cut predicts which vectors can hold a candidate.  During the
+//     pass each warp copies every vector whose maximum reaches it into its
+//     own queue in shared memory; after the pass the queued vectors are
+//     filtered in shared memory, with no re-read.  The prediction is
+//     checked exactly: when at least |S| elements reach the threshold, every
+//     element that reaches it was queued (a vector holding one has its
+//     maximum above it), so the threshold is a valid bound.  Otherwise (a
+//     threshold too high, a full queue, a NaN) the row takes the bound and
+//     gather above, from the same pass.
 //   select (one warp, overlapped with the next row): the histogram gives the
 //     |S|-th largest key and the count above it; the candidates are cut to
 //     the exact top-|S| by (logit desc, id asc), ranked by a count, and turned
@@ -37,6 +48,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "st_common.cuh"
@@ -61,6 +73,9 @@ constexpr int SX_FB_CAP = 1792;                  // robust path: candidate stora
 constexpr int SX_FB_HIGH = SX_FB_CAP - SX_FB_STEP;
 constexpr int SX_TBL = 32;                       // chunk maxima kept per thread: rows of up to 32 chunks
 constexpr int SX_GLIST = 1024;                   // gather list: (chunk, thread) pairs whose maximum reaches the bound
+constexpr int SX_QCH = 16;                       // queue path: rows of up to this many chunks
+constexpr int SX_QW = 56;                        // queue path: vectors queued per warp and row
+constexpr uint32_t SX_QMARGIN = 16;              // queue threshold: this many key steps below a recent cut
 // what the selector receives with a row's candidates
 constexpr int SX_HIST = 1;     // every element >= hbase, with its key histogram khist
 constexpr int SX_SORTED = 2;   // exactly the top-|S|, in order
@@ -74,12 +89,21 @@ struct RobustScratch {
   uint32_t hist[256];
 };
 
+// The queue path's storage: the table of rows of up to SX_QCH chunks, then
+// each warp's queued vectors and their vector indices in the row.
+struct QueueView {
+  uint16_t tbl_lo[SX_QCH][SX_CONS];
+  uint4 vec[SX_CWARPS][SX_QW];
+  uint16_t vid[SX_CWARPS][SX_QW];
+};
+
 struct SelShared {
   alignas(128) uint8_t ring[SX_STAGES][SX_CHUNK];
   uint64_t cand[2][SX_CAP];  // double-buffered candidates: streamers fill one, the selector drains the other
   union {
     uint16_t tbl[SX_TBL][SX_CONS];  // order key of each consumer thread's maximum in each chunk
     RobustScratch rb;
+    QueueView qv;
   };
   uint16_t glist[SX_GLIST];  // chunk << 8 | thread
   alignas(16) uint64_t ssel[SX_MAX_S];  // selector's scratch
@@ -105,6 +129,9 @@ struct SelShared {
   uint32_t thr_key;
   int strict;
   int timeout;
+  uint32_t last_cut;   // key of the |S|-th largest of the selector's latest row (0: none yet)
+  uint32_t thr_row[2]; // queue threshold of the rows of each parity (0: no queue)
+  int qbad;            // 1 + the last row whose queue failed (NaN, full queue)
 };
 
 // A candidate buffer and its fill count.
@@ -116,6 +143,9 @@ struct CandBuf {
 
 // two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
 static_assert(sizeof(SelShared) <= 233472 / 2 - 1024, "select_expand needs two CTAs per SM");
+static_assert(sizeof(QueueView) <= sizeof(RobustScratch) && sizeof(QueueView) <= 2 * SX_TBL * SX_CONS,
+              "the queue shares the table's storage");
+static_assert(offsetof(QueueView, vec) % 16 == 0, "queued vectors are 16-byte aligned");
 
 size_t select_expand_smem_bytes() { return sizeof(SelShared); }
 
@@ -522,6 +552,27 @@ __device__ __forceinline__ uint32_t chunk_max<float>(const uint4 (&v)[SX_VPT], b
     for (int j = 0; j < 4; ++j) k = max(k, elem_key<float>(v[q], j, nan));
   full = k;
   return k >> 16;
+}
+
+// Queue test: does any element of a 16-byte vector reach the threshold
+// (bf16 value, both halves)?  NaN never does.
+template <typename T>
+__device__ __forceinline__ bool vec_reaches(const uint4& v, __nv_bfloat162 thr2);
+
+template <>
+__device__ __forceinline__ bool vec_reaches<__nv_bfloat16>(const uint4& v, __nv_bfloat162 thr2) {
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
+  const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
+  const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&v.w);
+  __nv_bfloat162 mx = __hmax2(__hmax2(a, b), __hmax2(c, d));
+  mx = __hmax2(mx, __lowhigh2highlow(mx));
+  return __hbge2(mx, thr2);
+}
+
+template <>
+__device__ __forceinline__ bool vec_reaches<float>(const uint4&, __nv_bfloat162) {
+  return false;  // f32 rows never take the queue path
 }
 
 // Table threshold of a bound: entries at or above it may hold an element >= bound.
@@ -933,6 +984,10 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
     }
     fence_mbar_init();
     s.timeout = 0;
+    s.last_cut = 0u;
+    s.thr_row[0] = s.thr_row[1] = 0u;
+    s.qbad = 0;
+    s.count[0] = s.count[1] = 0;
   }
   for (int i = tid; i < 2 * 256; i += SX_THREADS) s.khist[i >> 8][i & 255] = 0u;
   __syncthreads();  // the last CTA-wide barrier: the roles split below
@@ -960,10 +1015,18 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
       } else {
         n_sup = warp_select_sort<E::KEY_BITS>(s, s.cand[q], min(n, SX_CAP), a.S, val);
       }
+      // the row's cut (the key of its |S|-th largest) predicts the next rows' cuts
+      if (n_sup == a.S) {
+        const int rl = n_sup - 1;
+        const uint64_t vc = (rl >> 5) == 0 ? val[0] : (rl >> 5) == 1 ? val[1] : (rl >> 5) == 2 ? val[2] : val[3];
+        const uint64_t cut = __shfl_sync(FULL, vc, rl & 31);
+        if (lane == 0) *reinterpret_cast<volatile uint32_t*>(&s.last_cut) = static_cast<uint32_t>(cut >> 32);
+      }
       expand_epilogue<T>(val, a, out_row, in_row, n_sup);
-      // the histogram starts the buffer's next row at zero
+      // the histogram and the count start the buffer's next row at zero
 #pragma unroll
       for (int j = 0; j < 8; ++j) s.khist[q][j * 32 + lane] = 0u;
+      if (lane == 0) s.count[q] = 0;
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.cempty[q]);
     }
@@ -1013,6 +1076,8 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
   const int jth = (a.S + SX_CWARPS - 1) / SX_CWARPS;
   const bool tabled = nch <= SX_TBL;  // longer rows take the robust path
   const bool has_vec = nch > 1 || tid < last_nvec;  // this thread sees at least one whole vector
+  const bool queue_rows = sizeof(T) == 2 && nch <= SX_QCH;  // rows that can take the queue path
+  const unsigned lt = (1u << lane) - 1u;
   for (int64_t lr = 0; lr < my_rows; ++lr) {
     const int64_t out_row = b * a.n_rows + a.sup_row0 + e;
     const int64_t in_row = b * a.in_rows + e;
@@ -1022,8 +1087,19 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
     const CandBuf cb{s.cand[q], &s.count[q], SX_CAP};
     uint32_t* const kh = s.khist[q];  // zeroed by the selector once it is done with the buffer
 
+    // the queue threshold of this row (a key; 0: no queue), set before a barrier
+    const uint32_t thr = queue_rows ? s.thr_row[q] : 0u;
+    const bool qmode = thr >= 0x80u;  // smaller keys are NaN patterns
+    __nv_bfloat162 thr2;
+    {
+      const __nv_bfloat16 tv = __float2bfloat16_rn(bf16_key_value(qmode ? thr : 0xffffu));
+      thr2 = __halves2bfloat162(tv, tv);
+    }
+    int qn = 0;  // vectors this warp queued (uniform over the warp)
+
     // the one pass over the row: each thread's maximum in every chunk goes
-    // to the table, and its running maximum is kept
+    // to the table, and its running maximum is kept; in queue mode every
+    // vector whose maximum reaches the threshold is queued by its warp
     uint32_t tkey = 0u;
     bool row_nan = false;
     for (int c = 0; c < nch; ++c) {
@@ -1046,6 +1122,21 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
       const uint32_t ck = chunk_max<T>(v, row_nan, full);
       tkey = max(tkey, full);
       if (tabled) s.tbl[c][tid] = static_cast<uint16_t>(ck);
+      if (qmode) {
+#pragma unroll
+        for (int k = 0; k < SX_VPT; ++k) {
+          const bool hit = vec_reaches<T>(v[k], thr2);
+          const unsigned bal = __ballot_sync(FULL, hit);
+          if (bal) {
+            const int pos = qn + __popc(bal & lt);
+            if (hit && pos < SX_QW) {
+              s.qv.vec[warp][pos] = v[k];
+              s.qv.vid[warp][pos] = static_cast<uint16_t>(c * (SX_CHUNK / 16) + tid + k * SX_CONS);
+            }
+            qn += __popc(bal);
+          }
+        }
+      }
       if (++st == SX_STAGES) {
         st = 0;
         phase ^= 1u;
@@ -1060,106 +1151,154 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
     uint32_t tmax = has_vec ? tkey : 0u;
     if (sizeof(T) == 2 && row_nan) tmax = 0u;
     tmax = max(tmax, tail_key);
-    // the bound: the minimum over warps of each warp's jth-largest thread
-    // maximum.  Thread maxima are distinct elements of the row and
-    // jth * warps >= |S|, so at least |S| elements reach it.
-    const uint32_t wv = warp_kth_largest(tmax, jth);
-    if (lane == 0) s.warp_bound[warp] = wv;
-    if (tid == 0) {
+
+    bool done = false;  // the row's candidates are complete
+    if (qmode) {
+      // the buffer's count and histogram were zeroed by the selector when it
+      // handed the buffer back two rows ago
       if (lr >= 2 && !mbar_wait(&s.cempty[q], static_cast<uint32_t>(((lr >> 1) - 1) & 1))) s.timeout = 1;
-      *cb.n = 0;
-      s.glist_n = 0;
-    }
-    csync();
-    uint32_t bound = 0xffffffffu;
-#pragma unroll
-    for (int w = 0; w < SX_CWARPS; ++w) bound = min(bound, s.warp_bound[w]);
-    // a key-0 bound (NaN, or too few elements) has no value to compare against
-    bool robust = bound == 0u || !tabled;
-    if (!robust) {
-      // the gather list: every (chunk, thread) whose maximum reaches the
-      // bound (warp-aggregated appends)
-      const uint32_t tb = table_bound<T>(bound);
-      uint32_t hits = 0u;
-      for (int c = 0; c < nch; ++c) hits |= (static_cast<uint32_t>(s.tbl[c][tid]) >= tb ? 1u : 0u) << c;
-      const int nh = __popc(hits);
-      int incl = nh;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(FULL, incl, o);
-        if (lane >= o) incl += y;
-      }
-      int gbase = 0;
-      if (lane == 31) gbase = atomicAdd(&s.glist_n, incl);
-      gbase = __shfl_sync(FULL, gbase, 31) + incl - nh;
-      while (hits) {
-        const int c = __ffs(hits) - 1;
-        hits &= hits - 1u;
-        if (gbase < SX_GLIST) s.glist[gbase] = static_cast<uint16_t>((c << 8) | tid);
-        ++gbase;
-      }
-      csync();
-      const int nlist = s.glist_n;
-      robust = nlist > SX_GLIST;  // more than the candidate buffer could hold anyway
-    }
-    if (!robust) {
-      // the gather: the listed vectors are re-read from L2 (each list entry
-      // is the four vectors of one thread in one chunk, spread over the CTA
-      // so that every load is in flight at once), and every element that
-      // reaches the bound is appended to the candidates and counted in the
-      // key histogram
+      if (row_nan || qn > SX_QW) s.qbad = static_cast<int>(lr) + 1;
+      // filter this warp's queue in shared memory: every element that
+      // reaches the threshold becomes a candidate
       Filter<T> flt;
-      flt.init(bound);
-      const int ntask = s.glist_n * SX_VPT;
-      for (int i0 = 0; i0 < ntask; i0 += SX_CONS * SX_VPT) {
-        uint4 v[SX_VPT];
-        uint32_t vid[SX_VPT];
-        bool ok[SX_VPT];
-#pragma unroll
-        for (int u = 0; u < SX_VPT; ++u) {
-          const int i = i0 + u * SX_CONS + tid;
-          ok[u] = false;
-          vid[u] = 0u;
-          v[u] = make_uint4(0, 0, 0, 0);
-          if (i < ntask) {
-            const uint32_t ent = s.glist[i / SX_VPT];
-            const int c = static_cast<int>(ent >> 8);
-            const int vi = static_cast<int>(ent & 0xffu) + (i % SX_VPT) * SX_CONS;
-            const int nvec = c + 1 < nch ? SX_CHUNK / 16 : last_nvec;
-            ok[u] = vi < nvec;
-            vid[u] = static_cast<uint32_t>(c * CHUNK_ELEMS + vi * VEC);
-            if (ok[u]) v[u] = ldg_stream(row + static_cast<int64_t>(c) * SX_CHUNK + static_cast<int64_t>(vi) * 16);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < SX_VPT; ++u)
-          if (ok[u] && flt.pass(v[u])) flt.emit(cb, v[u], vid[u], p2over, kh, bound);
-      }
-      if (tail_id < a.V && tail_key >= bound) {
+      flt.init(thr);
+      const int nq = min(qn, SX_QW);
+      for (int i = lane; i < nq; i += 32)
+        flt.emit(cb, s.qv.vec[warp][i], static_cast<uint32_t>(s.qv.vid[warp][i]) * VEC, p2over, kh, thr);
+      if (tail_id < a.V && tail_key >= thr) {
         const int pos = atomicAdd(cb.n, 1);
         if (pos < cb.cap) cb.c[pos] = make_comp(tail_key, static_cast<uint32_t>(tail_id));
-        atomicAdd(&kh[min(tail_key - bound, 255u)], 1u);
+        atomicAdd(&kh[min(tail_key - thr, 255u)], 1u);
+      }
+      if (tid == 0) {
+        // the next row's threshold: a margin below the latest cut (the slot
+        // of the other parity, read by the next row after a barrier)
+        const uint32_t lc = *reinterpret_cast<volatile uint32_t*>(&s.last_cut);
+        s.thr_row[q ^ 1] = lc >= 0x80u + SX_QMARGIN ? lc - SX_QMARGIN : thr;
       }
       csync();
-      if (*cb.n <= SX_CAP) {
-        // the selector cuts them to the top-|S| with the histogram
+      const int n = *cb.n;
+      done = s.qbad != static_cast<int>(lr) + 1 && n >= a.S && n <= SX_CAP;
+      if (done) {
+        // at least |S| elements reach the threshold, and all of them are
+        // here: the selector cuts them with the histogram
         if (tid == 0) {
           s.mode[q] = SX_HIST;
-          s.hbase[q] = bound;
+          s.hbase[q] = thr;
         }
       } else {
-        robust = true;  // massive ties at the bound
+        // start the row over on the bound-and-gather path
+        kh[tid] = 0u;
       }
     }
-    if (robust) {
-      // redo the row in id order from global memory with the robust path's
-      // own candidate storage, then hand the selector the exact top-|S|
-      const CandBuf fb{s.rb.fbuf, &s.count[q], SX_FB_CAP};
-      select_row_fallback<T>(s, fb, row, a.V, a.S, nonfinite, overflow);
-      select_topk<E::KEY_BITS>(s, fb, *fb.n, a.S);
-      for (int i = tid; i < *fb.n; i += SX_CONS) cb.c[i] = fb.c[i];
-      if (tid == 0) s.mode[q] = SX_SORTED;  // select_topk leaves them in order
+    if (!done) {
+      // the bound: the minimum over warps of each warp's jth-largest thread
+      // maximum.  Thread maxima are distinct elements of the row and
+      // jth * warps >= |S|, so at least |S| elements reach it.
+      const uint32_t wv = warp_kth_largest(tmax, jth);
+      if (lane == 0) s.warp_bound[warp] = wv;
+      if (tid == 0) {
+        if (lr >= 2 && !mbar_wait(&s.cempty[q], static_cast<uint32_t>(((lr >> 1) - 1) & 1))) s.timeout = 1;
+        *cb.n = 0;
+        s.glist_n = 0;
+      }
       csync();
+      uint32_t bound = 0xffffffffu;
+#pragma unroll
+      for (int w = 0; w < SX_CWARPS; ++w) bound = min(bound, s.warp_bound[w]);
+      if (tid == 0 && queue_rows) {
+        // the next row's threshold: a margin below the latest cut, else this
+        // row's bound
+        const uint32_t lc = *reinterpret_cast<volatile uint32_t*>(&s.last_cut);
+        s.thr_row[q ^ 1] = lc >= 0x80u + SX_QMARGIN ? lc - SX_QMARGIN : bound;
+      }
+      // a key-0 bound (NaN, or too few elements) has no value to compare against
+      bool robust = bound == 0u || !tabled;
+      if (!robust) {
+        // the gather list: every (chunk, thread) whose maximum reaches the
+        // bound (warp-aggregated appends)
+        const uint32_t tb = table_bound<T>(bound);
+        uint32_t hits = 0u;
+        for (int c = 0; c < nch; ++c) hits |= (static_cast<uint32_t>(s.tbl[c][tid]) >= tb ? 1u : 0u) << c;
+        const int nh = __popc(hits);
+        int incl = nh;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(FULL, incl, o);
+          if (lane >= o) incl += y;
+        }
+        int gbase = 0;
+        if (lane == 31) gbase = atomicAdd(&s.glist_n, incl);
+        gbase = __shfl_sync(FULL, gbase, 31) + incl - nh;
+        while (hits) {
+          const int c = __ffs(hits) - 1;
+          hits &= hits - 1u;
+          if (gbase < SX_GLIST) s.glist[gbase] = static_cast<uint16_t>((c << 8) | tid);
+          ++gbase;
+        }
+        csync();
+        const int nlist = s.glist_n;
+        robust = nlist > SX_GLIST;  // more than the candidate buffer could hold anyway
+      }
+      if (!robust) {
+        // the gather: the listed vectors are re-read from L2 (each list entry
+        // is the four vectors of one thread in one chunk, spread over the CTA
+        // so that every load is in flight at once), and every element that
+        // reaches the bound is appended to the candidates and counted in the
+        // key histogram
+        Filter<T> flt;
+        flt.init(bound);
+        const int ntask = s.glist_n * SX_VPT;
+        for (int i0 = 0; i0 < ntask; i0 += SX_CONS * SX_VPT) {
+          uint4 v[SX_VPT];
+          uint32_t vid[SX_VPT];
+          bool ok[SX_VPT];
+#pragma unroll
+          for (int u = 0; u < SX_VPT; ++u) {
+            const int i = i0 + u * SX_CONS + tid;
+            ok[u] = false;
+            vid[u] = 0u;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (i < ntask) {
+              const uint32_t ent = s.glist[i / SX_VPT];
+              const int c = static_cast<int>(ent >> 8);
+              const int vi = static_cast<int>(ent & 0xffu) + (i % SX_VPT) * SX_CONS;
+              const int nvec = c + 1 < nch ? SX_CHUNK / 16 : last_nvec;
+              ok[u] = vi < nvec;
+              vid[u] = static_cast<uint32_t>(c * CHUNK_ELEMS + vi * VEC);
+              if (ok[u]) v[u] = ldg_stream(row + static_cast<int64_t>(c) * SX_CHUNK + static_cast<int64_t>(vi) * 16);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < SX_VPT; ++u)
+            if (ok[u] && flt.pass(v[u])) flt.emit(cb, v[u], vid[u], p2over, kh, bound);
+        }
+        if (tail_id < a.V && tail_key >= bound) {
+          const int pos = atomicAdd(cb.n, 1);
+          if (pos < cb.cap) cb.c[pos] = make_comp(tail_key, static_cast<uint32_t>(tail_id));
+          atomicAdd(&kh[min(tail_key - bound, 255u)], 1u);
+        }
+        csync();
+        if (*cb.n <= SX_CAP) {
+          // the selector cuts them to the top-|S| with the histogram
+          if (tid == 0) {
+            s.mode[q] = SX_HIST;
+            s.hbase[q] = bound;
+          }
+        } else {
+          robust = true;  // massive ties at the bound
+        }
+      }
+      if (robust) {
+        // redo the row in id order from global memory with the robust path's
+        // own candidate storage, then hand the selector the exact top-|S|
+        const CandBuf fb{s.rb.fbuf, &s.count[q], SX_FB_CAP};
+        select_row_fallback<T>(s, fb, row, a.V, a.S, nonfinite, overflow);
+        select_topk<E::KEY_BITS>(s, fb, *fb.n, a.S);
+        for (int i = tid; i < *fb.n; i += SX_CONS) cb.c[i] = fb.c[i];
+        if (tid == 0) s.mode[q] = SX_SORTED;  // select_topk leaves them in order
+        csync();
+      }
     }
     // hand the candidates to the selector warp and move on to the next row
     if (tid == 0) {
