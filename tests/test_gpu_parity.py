@@ -161,6 +161,36 @@ def test_heavy_ties_and_constant_rows():
     assert ex + exm == wl.B
 
 
+def test_rows_whose_cut_jumps():
+    """Rows whose top-|S| cut jumps far from the previous rows' (scaled, shifted, integer-valued and
+    constant rows mixed among normal ones), many rows per CTA: a threshold predicted from earlier
+    rows is then too high, too low or floods the queue, and the exact path must take over."""
+    wl = WL.WORKLOADS["vicuna"].with_(B=64, V=20000)
+    case = parity.make_case(wl, 8)
+    n_rows = case.draft.shape[1]
+    g = torch.Generator().manual_seed(8)
+    kind = torch.randint(0, 20, (wl.B, n_rows), generator=g)
+    x = case.draft.float()
+    scale = torch.ones((wl.B, n_rows))
+    shift = torch.zeros((wl.B, n_rows))
+    scale[(kind >= 8) & (kind < 11)] = 3.0
+    scale[(kind >= 11) & (kind < 14)] = 0.3
+    shift[(kind >= 14) & (kind < 16)] = 6.0
+    shift[(kind >= 16) & (kind < 18)] = -6.0
+    x = x * scale[..., None] + shift[..., None]
+    ints = torch.randint(-6, 3, x.shape, generator=g).float()
+    x = torch.where((kind == 18)[..., None], ints, x)
+    x = torch.where((kind == 19)[..., None], torch.full_like(x, 0.25), x)
+    case.draft = x.to(torch.bfloat16)
+    sample = list(range(0, wl.B, 4))
+    trees = parity.oracle_build(case, sample)
+    out = parity.run_gpu(case, None)
+    assert out["status"] == 0, out["status"]
+    ex, exm = parity.compare_build(out, trees, min(wl.support, wl.V))
+    print(f"cut jumps: exact {ex} exempt {exm} of {len(sample)}")
+    assert exm <= 0.1 * len(sample) + 1
+
+
 def test_nan_row_sets_status_and_stays_in_bounds():
     from dynamic_tree_speculative_gb300 import binding as B
     wl = WL.WORKLOADS["vicuna"].with_(B=2, V=5000, depth=3, R=10, K=4, W=2)
