@@ -330,8 +330,11 @@ def e2e(args, wl, cparams, draft, target, u_probe, uv, ub, tree, out, status, in
     import torch
     from dynamic_tree_speculative_gb300 import binding as B
     from dynamic_tree_speculative_gb300 import ranks as R
-    hosts = [x.cpu().pin_memory() for x in (draft, target, u_probe, uv, ub)]
-    devs = [draft, target, u_probe, uv, ub]
+    # inputs copied to HBM every step; the target logits stay in pinned host memory and verify reads
+    # only the accepted path's rows from there (unified addressing over NVLink-C2C)
+    hosts = [x.cpu().pin_memory() for x in (draft, u_probe, uv, ub)]
+    devs = [draft, u_probe, uv, ub]
+    target_h = target.cpu().pin_memory()
     res_h = [torch.empty(out.accept_len.shape, dtype=torch.int32).pin_memory(),
              torch.empty(out.out_tok.shape, dtype=torch.int32).pin_memory()]
     stream = torch.cuda.current_stream()
@@ -341,7 +344,7 @@ def e2e(args, wl, cparams, draft, target, u_probe, uv, ub, tree, out, status, in
         for d, h in zip(devs, hosts):
             d.copy_(h, non_blocking=True)
         B.spec_tree_build(cparams, V, draft, u_probe, tree, status, stream)
-        B.spec_tree_verify(cparams, V, target, tree, uv, ub, out.accept_len, out.out_tok, out.out_node, None,
+        B.spec_tree_verify(cparams, V, target_h, tree, uv, ub, out.accept_len, out.out_tok, out.out_node, None,
                            status, stream)
         res_h[0].copy_(out.accept_len, non_blocking=True)
         res_h[1].copy_(out.out_tok, non_blocking=True)
@@ -358,11 +361,15 @@ def e2e(args, wl, cparams, draft, target, u_probe, uv, ub, tree, out, status, in
     torch.cuda.synchronize()
     R.barrier(info, dev)
     el = R.max_over_ranks(a.elapsed_time(b) / 1e3, info, dev)
-    h2d = sum(h.numel() * h.element_size() for h in hosts)
+    acc = res_h[0].long()
+    target_read = int((acc + 1).sum()) * target_h.shape[-1] * target_h.element_size()
+    h2d = sum(h.numel() * h.element_size() for h in hosts) + target_read
     d2h = sum(h.numel() * h.element_size() for h in res_h)
     return {"value": R.sum_over_ranks(wl.B * K, info, dev) / el, "unit": "trees/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
-            "path": "pinned host -> HBM copies, spec_tree_build, spec_tree_verify, results -> host"}
+            "target_rows_read_from_host_bytes": target_read,
+            "path": "draft logits and uniforms copied pinned host -> HBM, spec_tree_build, spec_tree_verify "
+                    "reading the accepted path's target rows from pinned host memory, results -> host"}
 
 
 def main():

@@ -219,9 +219,13 @@ int spec_tree_build(const spec_tree_params* p, int B, int V, int dtype,
  * u_verify[b][l][j].  An accepted child becomes the node; when every child
  * is rejected or the node has none, the bonus token is the first token in id
  * order with u_bonus[b] * Zr < sum_{v' <= v} w(v').
- *   target_logits: device [B][tree->max_nodes][row_stride]; row i is the
- *                  target logits at node i.  Only rows on the accepted path
- *                  are read.
+ *   target_logits: [B][tree->max_nodes][row_stride]; row i is the target
+ *                  logits at node i.  Only rows on the accepted path are
+ *                  read, with plain loads, so the array may also live in
+ *                  pinned host memory (cudaHostAlloc; its host pointer is a
+ *                  valid device address under unified addressing): the
+ *                  kernel then reads just those rows over NVLink-C2C (or
+ *                  PCIe) instead of the caller copying every row to HBM.
  *   u_verify: device [B][depth][K] float; u_bonus: device [B] float.
  *   accept_len: device [B]; out_tok, out_node: device [B][depth + 1]
  *   (accepted tokens then the bonus token; accepted node indices then -1;

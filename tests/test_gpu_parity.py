@@ -191,6 +191,31 @@ def test_rows_whose_cut_jumps():
     assert exm <= 0.1 * len(sample) + 1
 
 
+def test_verify_reads_target_rows_from_pinned_host_memory():
+    """Target logits left in pinned host memory (unified addressing): verify reads the accepted
+    path's rows over the host link and returns exactly what it returns from HBM."""
+    from dynamic_tree_speculative_gb300 import binding as B
+    wl = WL.WORKLOADS["llama3"].with_(B=8)
+    case = parity.make_case(wl, 12)
+    trees = parity.oracle_build(case, range(wl.B))
+    target = parity.target_for(case, trees, 12)
+    params = B.Params.from_workload(wl)
+    dev = "cuda"
+    tree = B.TreeBuffers(params, wl.B, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    B.spec_tree_build(params, wl.V, case.draft.to(dev), case.u_probe.to(dev), tree, status)
+    outs = []
+    for tgt in (target.to(dev), target.pin_memory()):
+        out = B.VerifyOutputs(params, wl.B, device=dev)
+        B.spec_tree_verify(params, wl.V, tgt, tree, case.u_verify.to(dev), case.u_bonus.to(dev), out.accept_len,
+                           out.out_tok, out.out_node, out.margins, status)
+        torch.cuda.synchronize()
+        outs.append([x.cpu() for x in (out.accept_len, out.out_tok, out.out_node)])
+    assert int(status.item()) == 0
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
 def test_nan_row_sets_status_and_stays_in_bounds():
     from dynamic_tree_speculative_gb300 import binding as B
     wl = WL.WORKLOADS["vicuna"].with_(B=2, V=5000, depth=3, R=10, K=4, W=2)
