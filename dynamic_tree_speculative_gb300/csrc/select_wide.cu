@@ -62,13 +62,13 @@ struct WideShared {
 };
 
 // Calls f(key, id) for every element of the row that thread tid owns: the
-// 16-byte vectors tid, tid + 1024, ... (loaded eight at a time, so that eight
-// loads are in flight) and then the scalar tail element nvec * VEC + tid, if
-// any.
+// 16-byte vectors tid, tid + 1024, ... (loaded four at a time, so that four
+// loads are in flight; two CTAs of 1024 threads share an SM, 32 registers a
+// thread) and then the scalar tail element nvec * VEC + tid, if any.
 template <typename T, typename F>
 __device__ __forceinline__ void for_each_elem(const uint8_t* row, int V, int nvec, bool& nonfinite, F f) {
   using E = Elem<T>;
-  constexpr int VEC = E::VEC, U = 8;
+  constexpr int VEC = E::VEC, U = 4;
   const int tid = threadIdx.x;
   for (int v0 = tid; v0 < nvec; v0 += U * SW_THREADS) {
     uint4 v[U];
@@ -358,7 +358,7 @@ __device__ __forceinline__ uint32_t vec_max_key16<float>(const uint4& v, bool& n
 // (ties); block-uniform.
 template <typename T>
 __device__ bool table_select(WideShared& s, const uint8_t* row, int V, int nvec, int S, bool& nonfinite) {
-  constexpr int VEC = Elem<T>::VEC, U = 8;
+  constexpr int VEC = Elem<T>::VEC, U = 4;
   const int tid = threadIdx.x;
   for (int v0 = tid; v0 < nvec; v0 += U * SW_THREADS) {
     uint4 v[U];
@@ -505,7 +505,7 @@ __device__ void wide_epilogue(WideShared& s, const SelLaunch& a, int64_t out_row
 }
 
 template <typename T>
-__global__ void __launch_bounds__(SW_THREADS) select_wide_kernel(SelLaunch a, int64_t row_bytes) {
+__global__ void __launch_bounds__(SW_THREADS, 2) select_wide_kernel(SelLaunch a, int64_t row_bytes) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   WideShared& s = *reinterpret_cast<WideShared*>(smem_raw);
   const int64_t g = blockIdx.x;
