@@ -44,6 +44,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="one JSON line per configuration: the workloads, the batch sweep with both builders, "
+                         "the wide supports (single GPU; not the contract line)")
     return ap.parse_args()
 
 
@@ -372,10 +375,90 @@ def e2e(args, wl, cparams, draft, target, u_probe, uv, ub, tree, out, status, in
                     "reading the accepted path's target rows from pinned host memory, results -> host"}
 
 
+def sweep_configs():
+    from dynamic_tree_speculative_gb300 import workloads as WL
+    base = WL.WORKLOADS["sweep_smart"]
+    cfgs = [WL.WORKLOADS["vicuna"], WL.WORKLOADS["llama3"], WL.WORKLOADS["rl"]]
+    for builder in ("topr", "smart"):
+        for b in (1, 2, 4, 8, 16, 32, 64, 128, 256):
+            cfgs.append(base.with_(name=f"sweep_{builder}_b{b}", B=b, builder=builder))
+    for sup in (256, 512, 1024):
+        cfgs.append(WL.BENCH_WORKLOAD.with_(name=f"llama3_b64_support{sup}", support=sup))
+    return cfgs
+
+
+def run_sweep(args):
+    """Build + verify throughput per configuration, inputs resident in HBM, CUDA-event timed."""
+    import torch
+    from dynamic_tree_speculative_gb300 import binding as B
+    from dynamic_tree_speculative_gb300 import workloads as WL
+    dev = torch.device("cuda")
+    hbm, peak_kind = peaks()
+    steps = min(args.steps, 200)
+    for wl in sweep_configs():
+        params = B.Params.from_workload(wl)
+        cp = params.c()
+        n_rows = B.rows_needed(params)
+        draft, latent = WL.draft_logits(wl, args.seed, n_rows=n_rows, device=dev)
+        u_probe = WL.build_uniforms(wl, args.seed, n_rows, device=dev)
+        uv, ub = WL.verify_uniforms(wl, args.seed, device=dev)
+        tree = B.TreeBuffers(params, wl.B, device=dev)
+        out = B.VerifyOutputs(params, wl.B, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        B.spec_tree_build(cp, wl.V, draft, u_probe, tree, status)
+        torch.cuda.synchronize()
+        target = WL.target_logits(wl, args.seed, latent, tree.node_exp_row, device=dev)
+        del latent
+        stream = torch.cuda.current_stream()
+
+        def step(ev=None):
+            if ev is not None:
+                ev[0].record(stream)
+            B.spec_tree_select_expand(cp, wl.V, draft, u_probe, tree, status, stream)
+            if ev is not None:
+                ev[1].record(stream)
+            B.spec_tree_rank(cp, wl.V, tree, status, stream)
+            B.spec_tree_verify(cp, wl.V, target, tree, uv, ub, out.accept_len, out.out_tok, out.out_node, None,
+                               status, stream)
+
+        for _ in range(max(args.warmup, 3)):
+            step()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for k in range(steps):
+            step(evs[k])
+        b.record(stream)
+        torch.cuda.synchronize()
+        el = a.elapsed_time(b) / 1e3
+        sel_s = statistics.mean(x.elapsed_time(y) for x, y in evs) / 1e3
+        acc = out.accept_len.cpu()
+        es = 2 if wl.dtype == "bf16" else 4
+        S = min(wl.support, wl.V)
+        draft_bytes = wl.B * n_rows * wl.V * es
+        sup_bytes = wl.B * n_rows * (S * 12 + 12)
+        step_bytes = draft_bytes + sup_bytes + int((acc.long() + 1).sum()) * wl.V * es
+        sel_bytes = draft_bytes + sup_bytes + wl.B * n_rows * 4
+        line = {"sweep": wl.name, "config": config_of(wl, 1), "trees_per_s": wl.B * steps / el,
+                "ms_per_step": 1e3 * el / steps, "logit_gbs": step_bytes * steps / el / 1e9,
+                "logit_frac_of_peak": step_bytes * steps / el / 1e9 / hbm,
+                "select_expand_ms": 1e3 * sel_s, "select_expand_frac": sel_bytes / sel_s / 1e9 / hbm,
+                "peak_gbs": hbm, "peak_kind": peak_kind, "accept_len_mean": float(acc.float().mean()),
+                "tree_nodes_mean": float((tree.n_nodes.cpu().float() - 1).mean()), "status": int(status.item()),
+                "steps": steps}
+        print(json.dumps(line), flush=True)
+        del draft, target, tree, out
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 
