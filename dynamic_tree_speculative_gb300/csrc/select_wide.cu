@@ -46,7 +46,6 @@ struct WideShared {
   };
   uint64_t cand[SW_CAP];            // candidates; at the end the top-|S| in rank order
   uint32_t list[SW_CAP];            // table path: vectors to gather
-  uint32_t sample[SW_THREADS];      // table path: a sorted sample of the table
   uint32_t hist[256];
   float red[4][SW_WARPS];         // block reductions
   float scan[SW_WARPS];           // block scan of the tail weights
@@ -296,24 +295,21 @@ __device__ void sort_cand_desc(WideShared& s, int n) {
   __syncthreads();
 }
 
-// Bitonic sort of a[0..P) descending (P a power of two <= 2048).
-__device__ void sort_u32_desc(uint32_t* a, int P) {
-  const int tid = threadIdx.x;
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      __syncthreads();
-      for (int i = tid; i < P / 2; i += SW_THREADS) {
-        const int pos = 2 * i - (i & (stride - 1));
-        const uint32_t x = a[pos], y = a[pos + stride];
-        const bool desc = (pos & size) == 0;
-        if ((x < y) == desc) {
-          a[pos] = y;
-          a[pos + stride] = x;
-        }
-      }
-    }
+// The (r+1)-th largest, with multiplicity, of the 16-bit values x held one
+// per thread of the block (0 <= r < blockDim.x): fixes the answer's bits from
+// the top, each by one block-wide count of the values that share the bits
+// fixed so far and have the next bit set.  All threads call it.
+__device__ __forceinline__ uint32_t block_kth_largest_u16(uint32_t x, int r) {
+  uint32_t prefix = 0u;
+  int need = r + 1;
+  for (int bit = 15; bit >= 0; --bit) {
+    const uint32_t cand = prefix | (1u << bit);
+    const uint32_t hi = 0xffffu & ~((1u << bit) - 1u);
+    const int c = __syncthreads_count((x & hi) == cand);
+    if (c >= need) prefix = cand;
+    else need -= c;
   }
-  __syncthreads();
+  return prefix;
 }
 
 // 16-bit order key of the maximum of one 16-byte vector, for the table:
@@ -348,7 +344,7 @@ __device__ __forceinline__ uint32_t vec_max_key16<float>(const uint4& v, bool& n
 }
 
 // Table path: one pass stores every vector's maximum key; the bound is a rank
-// of a sorted sample of the table expected to leave about 1.5 |S| entries at
+// of a sample of the table expected to leave about 1.5 |S| entries at
 // or above it, accepted once an exact count shows between |S| and SW_CAP
 // entries there (each entry is a distinct element, so at least |S| elements
 // reach the bound); the listed vectors are re-read and every element that
@@ -374,14 +370,13 @@ __device__ bool table_select(WideShared& s, const uint8_t* row, int V, int nvec,
     }
   }
   __syncthreads();
-  s.sample[tid] = s.tbl[static_cast<int64_t>(tid) * nvec / SW_THREADS];
-  sort_u32_desc(s.sample, SW_THREADS);
+  const uint32_t sample = s.tbl[static_cast<int64_t>(tid) * nvec / SW_THREADS];
   int r = static_cast<int>(ceilf(1.5f * S * SW_THREADS / nvec)) - 1;
   r = r < 0 ? 0 : (r > SW_THREADS - 1 ? SW_THREADS - 1 : r);
   uint32_t b16 = 0u;
   bool ok = false;
   for (int attempt = 0; attempt < 4 && !ok; ++attempt) {
-    b16 = s.sample[r];
+    b16 = block_kth_largest_u16(sample, r);  // rank r of the sample, in descending order
     int c = 0;
     for (int vi = tid; vi < nvec; vi += SW_THREADS) c += s.tbl[vi] >= b16;
     int total;
