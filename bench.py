@@ -450,7 +450,54 @@ def run_sweep(args):
         print(json.dumps(line), flush=True)
         del draft, target, tree, out
         torch.cuda.empty_cache()
+    for b in (8, 64):
+        print(json.dumps(sweep_layer_mode(WL.BENCH_WORKLOAD.with_(name=f"layer_mode_b{b}", B=b), args)), flush=True)
     return 0
+
+
+def sweep_layer_mode(wl, args):
+    """The layer-by-layer build (one spec_tree_layer call per layer, then spec_tree_finish) against the
+    one-shot spec_tree_build on the same draft rows; each layer's rows are a slice of the same tensor."""
+    import torch
+    from dynamic_tree_speculative_gb300 import binding as B
+    from dynamic_tree_speculative_gb300 import workloads as WL
+    dev = torch.device("cuda")
+    params = B.Params.from_workload(wl)
+    cp = params.c()
+    n_rows = B.rows_needed(params)
+    draft, _ = WL.draft_logits(wl, args.seed, n_rows=n_rows, device=dev)
+    u_probe = WL.build_uniforms(wl, args.seed, n_rows, device=dev)
+    tree = B.TreeBuffers(params, wl.B, device=dev)
+    state = B.LayerState(params, wl.B, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    layers = []
+    for layer in range(wl.depth):
+        rows = B.spec_tree_layer_rows(params, layer)
+        r0 = 0 if layer == 0 else 1 + (layer - 1) * wl.W
+        layers.append((layer, draft[:, r0:r0 + rows].contiguous(), u_probe[:, r0:r0 + rows].contiguous()))
+
+    def one_shot():
+        B.spec_tree_build(cp, wl.V, draft, u_probe, tree, status)
+
+    def layered():
+        for layer, d, u in layers:
+            B.spec_tree_layer(cp, wl.V, layer, d, u, tree, state, status)
+        B.spec_tree_finish(cp, wl.V, tree, state, status)
+
+    res = {}
+    for name, fn in (("one_shot_build_us", one_shot), ("layer_by_layer_build_us", layered)):
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(20):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        res[name] = a.elapsed_time(b) / 20 * 1e3
+    return {"sweep": wl.name, "config": config_of(wl, 1), **res, "layer_calls": wl.depth + 1,
+            "status": int(status.item())}
 
 
 def main():

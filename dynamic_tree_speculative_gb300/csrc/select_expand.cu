@@ -783,10 +783,13 @@ __device__ int warp_select_sort(SelShared& s, const uint64_t* c, int n, int k, u
 // key hbase + b; the last bin also takes every larger key), by one warp.
 // The histogram gives the k-th largest key t and the count above it; keys
 // above t are in, and of the keys equal to t the smallest ids fill the rest.
-// A rank count then orders the k.  Falls back to warp_select_sort when t
-// falls in the open last bin or more than 32 keys tie at t.
+// A counting sort over the histogram's bins then orders the k (descending
+// key), and inside a bin a count of larger composites orders them (ascending
+// id; the open last bin holds several keys).  Falls back to warp_select_sort
+// when t falls in the open last bin or more than 32 keys tie at t.  The
+// histogram is used as the bins' cursors (the caller zeroes it afterwards).
 template <int KEY_BITS>
-__device__ int warp_hist_select_sort(SelShared& s, const uint64_t* c, int n, int k, const uint32_t* h,
+__device__ int warp_hist_select_sort(SelShared& s, const uint64_t* c, int n, int k, uint32_t* h,
                                      uint32_t hbase, uint64_t (&val)[4]) {
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
@@ -852,31 +855,45 @@ __device__ int warp_hist_select_sort(SelShared& s, const uint64_t* c, int n, int
     base += __popc(tb);
     __syncwarp();
   }
-  // rank of each of the k among them, then into rank order
-  uint64_t x[4];
-  int r[4];
+  // bin b (>= the cut's bin) starts at the count of selected candidates in
+  // higher bins: the cut's bin holds `need` of its ties, higher bins all of theirs
+  {
+    uint32_t acc = excl;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    x[j] = j * 32 + lane < k ? s.ssel[j * 32 + lane] : 0ull;
-    r[j] = 0;
-  }
-  const uint4* s4 = reinterpret_cast<const uint4*>(s.ssel);
-  for (int i = 0; i < k / 2; ++i) {
-    const uint4 w = s4[i];
-    const uint64_t y0 = (static_cast<uint64_t>(w.y) << 32) | w.x;
-    const uint64_t y1 = (static_cast<uint64_t>(w.w) << 32) | w.z;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) r[j] += (y0 > x[j]) + (y1 > x[j]);
-  }
-  if (k & 1) {
-    const uint64_t y = s.ssel[k - 1];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) r[j] += y > x[j];
+    for (int j = 0; j < 8; ++j) {
+      const int bb = 255 - 8 * lane - j;
+      if (bb >= bin) h[bb] = acc;
+      acc += hv[j];
+    }
   }
   __syncwarp();
+  // group the k by bin: each takes the next slot of its bin
+  uint64_t* grp = reinterpret_cast<uint64_t*>(s.shist);
+  uint64_t x[4];
+  int xb[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    if (j * 32 + lane < k) s.ssel[r[j]] = x[j];
+  for (int j = 0; j < 4; ++j) {
+    const int r = j * 32 + lane;
+    x[j] = 0ull;
+    xb[j] = -1;
+    if (r < k) {
+      x[j] = s.ssel[r];
+      xb[j] = static_cast<int>(min(static_cast<uint32_t>(x[j] >> 32) - hbase, 255u));
+      grp[atomicAdd(&h[xb[j]], 1u)] = x[j];
+    }
+  }
+  __syncwarp();
+  // inside its bin [end of the next higher bin, end of its own), a candidate's
+  // place is the count of larger composites there
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (xb[j] < 0) continue;
+    const int lo = xb[j] == 255 ? 0 : static_cast<int>(h[xb[j] + 1]);
+    const int hi = static_cast<int>(h[xb[j]]);
+    int rk = 0;
+    for (int i = lo; i < hi; ++i) rk += grp[i] > x[j];
+    s.ssel[lo + rk] = x[j];
+  }
   __syncwarp();
   warp_load<4>(s.ssel, k, val);
   __syncwarp();
@@ -894,6 +911,7 @@ __device__ void expand_epilogue(const uint64_t (&val)[4], const SelArgs& a, int6
   float l[4], e[4], eT[4];
   const float lmax = key_value<T>(static_cast<uint32_t>(__shfl_sync(FULL, val[0], 0) >> 32));
   if (lane == 0 && !(lmax < INFINITY)) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
+  const bool unit_T = a.temperature == 1.0f;  // then the tempered weights are the untempered ones
   float se = 0.0f, seT = 0.0f, te = 0.0f, teT = 0.0f;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -902,7 +920,7 @@ __device__ void expand_epilogue(const uint64_t (&val)[4], const SelArgs& a, int6
     l[j] = key_value<T>(static_cast<uint32_t>(val[j] >> 32));
     const float dd = l[j] - lmax;
     e[j] = valid ? expf(dd) : 0.0f;
-    eT[j] = valid ? expf(dd / a.temperature) : 0.0f;
+    eT[j] = unit_T ? e[j] : (valid ? expf(dd / a.temperature) : 0.0f);
     se += e[j];
     seT += eT[j];
     if (valid && r >= a.m) {
@@ -910,10 +928,14 @@ __device__ void expand_epilogue(const uint64_t (&val)[4], const SelArgs& a, int6
       teT += eT[j];
     }
   }
-  se = warp_sum(se);
-  seT = warp_sum(seT);
-  te = warp_sum(te);
-  teT = warp_sum(teT);
+  // the four sums, their butterfly steps interleaved
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    se += __shfl_xor_sync(FULL, se, o);
+    seT += __shfl_xor_sync(FULL, seT, o);
+    te += __shfl_xor_sync(FULL, te, o);
+    teT += __shfl_xor_sync(FULL, teT, o);
+  }
   int32_t* sid = a.sup_id + out_row * a.sup_stride;
   float* sq = a.sup_q + out_row * a.sup_stride;
   float* sqT = a.sup_qT + out_row * a.sup_stride;
@@ -928,25 +950,35 @@ __device__ void expand_epilogue(const uint64_t (&val)[4], const SelArgs& a, int6
   }
   int probe = -1;
   if (a.draw_probe && a.m < n_sup && teT > 0.0f) {
+    // inclusive scans of the tempered tail weights of the four rank blocks,
+    // interleaved, then the blocks' carries
     const float target = a.u_probe[in_row] * teT;
+    float x[4], incl[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = j * 32 + lane;
+      x[j] = (r < n_sup && r >= a.m) ? eT[j] : 0.0f;
+      incl[j] = x[j];
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float y = __shfl_up_sync(FULL, incl[j], o);
+        if (lane >= o) incl[j] += y;
+      }
+    }
     float carry = 0.0f;
     int last = -1;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int r = j * 32 + lane;
       const bool tl = r < n_sup && r >= a.m;
-      const float x = tl ? eT[j] : 0.0f;
-      float incl = x;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(FULL, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const unsigned hit = __ballot_sync(FULL, tl && target < carry + incl);
+      const unsigned hit = __ballot_sync(FULL, tl && target < carry + incl[j]);
       if (probe < 0 && hit) probe = j * 32 + __ffs(hit) - 1;
-      const unsigned pos = __ballot_sync(FULL, tl && x > 0.0f);
+      const unsigned pos = __ballot_sync(FULL, tl && x[j] > 0.0f);
       if (pos) last = j * 32 + 31 - __clz(pos);
-      carry += __shfl_sync(FULL, incl, 31);
+      carry += __shfl_sync(FULL, incl[j], 31);
     }
     if (probe < 0) probe = last;
   }
