@@ -50,7 +50,8 @@ class c_tree(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "node_token", "node_parent", "node_depth", "node_kind", "node_slot", "node_exp_row", "node_score",
         "n_nodes", "sup_id", "sup_q", "sup_qT", "sup_z", "sup_zT", "probe_pos")] + [
-        ("n_rows", ctypes.c_int32), ("max_nodes", ctypes.c_int32), ("sup_stride", ctypes.c_int32)]
+        ("n_rows", ctypes.c_int32), ("max_nodes", ctypes.c_int32), ("sup_stride", ctypes.c_int32),
+        ("sched", ctypes.c_void_p)]
 
 
 def _load():
@@ -156,6 +157,8 @@ class TreeBuffers:
         self.sup_q = mk(r + (self.sup_stride,), f32)
         self.sup_qT = mk(r + (self.sup_stride,), f32)
         self.sup_z, self.sup_zT, self.probe_pos = mk(r, f32), mk(r, f32), mk(r, i32)
+        # row counter of the support selection (zero; every call leaves it zero)
+        self.sched = torch.zeros((2,), dtype=i32, device=device)
 
     def c(self) -> c_tree:
         if getattr(self, "_c", None) is None:
@@ -163,6 +166,7 @@ class TreeBuffers:
             for name, _ in c_tree._fields_[:14]:
                 setattr(t, name, getattr(self, name).data_ptr())
             t.n_rows, t.max_nodes, t.sup_stride = self.n_rows, self.max_nodes, self.sup_stride
+            t.sched = self.sched.data_ptr()
             self._c = t
         return self._c
 

@@ -138,6 +138,7 @@ int spec_tree_select_expand(const spec_tree_params* p, int B, int V, int dtype, 
   L.status = status;
   L.num_sms = num_sms_of_current_device();
   L.ctas_per_sm = 2;
+  L.sched = tree->sched;
   if (L.num_sms <= 0) return SPEC_TREE_E_CUDA;
   return launch_select(dtype, L, as_stream(stream)) == cudaSuccess ? SPEC_TREE_OK : SPEC_TREE_E_CUDA;
 }
@@ -225,6 +226,7 @@ int spec_tree_layer(const spec_tree_params* p, int B, int V, int layer, int dtyp
   S.status = status;
   S.num_sms = num_sms_of_current_device();
   S.ctas_per_sm = 2;
+  S.sched = tree->sched;
   if (S.num_sms <= 0) return SPEC_TREE_E_CUDA;
   if (launch_select(dtype, S, as_stream(stream)) != cudaSuccess) return SPEC_TREE_E_CUDA;
   st::RankLaunch L;

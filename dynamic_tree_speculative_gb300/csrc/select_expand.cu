@@ -76,6 +76,7 @@ constexpr int SX_GLIST = 1024;                   // gather list: (chunk, thread)
 constexpr int SX_QCH = 16;                       // queue path: rows of up to this many chunks
 constexpr int SX_QW = 56;                        // queue path: vectors queued per warp and row
 constexpr uint32_t SX_QMARGIN = 16;              // queue threshold: this many key steps below a recent cut
+constexpr int SX_ANN = 8;                        // rows announced by the producer ahead of the consumers
 // what the selector receives with a row's candidates
 constexpr int SX_HIST = 1;     // every element >= hbase, with its key histogram khist
 constexpr int SX_SORTED = 2;   // exactly the top-|S|, in order
@@ -132,6 +133,8 @@ struct SelShared {
   uint32_t last_cut;   // key of the |S|-th largest of the selector's latest row (0: none yet)
   uint32_t thr_row[2]; // queue threshold of the rows of each parity (0: no queue)
   int qbad;            // 1 + the last row whose queue failed (NaN, full queue)
+  int64_t ann_row[SX_ANN];   // rows announced by the producer, in this CTA's order (-1: no more)
+  uint64_t ann_bar[SX_ANN];  // one arrival per announcement
 };
 
 // A candidate buffer and its fill count.
@@ -603,6 +606,7 @@ struct SelArgs {
   int32_t* probe_pos;
   int sup_stride;
   uint32_t* status;
+  unsigned int* sched;  // [2]: next row to hand out, producers done (NULL: static order)
 };
 
 // Robust selection of a row straight from global memory, in id order: keep
@@ -1003,7 +1007,17 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
   const int nch = static_cast<int>((tma_bytes + SX_CHUNK - 1) / SX_CHUNK);
   const int tail_begin = static_cast<int>(tma_bytes / 16) * VEC;
   const int last_nvec = nch > 0 ? static_cast<int>((tma_bytes - static_cast<int64_t>(nch - 1) * SX_CHUNK) / 16) : 0;
-  const int64_t my_rows = a.total_rows > blockIdx.x ? (a.total_rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  // Rows reach a CTA in the order its producer claims them: its first row is
+  // blockIdx.x, later ones come from the shared counter a.sched (dynamic
+  // balance: a CTA that runs ahead takes more rows), or blockIdx.x +
+  // gridDim.x, ... without one; the producer announces each to the
+  // consumers.  Rows without a whole chunk have no producer and take the
+  // static order.
+  const auto static_row = [&](int64_t lr) -> int64_t {
+    const int64_t r = static_cast<int64_t>(blockIdx.x) + lr * gridDim.x;
+    return r < a.total_rows ? r : -1;
+  };
+  const bool announced = nch > 0;
 
   if (tid == 0) {
     for (int i = 0; i < SX_STAGES; ++i) {
@@ -1013,6 +1027,11 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.cfull[i], 1);
       mbar_init(&s.cempty[i], 1);
+      s.cand_row[i] = -1;
+    }
+    for (int i = 0; i < SX_ANN; ++i) {
+      mbar_init(&s.ann_bar[i], 1);
+      s.ann_row[i] = -1;
     }
     fence_mbar_init();
     s.timeout = 0;
@@ -1031,11 +1050,12 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
     // Rows in order: wait for the streamers' candidates, select the exact
     // top-|S|, sort, expand, write the outputs, hand the buffer back.
     bool timed_out = false;
-    for (int64_t lr = 0; lr < my_rows; ++lr) {
+    for (int64_t lr = 0;; ++lr) {
       const int q = static_cast<int>(lr & 1);
       if (!mbar_wait(&s.cfull[q], static_cast<uint32_t>((lr >> 1) & 1))) timed_out = true;
-      const int n = s.count[q];
       const int64_t out_row = s.cand_row[q], in_row = s.cand_in[q];
+      if (out_row < 0) break;  // the consumers have no more rows
+      const int n = s.count[q];
       uint64_t val[4];
       int n_sup;
       const int mode = s.mode[q];
@@ -1074,10 +1094,27 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
       uint32_t phase = 0;
       int64_t g = 0;
       bool timed_out = false;
-      int64_t b = blockIdx.x / a.rows_used, e = blockIdx.x % a.rows_used;
-      for (int64_t lr = 0; lr < my_rows; ++lr) {
+      // a CTA's first row is its own index (the grid never exceeds the rows),
+      // so the stream starts without a round trip; the counter hands out the rest
+      const auto claim = [&](int64_t lr) -> int64_t {
+        if (a.sched == nullptr || lr == 0) return static_row(lr);
+        const int64_t r = static_cast<int64_t>(gridDim.x) + atomicAdd(a.sched, 1u);
+        return r < a.total_rows ? r : -1;
+      };
+      // the next row is claimed three chunks before this row's end: late
+      // enough that every CTA has its first row by then, early enough that
+      // the claim's round trip hides behind the chunks still in the ring
+      const int claim_at = nch > 3 ? nch - 3 : 0;
+      int64_t next = claim(0);
+      for (int64_t lr = 0;; ++lr) {
+        const int64_t r = next;
+        s.ann_row[lr & (SX_ANN - 1)] = r;
+        mbar_arrive(&s.ann_bar[lr & (SX_ANN - 1)]);  // releases the announcement
+        if (r < 0) break;
+        const int64_t b = r / a.rows_used, e = r - b * a.rows_used;
         const uint8_t* row = a.logits + (b * a.in_rows + e) * a.row_bytes_stride;
         for (int c = 0; c < nch; ++c, ++g) {
+          if (c == claim_at) next = claim(lr + 1);
           // stage reuse: wait until every consumer warp released its last use
           if (g >= SX_STAGES && !mbar_wait(&s.empty[st], phase ^ 1u)) timed_out = true;
           const int64_t off = static_cast<int64_t>(c) * SX_CHUNK;
@@ -1089,10 +1126,14 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
             phase ^= 1u;
           }
         }
-        e += gridDim.x;  // next row of this CTA, without dividing
-        while (e >= a.rows_used) {
-          e -= a.rows_used;
-          ++b;
+      }
+      if (a.sched != nullptr) {
+        // the last producer to stop claiming leaves the counter at zero for
+        // the next launch (no claim of this launch can follow)
+        __threadfence();
+        if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
+          atomicExch(a.sched, 0u);
+          atomicExch(a.sched + 1, 0u);
         }
       }
       if (timed_out) s.timeout = 1;
@@ -1104,18 +1145,34 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
   bool nonfinite = false, overflow = false, p2over = false;
   int st = 0;
   uint32_t phase = 0;
-  int64_t b = blockIdx.x / a.rows_used, e = blockIdx.x % a.rows_used;
   const int jth = (a.S + SX_CWARPS - 1) / SX_CWARPS;
   const bool tabled = nch <= SX_TBL;  // longer rows take the robust path
   const bool has_vec = nch > 1 || tid < last_nvec;  // this thread sees at least one whole vector
   const bool queue_rows = sizeof(T) == 2 && nch <= SX_QCH;  // rows that can take the queue path
   const unsigned lt = (1u << lane) - 1u;
-  for (int64_t lr = 0; lr < my_rows; ++lr) {
+  for (int64_t lr = 0;; ++lr) {
+    // candidate buffer of this row (the selector may still drain it from two rows ago)
+    const int q = static_cast<int>(lr & 1);
+    int64_t r;
+    if (announced) {
+      if (!mbar_wait(&s.ann_bar[lr & (SX_ANN - 1)], static_cast<uint32_t>((lr >> 3) & 1))) s.timeout = 1;
+      r = s.ann_row[lr & (SX_ANN - 1)];
+    } else {
+      r = static_row(lr);
+    }
+    if (r < 0) {
+      // no more rows: tell the selector, once it is done with the buffer
+      if (tid == 0) {
+        if (lr >= 2 && !mbar_wait(&s.cempty[q], static_cast<uint32_t>(((lr >> 1) - 1) & 1))) s.timeout = 1;
+        s.cand_row[q] = -1;
+        mbar_arrive(&s.cfull[q]);
+      }
+      break;
+    }
+    const int64_t b = r / a.rows_used, e = r - b * a.rows_used;
     const int64_t out_row = b * a.n_rows + a.sup_row0 + e;
     const int64_t in_row = b * a.in_rows + e;
     const uint8_t* row = a.logits + in_row * a.row_bytes_stride;
-    // candidate buffer of this row (the selector may still drain it from two rows ago)
-    const int q = static_cast<int>(lr & 1);
     const CandBuf cb{s.cand[q], &s.count[q], SX_CAP};
     uint32_t* const kh = s.khist[q];  // zeroed by the selector once it is done with the buffer
 
@@ -1338,11 +1395,6 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
       s.cand_in[q] = in_row;
       mbar_arrive(&s.cfull[q]);
     }
-    e += gridDim.x;
-    while (e >= a.rows_used) {
-      e -= a.rows_used;
-      ++b;
-    }
   }
   if (s.timeout && tid == 0) set_status(a.status, SPEC_TREE_S_TIMEOUT);
   if (nonfinite) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
@@ -1375,6 +1427,9 @@ cudaError_t launch_select_expand(int dtype, const SelLaunch& L, cudaStream_t str
   if (a.total_rows == 0) return cudaSuccess;
   const size_t smem = sizeof(SelShared);
   const int64_t grid = min64(a.total_rows, static_cast<int64_t>(L.num_sms) * L.ctas_per_sm);
+  // rows on demand once a CTA has several; with one or two rows a CTA the
+  // fixed order spreads the second rows evenly over the SMs
+  a.sched = a.total_rows >= 4 * grid ? reinterpret_cast<unsigned int*>(L.sched) : nullptr;
   if (dtype == SPEC_TREE_BF16) {
     cudaError_t err = cudaFuncSetAttribute(select_expand_kernel<__nv_bfloat16>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -30,6 +30,7 @@ struct SelLaunch {
   uint32_t* status;
   int num_sms;
   int ctas_per_sm;
+  int32_t* sched;  // the tree's row counter (or NULL)
 };
 
 struct RankLaunch {

@@ -142,6 +142,13 @@ typedef struct spec_tree_params {
  *   untempered / tempered truncated softmax; sup_z / sup_zT tail masses over
  *   ranks m..|S|-1; probe_pos rank of the probe in S (-1: no probe).
  *   `sup_stride` is the per-row capacity of sup_id/sup_q/sup_qT (>= |S|).
+ * Row schedule (optional, may be NULL):
+ *   sched        device uint32[2], zero before the first call that uses it.
+ *                The support selection hands draft rows to its CTAs on demand
+ *                from this counter (a CTA that runs ahead takes more rows, so
+ *                they finish together) and leaves it at zero again when it
+ *                ends.  NULL: rows are dealt to the CTAs in a fixed order.
+ *                Calls that overlap on the GPU must not share one counter.
  */
 typedef struct spec_tree_t {
   int32_t* node_token;
@@ -161,6 +168,7 @@ typedef struct spec_tree_t {
   int32_t n_rows;
   int32_t max_nodes;
   int32_t sup_stride;
+  int32_t* sched;
 } spec_tree_t;
 
 /* Draft rows one tree consumes: 1 + (depth-1)*W (top-R), at most R + 1 (SMART). */

@@ -86,6 +86,8 @@ def run_gpu(case: Case, target=None, device="cuda"):
         host.update(accept_len=out.accept_len.cpu().numpy(), out_tok=out.out_tok.cpu().numpy(),
                     out_node=out.out_node.cpu().numpy(), margins=out.margins.cpu().numpy())
     host["status"] = int(status.item())
+    # the support selection hands rows out from the tree's counter and leaves it at zero
+    assert tree.sched.cpu().tolist() == [0, 0], tree.sched
     return host
 
 
