@@ -161,3 +161,31 @@ def test_layer_static_host_checks(binding):
     smart = binding.Params(K=8, m=1, W=8, depth=8, R=60, builder=binding.BUILDER_SMART)
     t.n_rows = 61
     assert call(0, 0, params=smart) == binding.E_PARAM                    # top-R builder only
+
+
+def test_binding_structs_match_the_c_header(binding, tmp_path):
+    """The ctypes mirrors of spec_tree_params and spec_tree_t have the header's sizes and field offsets."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = {"spec_tree_params": binding.c_params, "spec_tree_t": binding.c_tree}
+    # the C names of the binding's fields (the binding spells lambda as lam)
+    cname = {"lam": "lambda"}
+    src = ["#include <stddef.h>", "#include <stdio.h>", '#include "spec_tree.h"', "int main(void) {"]
+    for st, cls in fields.items():
+        src.append(f'  printf("{st} %zu\\n", sizeof({st}));')
+        for f, _ in cls._fields_:
+            c = cname.get(f, f)
+            src.append(f'  printf("{st}.{f} %zu\\n", offsetof({st}, {c}));')
+    src += ["  return 0;", "}"]
+    c_file, exe = tmp_path / "abi.c", tmp_path / "abi"
+    c_file.write_text("\n".join(src) + "\n")
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(c_file), "-o", str(exe)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                       check=True).stdout.splitlines())
+    for st, cls in fields.items():
+        assert int(got[st]) == ctypes.sizeof(cls), st
+        for f, _ in cls._fields_:
+            assert int(got[f"{st}.{f}"]) == getattr(cls, f).offset, (st, f)
