@@ -1,5 +1,5 @@
 // Support selection + dual-identity expansion for supports of 129 to 1024
-// tokens (sm_103a): one CTA of 1024 threads per draft row.
+// tokens (sm_103a): one CTA of SW_THREADS threads per draft row, two per SM.
 //
 // RheoSampling notes, Method / Key design 1 (the support-size ablation:
 // top-128, 256, 512, 1024, and the dense support when it is the whole
@@ -11,7 +11,7 @@
 //     four for f32), each pass counting the elements that match the digits
 //     fixed so far into per-warp histograms.  It ends with the |S|-th largest
 //     key t and the number of elements equal to t still needed.
-//   collect: one more pass, in rounds of 1024 consecutive vectors (token-id
+//   collect: one more pass, in rounds of SW_THREADS consecutive vectors (token-id
 //     order), appends every element above t and, of the elements equal to t,
 //     the smallest ids (a block scan ranks them within the round): exactly
 //     |S| (key, ~id) composites.
@@ -33,9 +33,10 @@
 
 namespace st {
 
-constexpr int SW_THREADS = 1024;
+constexpr int SW_THREADS = 512;
 constexpr int SW_WARPS = SW_THREADS / 32;
 constexpr int SW_MAX_S = SPEC_TREE_MAX_SUPPORT;
+constexpr int SW_RPT = (SW_MAX_S + SW_THREADS - 1) / SW_THREADS;  // support ranks a thread owns in the epilogue
 constexpr int SW_TBL = 32768;  // table path: rows of up to 32768 vectors (256K bf16 / 128K f32 tokens)
 constexpr int SW_CAP = 2048;   // table path: candidates
 
@@ -48,7 +49,7 @@ struct WideShared {
   uint32_t list[SW_CAP];            // table path: vectors to gather
   uint32_t hist[256];
   float red[4][SW_WARPS];         // block reductions
-  float scan[SW_WARPS];           // block scan of the tail weights
+  float scan[SW_RPT][SW_WARPS];   // block scans of the tail weights, one per rank block
   int tie_scan[SW_WARPS];         // block scan of tie counts
   int n_cand;
   int n_list;
@@ -61,13 +62,13 @@ struct WideShared {
 };
 
 // Calls f(key, id) for every element of the row that thread tid owns: the
-// 16-byte vectors tid, tid + 1024, ... (loaded four at a time, so that four
-// loads are in flight; two CTAs of 1024 threads share an SM, 32 registers a
-// thread) and then the scalar tail element nvec * VEC + tid, if any.
+// 16-byte vectors tid, tid + SW_THREADS, ... (loaded eight at a time, so that
+// eight loads are in flight) and then the scalar tail element
+// nvec * VEC + tid, if any.
 template <typename T, typename F>
 __device__ __forceinline__ void for_each_elem(const uint8_t* row, int V, int nvec, bool& nonfinite, F f) {
   using E = Elem<T>;
-  constexpr int VEC = E::VEC, U = 4;
+  constexpr int VEC = E::VEC, U = 8;
   const int tid = threadIdx.x;
   for (int v0 = tid; v0 < nvec; v0 += U * SW_THREADS) {
     uint4 v[U];
@@ -185,7 +186,7 @@ __device__ __forceinline__ int block_excl_scan(WideShared& s, int x, int* total)
 
 // Appends to s.cand every element above the prefix and, unless exact, the
 // `need` smallest ids among the elements equal to it (exact: every element
-// equal to it).  Rounds of 1024 consecutive vectors keep id order for ties.
+// equal to it).  Rounds of SW_THREADS consecutive vectors keep id order for ties.
 template <typename T>
 __device__ void collect_row(WideShared& s, const uint8_t* row, int V, int nvec, uint32_t prefix, uint32_t pmask,
                             int need, bool exact, bool& nonfinite) {
@@ -354,7 +355,7 @@ __device__ __forceinline__ uint32_t vec_max_key16<float>(const uint4& v, bool& n
 // (ties); block-uniform.
 template <typename T>
 __device__ bool table_select(WideShared& s, const uint8_t* row, int V, int nvec, int S, bool& nonfinite) {
-  constexpr int VEC = Elem<T>::VEC, U = 4;
+  constexpr int VEC = Elem<T>::VEC, U = 8;
   const int tid = threadIdx.x;
   for (int v0 = tid; v0 < nvec; v0 += U * SW_THREADS) {
     uint4 v[U];
@@ -434,23 +435,33 @@ __device__ bool table_select(WideShared& s, const uint8_t* row, int V, int nvec,
 }
 
 // Softmaxes, tail masses and the probe of a row from its sorted support
-// s.cand[0..n): thread r owns support rank r.  RheoSampling Key design 2; the
-// probe is the first tail rank k with u * z_T < sum_{j=m..k} q_T(j), on
-// unnormalised weights (the last tail rank with weight if rounding leaves
-// none).
+// s.cand[0..n): thread t owns support ranks t, t + SW_THREADS, ...
+// RheoSampling Key design 2; the probe is the first tail rank k with
+// u * z_T < sum_{j=m..k} q_T(j), on unnormalised weights (the last tail rank
+// with weight if rounding leaves none).
 template <typename T>
 __device__ void wide_epilogue(WideShared& s, const SelLaunch& a, int64_t out_row, int64_t in_row, int n) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool valid = tid < n;
-  const uint64_t x = valid ? s.cand[tid] : 0ull;
   const float lmax = key_value<T>(static_cast<uint32_t>(s.cand[0] >> 32));
   if (tid == 0 && !(lmax < INFINITY)) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
-  const float l = key_value<T>(static_cast<uint32_t>(x >> 32));
-  const float dd = l - lmax;
-  const float e = valid ? expf(dd) : 0.0f;
-  const float eT = valid ? expf(dd / a.temperature) : 0.0f;
-  const bool tail = valid && tid >= a.m;
-  float v4[4] = {e, eT, tail ? e : 0.0f, tail ? eT : 0.0f};
+  uint64_t x[SW_RPT];
+  float e[SW_RPT], eT[SW_RPT];
+  float v4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int k = 0; k < SW_RPT; ++k) {
+    const int r = tid + k * SW_THREADS;
+    const bool valid = r < n;
+    x[k] = valid ? s.cand[r] : 0ull;
+    const float dd = key_value<T>(static_cast<uint32_t>(x[k] >> 32)) - lmax;
+    e[k] = valid ? expf(dd) : 0.0f;
+    eT[k] = valid ? expf(dd / a.temperature) : 0.0f;
+    v4[0] += e[k];
+    v4[1] += eT[k];
+    if (valid && r >= a.m) {
+      v4[2] += e[k];
+      v4[3] += eT[k];
+    }
+  }
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     v4[k] = warp_sum(v4[k]);
@@ -466,28 +477,48 @@ __device__ void wide_epilogue(WideShared& s, const SelLaunch& a, int64_t out_row
 #pragma unroll
     for (int k = 0; k < 4; ++k) sum[k] += s.red[k][w];
   const float se = sum[0], seT = sum[1], te = sum[2], teT = sum[3];
-  if (valid) {
-    a.sup_id[out_row * a.sup_stride + tid] = static_cast<int32_t>(~static_cast<uint32_t>(x));
-    a.sup_q[out_row * a.sup_stride + tid] = e / se;
-    a.sup_qT[out_row * a.sup_stride + tid] = eT / seT;
+#pragma unroll
+  for (int k = 0; k < SW_RPT; ++k) {
+    const int r = tid + k * SW_THREADS;
+    if (r < n) {
+      a.sup_id[out_row * a.sup_stride + r] = static_cast<int32_t>(~static_cast<uint32_t>(x[k]));
+      a.sup_q[out_row * a.sup_stride + r] = e[k] / se;
+      a.sup_qT[out_row * a.sup_stride + r] = eT[k] / seT;
+    }
   }
   const bool draw = a.draw_probe && a.m < n && teT > 0.0f;  // block-uniform
   if (draw) {
-    // inclusive scan of the tail weights in rank order
-    const float w = tail ? eT : 0.0f;
-    float incl = w;
+    // inclusive scans of the tail weights in rank order, one per rank block
+    float w[SW_RPT], incl[SW_RPT];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(FULL, incl, o);
-      if (lane >= o) incl += y;
+    for (int k = 0; k < SW_RPT; ++k) {
+      const int r = tid + k * SW_THREADS;
+      w[k] = (r < n && r >= a.m) ? eT[k] : 0.0f;
+      incl[k] = w[k];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(FULL, incl[k], o);
+        if (lane >= o) incl[k] += y;
+      }
+      if (lane == 31) s.scan[k][warp] = incl[k];
     }
-    if (lane == 31) s.scan[warp] = incl;
     __syncthreads();
-    float before = 0.0f;
-    for (int k = 0; k < warp; ++k) before += s.scan[k];
     const float target = a.u_probe[in_row] * teT;
-    if (tail && target < before + incl) atomicMin(&s.probe, tid);
-    if (tail && w > 0.0f) atomicMax(&s.last_pos, tid);
+    float carry = 0.0f;
+#pragma unroll
+    for (int k = 0; k < SW_RPT; ++k) {
+      const int r = tid + k * SW_THREADS;
+      float before = carry, block = 0.0f;
+      for (int j = 0; j < SW_WARPS; ++j) {
+        const float y = s.scan[k][j];
+        if (j < warp) before += y;
+        block += y;
+      }
+      const bool tail = r < n && r >= a.m;
+      if (tail && target < before + incl[k]) atomicMin(&s.probe, r);
+      if (tail && w[k] > 0.0f) atomicMax(&s.last_pos, r);
+      carry += block;
+    }
   }
   __syncthreads();
   if (tid == 0) {
