@@ -54,6 +54,7 @@ struct VerShared {
   float p_sup[SPEC_TREE_MAX_SUPPORT];          // p at support ranks of the node's draft row
   float qt_sup[SPEC_TREE_MAX_SUPPORT];         // q~_T at support ranks (0 off the tail)
   float w_sup[SPEC_TREE_MAX_SUPPORT];          // residual at support ranks
+  float uv_lv[SPEC_TREE_MAX_SUPPORT];          // the level's accept uniforms, loaded at its start
   float all_m[2][VER_MAX_SLICES];              // leader, per level parity: every slice's maximum logit
   float all_s[2][VER_MAX_SLICES];              //   and sum of exp2((t - slice max) * c)
   uint64_t stats_bar[2];                       // leader: all slices of the level have arrived
@@ -394,6 +395,9 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
     const uint32_t wpar = static_cast<uint32_t>((level >> 1) & 1);
     const uint8_t* row = tgt + (nb + node) * row_bytes;
     const int er = leader && level < D ? s.nd_exp_row[node] : -1;
+    // the level's accept uniforms, for thread 0's decisions after the barriers
+    // below (its reads of the previous level's are done)
+    if (er >= 0 && tid < K) s.uv_lv[tid] = L.u_verify[(static_cast<int64_t>(b) * D + level) * K + tid];
     float wm, ws;
     slice_stats<T>(row, V, cr * VER_WARPS + warp, NS, c, nonfinite, wm, ws);
     // target logits of the support tokens, landing while the slices arrive
@@ -452,7 +456,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
         const bool residual = probe_node >= 0 && !probe_last;
         float mn = 0.0f;
         if (tid < S) {
-          const float p = expf((t_sup - M) / Tmp) * invZp;
+          const float p = expf(Tmp == 1.0f ? t_sup - M : (t_sup - M) / Tmp) * invZp;
           const float qt = (tid >= m && zT > 0.0f) ? sup_qt / zT : 0.0f;
           s.p_sup[tid] = p;
           s.qt_sup[tid] = qt;
@@ -463,7 +467,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
         if (lane == 0) s.red[warp] = mn;
         __syncthreads();
         if (tid == 0) {
-          const float* uv = L.u_verify + (static_cast<int64_t>(b) * D + level) * K;
+          const float* uv = s.uv_lv;
           int j = 0, accepted = -1;
           float Zr = 1.0f;
           bool empty = false;
