@@ -75,6 +75,7 @@ struct VerShared {
   int bonus_last;
   int bonus_slice;
   float bonus_target;  // target mass relative to the start of the bonus slice
+  float u_bonus;       // the tree's bonus uniform, loaded at the start
 };
 
 // 2^x on the special-function unit (PTX ex2.approx.ftz: a few ulp; results
@@ -362,6 +363,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
       s.nd_exp_row[i] = t.node_exp_row[nb + i];
       s.nd_token[i] = t.node_token[nb + i];
     }
+    if (tid == 0) s.u_bonus = L.u_bonus[b];
   }
   cluster.sync();  // barriers initialised cluster-wide before any remote arrival
   bool nonfinite = false, timed_out = false;
@@ -578,7 +580,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
       // slice masses of w in id order; the first slice whose cumulative mass
       // exceeds u * Zr holds the bonus token
       constexpr int PER = (NS + 31) / 32;
-      const float target = L.u_bonus[b] * s.Zr;
+      const float target = s.u_bonus * s.Zr;
       float mass[PER], run = 0.0f;
       int last_l = -1;
 #pragma unroll
