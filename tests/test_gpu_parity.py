@@ -191,6 +191,15 @@ def test_rows_whose_cut_jumps():
     assert exm <= 0.1 * len(sample) + 1
 
 
+def test_queue_path_with_ragged_vocabulary():
+    """Many rows per CTA (the predicted-threshold queue path and rows handed out on demand) on a
+    vocabulary that is not a multiple of the vector width: the elements past the last whole vector
+    join the candidates through their own branch."""
+    wl = WL.WORKLOADS["vicuna"].with_(B=64, V=32001)
+    out = parity.run_parity(wl, 19, sample=[0, 13, 29, 47, 63], row_stride=32008)
+    _report("queue_ragged", out)
+
+
 def test_verify_reads_target_rows_from_pinned_host_memory():
     """Target logits left in pinned host memory (unified addressing): verify reads the accepted
     path's rows over the host link and returns exactly what it returns from HBM."""
