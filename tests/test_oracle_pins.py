@@ -36,7 +36,9 @@ def test_bf16_bits_decode_matches_torch():
 
 # ----------------------------------------------------------- truncation ---
 
-@pytest.mark.parametrize("V,size", [(40, 128), (300, 128), (1000, 128), (257, 7)])
+@pytest.mark.parametrize("V,size", [(40, 128), (300, 128), (1000, 128), (257, 7),
+                                    # the support-size ablation, and the dense support of a small vocabulary
+                                    (3000, 256), (3000, 512), (5000, 1024), (700, 1024)])
 def test_support_is_brute_force_top_by_logit_then_id(V, size):
     rng = np.random.default_rng(V)
     for _ in range(20):
