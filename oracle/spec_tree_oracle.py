@@ -70,24 +70,68 @@ class Params:
 
 
 class Margins:
-    """Smallest margin seen per decision kind, and the count of near-ties."""
+    """Smallest margin seen per decision kind, the count of near-ties, and where each one sits.
+
+    `ties` lists every near-tie as (kind, where, margin).  `where` names the
+    decision: ("probe", row) for a probe draw, ("order", layer, i) for the gap
+    between positions i and i+1 of a ranked layer (layer "final" for the top-R
+    cut), ("smart", layer, creation key) for a keep test, ("accept", level, j)
+    for the j-th accept test of a verification level, ("bonus", level) for the
+    bonus draw.
+    """
 
     def __init__(self):
         self.min = {}
         self.near = 0
+        self.ties = []
 
-    def add(self, kind: str, value: float, threshold: float):
+    def add(self, kind: str, value: float, threshold: float, where=None):
         value = abs(float(value))
         if kind not in self.min or value < self.min[kind]:
             self.min[kind] = value
         if value < threshold:
             self.near += 1
+            self.ties.append((kind, where, value))
 
     def merge(self, other: "Margins"):
         for k, v in other.min.items():
             if k not in self.min or v < self.min[k]:
                 self.min[k] = v
         self.near += other.near
+        self.ties.extend(other.ties)
+
+
+class ReplayRefused(AssertionError):
+    """A decision offered for replay was not a near-tie of this oracle."""
+
+
+@dataclasses.dataclass
+class Replay:
+    """Decisions adopted from another implementation (the replay mode of a parity check).
+
+    Where two implementations take a floating-point decision on opposite sides
+    of a near-tie, the oracle can adopt the other side's choice and go on, so
+    that everything downstream is still compared.  It adopts a choice only
+    where its own margin for that decision is a near-tie (below the thresholds
+    above) and raises ReplayRefused otherwise:
+
+      probe[row]          = probe rank drawn for a draft row;
+      before              = set of (a, b) creation keys, a ranked before b;
+      keep[key]           = SMART keep decision of a candidate;
+      accept[(level, j)]  = outcome of the j-th accept test of a level;
+      bonus[level]        = bonus token drawn at a level.
+
+    `adopted` lists the decisions that changed the oracle's result.
+    """
+    probe: dict = dataclasses.field(default_factory=dict)
+    before: set = dataclasses.field(default_factory=set)
+    keep: dict = dataclasses.field(default_factory=dict)
+    accept: dict = dataclasses.field(default_factory=dict)
+    bonus: dict = dataclasses.field(default_factory=dict)
+    adopted: list = dataclasses.field(default_factory=list)
+
+    def __bool__(self):
+        return bool(self.probe or self.before or self.keep or self.accept or self.bonus)
 
 
 # --------------------------------------------------------------------------
@@ -145,7 +189,21 @@ class Expansion:
     margins: Margins
 
 
-def expand_row(row, p: Params, u_probe: float, force_probe_pos: Optional[int] = None) -> Expansion:
+def _draw_accepts(cum: np.ndarray, weights: np.ndarray, target: float, k: int) -> bool:
+    """Whether index k is a choice of the inverse-CDF draw `target` within MASS_MARGIN.
+
+    k is a valid choice of another implementation when its own cumulative
+    interval [cum[k-1], cum[k]) holds the target up to the near-tie margin and
+    its weight is positive.
+    """
+    if not 0 <= k < cum.shape[0] or not weights[k] > 0.0:
+        return False
+    lo = cum[k - 1] if k > 0 else 0.0
+    return lo - MASS_MARGIN <= target < cum[k] + MASS_MARGIN
+
+
+def expand_row(row, p: Params, u_probe: float, force_probe_pos: Optional[int] = None,
+               row_index=None, replay: Optional[Replay] = None) -> Expansion:
     """Dual-identity expansion of one draft row (RheoSampling, Key design 2).
 
     * x_1..x_m: the m highest-q tokens (ranks 0..m-1), kind DET.
@@ -166,7 +224,9 @@ def expand_row(row, p: Params, u_probe: float, force_probe_pos: Optional[int] = 
       (untempered), the proxy for the probe.
 
     `force_probe_pos` replaces the sampled probe by a given tail rank (used
-    only to enumerate probe identities exactly).
+    only to enumerate probe identities exactly).  `row_index` locates the
+    draw's near-tie; `replay.probe[row_index]` adopts another implementation's
+    probe rank where the draw is a near-tie.
     """
     row = as_f64(row)
     V = row.shape[0]
@@ -193,7 +253,13 @@ def expand_row(row, p: Params, u_probe: float, force_probe_pos: Optional[int] = 
                 k = int(np.nonzero(qT[m:] > 0)[0][-1])
             probe_pos = m + k
             lo = cum[k - 1] if k > 0 else 0.0
-            mg.add("probe_sample", min(target - lo, cum[k] - target), MASS_MARGIN)
+            mg.add("probe_sample", min(target - lo, cum[k] - target), MASS_MARGIN, ("probe", row_index))
+            if replay is not None and row_index in replay.probe and replay.probe[row_index] != probe_pos:
+                other = int(replay.probe[row_index])
+                if not _draw_accepts(cum, qT[m:], target, other - m):
+                    raise ReplayRefused(f"probe of row {row_index}: rank {other} is not a near-tie of {probe_pos}")
+                probe_pos = other
+                replay.adopted.append(("probe", row_index))
     children = []
     for s in range(m):
         children.append((s, DET, s, int(sup[s]), float(q[s])))
@@ -226,6 +292,10 @@ class Tree:
     # top-R builder: for each layer d < D, its frontier in rank order as
     # (token, rank of the parent in the previous frontier, -1 for the root)
     frontiers: list = dataclasses.field(default_factory=list)
+    # SMART builder: every keep test in the order taken, as a dict with the
+    # candidate's layer, token path, score and the state (n, L, |P|) it saw,
+    # lhs, rhs and the decision
+    trace: list = dataclasses.field(default_factory=list)
 
     @property
     def n_nodes(self) -> int:
@@ -249,8 +319,50 @@ class _Cand:
         """
         return (-self.score, self.depth, self.prank, self.slot)
 
+    def ckey(self):
+        """Creation index (depth, parent's rank in its frontier, slot)."""
+        return (self.depth, self.prank, self.slot)
 
-def _record_order_margins(ordered: Sequence[_Cand], upto: int, mg: Margins):
+    def path(self):
+        """Token path from the root's first child down to this candidate."""
+        out, c = [], self
+        while c.parent is not None:
+            out.append(c.token)
+            c = c.parent
+        return tuple(reversed(out))
+
+
+def _ranked(cands: Sequence[_Cand], replay: Optional[Replay], where) -> List[_Cand]:
+    """Candidates in ranking-key order; with a replay, adopted near-tie orders applied.
+
+    replay.before holds (a, b) creation-key pairs that another implementation
+    ranked a before b.  Such a pair is adopted only when the two path scores
+    lie within SCORE_MARGIN (relative) of each other.
+    """
+    ordered = sorted(cands, key=_Cand.key)
+    if not replay or not replay.before:
+        return ordered
+    import functools
+
+    def cmp(a, b):
+        ka, kb = a.ckey(), b.ckey()
+        flip = (ka, kb) in replay.before or (kb, ka) in replay.before
+        natural = -1 if a.key() < b.key() else (1 if a.key() > b.key() else 0)
+        if not flip:
+            return natural
+        want = -1 if (ka, kb) in replay.before else 1
+        if want != natural:
+            top = max(a.score, b.score)
+            if top > 0 and abs(a.score - b.score) > SCORE_MARGIN * top:
+                raise ReplayRefused(f"order of {ka} and {kb} at {where}: scores {a.score} and {b.score}")
+        return want
+    out = sorted(cands, key=functools.cmp_to_key(cmp))
+    if [c.ckey() for c in out] != [c.ckey() for c in ordered]:
+        replay.adopted.append(("order", where))
+    return out
+
+
+def _record_order_margins(ordered: Sequence[_Cand], upto: int, mg: Margins, layer=None):
     """Relative gaps of adjacent scores in a ranked list, over the first `upto`+1 items.
 
     Exact ties (gap 0) are structural (equal logits under one parent, or a
@@ -261,14 +373,14 @@ def _record_order_margins(ordered: Sequence[_Cand], upto: int, mg: Margins):
     for i in range(n):
         a, b = ordered[i].score, ordered[i + 1].score
         if a > 0 and a != b:
-            mg.add("rank", (a - b) / a, SCORE_MARGIN)
+            mg.add("rank", (a - b) / a, SCORE_MARGIN, ("order", layer, i))
 
 
-def _expand(rows, u_probe, p, row_idx, cache, mg):
+def _expand(rows, u_probe, p, row_idx, cache, mg, replay=None):
     if row_idx not in cache:
         if row_idx >= len(rows):
             raise ValueError(f"tree needs draft row {row_idx} but only {len(rows)} were given")
-        ex = expand_row(rows[row_idx], p, float(u_probe[row_idx]))
+        ex = expand_row(rows[row_idx], p, float(u_probe[row_idx]), row_index=row_idx, replay=replay)
         mg.merge(ex.margins)
         cache[row_idx] = ex
     return cache[row_idx]
@@ -279,9 +391,12 @@ def _children(parent: _Cand, prank: int, ex: Expansion, depth: int) -> List[_Can
             for (slot, kind, _rank, tok, lp) in ex.children]
 
 
-def _emit(selected: List[_Cand], root: _Cand, cache: dict, mg: Margins, n_cand: int) -> Tree:
+def _emit(selected: List[_Cand], root: _Cand, cache: dict, mg: Margins, n_cand: int,
+          replay: Optional[Replay] = None) -> Tree:
     """Canonical order: root, then depth ascending, then ranking key."""
-    nodes = [root] + sorted(selected, key=lambda c: (c.depth, -c.score, c.prank, c.slot))
+    depths = sorted({c.depth for c in selected})
+    nodes = [root] + [c for d in depths
+                      for c in _ranked([x for x in selected if x.depth == d], replay, ("canonical", d))]
     for i, c in enumerate(nodes):
         c.idx = i
     n = len(nodes)
@@ -308,7 +423,7 @@ def _new_root():
     return root
 
 
-def build_topr(rows, u_probe, p: Params) -> Tree:
+def build_topr(rows, u_probe, p: Params, replay: Optional[Replay] = None) -> Tree:
     """Expand-then-rerank tree with global top-R pruning (RheoSampling, overall framework).
 
     Layer d = 1..D: the candidates are the children of every frontier node of
@@ -319,6 +434,8 @@ def build_topr(rows, u_probe, p: Params) -> Tree:
     (R counts draft nodes; the root is kept in addition).  Because a child's
     score never exceeds its parent's and ties go to the shallower node, the
     top-R set is ancestor-closed.
+
+    `replay` (optional) adopts another implementation's choices at near-ties.
     """
     mg = Margins()
     cache = {}
@@ -329,19 +446,19 @@ def build_topr(rows, u_probe, p: Params) -> Tree:
     for d in range(1, p.depth + 1):
         layer = []
         for prank, node in enumerate(frontier):
-            ex = _expand(rows, u_probe, p, node.exp_row, cache, mg)
+            ex = _expand(rows, u_probe, p, node.exp_row, cache, mg, replay)
             layer.extend(_children(node, prank, ex, d))
         allc.extend(layer)
         if d < p.depth:
-            ordered = sorted(layer, key=_Cand.key)
-            _record_order_margins(ordered, p.W, mg)
+            _record_order_margins(sorted(layer, key=_Cand.key), p.W, mg, d)
+            ordered = _ranked(layer, replay, ("frontier", d))
             frontier = ordered[:p.W]
             for r, c in enumerate(frontier):
                 c.exp_row = 1 + (d - 1) * p.W + r
             frontiers.append([(c.token, -1 if d == 1 else c.prank) for c in frontier])
-    ordered = sorted(allc, key=_Cand.key)
-    _record_order_margins(ordered, p.R, mg)
-    tree = _emit(ordered[:p.R], root, cache, mg, len(allc))
+    _record_order_margins(sorted(allc, key=_Cand.key), p.R, mg, "final")
+    ordered = _ranked(allc, replay, ("final",))
+    tree = _emit(ordered[:p.R], root, cache, mg, len(allc), replay)
     tree.frontiers = frontiers
     return tree
 
@@ -375,7 +492,7 @@ def smart_keep(P_u: float, n: int, L: float, paths: int, p: Params):
     return lhs > rhs, lhs, rhs
 
 
-def build_smart(rows, u_probe, p: Params) -> Tree:
+def build_smart(rows, u_probe, p: Params, replay: Optional[Replay] = None) -> Tree:
     """Layer-wise greedy SMART builder over dual-identity children (SMART, flowchart + Key design 3).
 
     State: n = kept draft nodes, L = 1 + sum of kept P(v) (expected accepted
@@ -386,8 +503,12 @@ def build_smart(rows, u_probe, p: Params) -> Tree:
     parent was still a leaf.  Building stops when a layer keeps nothing, the
     budget is reached or l = D; otherwise the kept nodes of the layer are
     expanded in key order from the next draft rows (1, 2, ...).
+
+    Every keep test is recorded in `Tree.trace`.  `replay` (optional) adopts
+    another implementation's choices at near-ties.
     """
     mg = Margins()
+    trace = []
     cache = {}
     root = _new_root()
     active = [root]
@@ -399,10 +520,11 @@ def build_smart(rows, u_probe, p: Params) -> Tree:
     for d in range(1, p.depth + 1):
         layer = []
         for prank, node in enumerate(active):
-            ex = _expand(rows, u_probe, p, node.exp_row, cache, mg)
+            ex = _expand(rows, u_probe, p, node.exp_row, cache, mg, replay)
             layer.extend(_children(node, prank, ex, d))
         n_cand += len(layer)
-        layer.sort(key=_Cand.key)
+        _record_order_margins(sorted(layer, key=_Cand.key), len(layer), mg, d)
+        layer = _ranked(layer, replay, ("layer", d))
         kept_layer = []
         for c in layer:
             if n >= p.R:
@@ -410,7 +532,14 @@ def build_smart(rows, u_probe, p: Params) -> Tree:
             P_paths = paths if p.smart_paths == "leaves" else 1
             keep, lhs, rhs = smart_keep(c.score, n, L, P_paths, p)
             if rhs > 0:
-                mg.add("smart", (lhs - rhs) / rhs, SMART_MARGIN)
+                mg.add("smart", (lhs - rhs) / rhs, SMART_MARGIN, ("smart", d, c.ckey()))
+            if replay is not None and c.ckey() in replay.keep and replay.keep[c.ckey()] != keep:
+                if not (rhs > 0 and abs(lhs - rhs) < SMART_MARGIN * rhs):
+                    raise ReplayRefused(f"keep test of {c.ckey()}: lhs {lhs} rhs {rhs}")
+                keep = replay.keep[c.ckey()]
+                replay.adopted.append(("smart", d, c.ckey()))
+            trace.append(dict(layer=d, path=c.path(), score=c.score, n=n, L=L, paths=P_paths,
+                              lhs=lhs, rhs=rhs, keep=bool(keep)))
             if keep:
                 n += 1
                 L += c.score
@@ -426,14 +555,16 @@ def build_smart(rows, u_probe, p: Params) -> Tree:
             c.exp_row = next_row
             next_row += 1
         active = kept_layer
-    return _emit(kept, root, cache, mg, n_cand)
+    tree = _emit(kept, root, cache, mg, n_cand, replay)
+    tree.trace = trace
+    return tree
 
 
-def build(rows, u_probe, p: Params) -> Tree:
+def build(rows, u_probe, p: Params, replay: Optional[Replay] = None) -> Tree:
     """Build one tree from its draft rows [n_rows][V] and probe uniforms [n_rows]."""
     if p.builder == "smart":
-        return build_smart(rows, u_probe, p)
-    return build_topr(rows, u_probe, p)
+        return build_smart(rows, u_probe, p, replay)
+    return build_topr(rows, u_probe, p, replay)
 
 
 # --------------------------------------------------------------------------
@@ -525,7 +656,8 @@ class VerifyResult:
     residual_empty: bool = False
 
 
-def verify(tree: Tree, target_rows, u_verify, u_bonus: float, p: Params, mode: str = "rheo") -> VerifyResult:
+def verify(tree: Tree, target_rows, u_verify, u_bonus: float, p: Params, mode: str = "rheo",
+           replay: Optional[Replay] = None) -> VerifyResult:
     """Layer-by-layer verification of one tree (RheoSampling, Key design 3).
 
     From the root: p = softmax(t/T) of the node's target row over the full
@@ -536,6 +668,10 @@ def verify(tree: Tree, target_rows, u_verify, u_bonus: float, p: Params, mode: s
     id order with u_bonus * Zr < sum_{v' <= v} w(v'), and the walk ends.
     If rounding leaves the residual mass Zr <= 0, the bonus is drawn from p
     and `residual_empty` is set.
+
+    `replay` (optional) adopts another implementation's accept outcomes
+    (replay.accept[(level, j)]) and bonus tokens (replay.bonus[level]) where
+    the decision is a near-tie.
     """
     mg = Margins()
     node, level = 0, 0
@@ -553,10 +689,17 @@ def verify(tree: Tree, target_rows, u_verify, u_bonus: float, p: Params, mode: s
                 u = float(u_verify[level][j])
                 if kind == PROBE:
                     qt = tail_q_tilde(ex, p.m, p_full.shape[0])[x]
-                    mg.add("accept", u * qt - w_before[x] / Z_before, MASS_MARGIN)
+                    margin = u * qt - w_before[x] / Z_before
                 else:
-                    mg.add("accept", u * Z_before - w_before[x], MASS_MARGIN)
-                if u < a:
+                    margin = u * Z_before - w_before[x]
+                mg.add("accept", margin, MASS_MARGIN, ("accept", level, j))
+                accept = u < a
+                if replay is not None and (level, j) in replay.accept and replay.accept[(level, j)] != accept:
+                    if not abs(margin) < MASS_MARGIN:
+                        raise ReplayRefused(f"accept test {j} of level {level}: margin {margin}")
+                    accept = replay.accept[(level, j)]
+                    replay.adopted.append(("accept", level, j))
+                if accept:
                     accepted = next(k for k in kids if int(tree.token[k]) == x and int(tree.kind[k]) == kind)
                     break
         else:
@@ -575,7 +718,13 @@ def verify(tree: Tree, target_rows, u_verify, u_bonus: float, p: Params, mode: s
         if v >= cum.shape[0]:
             v = int(np.nonzero(w > 0)[0][-1])
         lo = cum[v - 1] if v > 0 else 0.0
-        mg.add("bonus", min(target - lo, cum[v] - target), MASS_MARGIN)
+        mg.add("bonus", min(target - lo, cum[v] - target), MASS_MARGIN, ("bonus", level))
+        if replay is not None and level in replay.bonus and replay.bonus[level] != v:
+            other = int(replay.bonus[level])
+            if not _draw_accepts(cum, w, target, other):
+                raise ReplayRefused(f"bonus at level {level}: token {other} is not a near-tie of {v}")
+            v = other
+            replay.adopted.append(("bonus", level))
         toks.append(v)
         return VerifyResult(len(nodes), toks, nodes, mg, empty)
 

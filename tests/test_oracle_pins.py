@@ -315,6 +315,41 @@ def test_smart_cost_golden_values():
     assert O.smart_keep(P * 1.001, 0, 1.0, 1, p)[0]
 
 
+def check_smart_golden(O_mod):
+    """The SMART builder against the hand-worked trees of tests/golden/smart_tree.json:
+    every keep test (candidate, state n / L / |P|, lhs, rhs, decision) in order, the kept
+    set in canonical order and each kept node's expansion row."""
+    g = _golden("smart_tree.json")
+    rows = np.log(np.array(g["draft_q"]))
+    u = np.array(g["u_probe"])
+    for case in g["cases"]:
+        p = O_mod.Params(K=2, m=1, W=2, depth=3, R=case["R"], support=6, builder="smart", lam=case["lam"],
+                         gamma=case["gamma"], delta=case["delta"], rho=case["rho"], alpha=case["alpha"])
+        t = O_mod.build_smart(rows, u, p)
+        got = [(e["layer"], list(e["path"]), e["n"], e["paths"], e["keep"]) for e in t.trace]
+        want = [(e["layer"], e["path"], e["n"], e["paths"], e["keep"]) for e in case["expected_trace"]]
+        assert got == want, (case["name"], got, want)
+        for e, w in zip(t.trace, case["expected_trace"]):
+            for k in ("score", "L", "lhs", "rhs"):
+                assert e[k] == pytest.approx(w[k], rel=1e-12), (case["name"], w["path"], k)
+        paths = []
+        for i in range(1, t.n_nodes):
+            path, j = [], i
+            while j > 0:
+                path.append(int(t.token[j]))
+                j = int(t.parent[j])
+            paths.append(list(reversed(path)))
+        assert paths == [k["path"] for k in case["expected_kept"]], (case["name"], paths)
+        assert t.exp_row[1:].tolist() == [k["exp_row"] for k in case["expected_kept"]], case["name"]
+        assert t.exp_row[0] == 0
+
+
+def test_smart_builder_hand_worked_trees():
+    """SMART notes, flowchart and Key design 3: three hand-worked trees (linear cost, a budget
+    reached mid-layer, convex cost with alpha = 0.8) with every keep test derived by hand."""
+    check_smart_golden(O)
+
+
 def _first_token_law(rows, u_rest, p, target_root, mode="rheo"):
     """Exact law of the first emitted token: sum over root probe identities s of
     q~(s) * P(token | s), where P(token | s) follows the accept probabilities of
