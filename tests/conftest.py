@@ -38,3 +38,10 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """One line with the session's GPU-vs-oracle parity counts (trees compared, near-ties adopted)."""
+    mod = sys.modules.get("parity_compare")
+    if mod is not None and (mod.TALLY["build_trees"] or mod.TALLY["verify_trees"]):
+        terminalreporter.write_line(mod.tally_line())

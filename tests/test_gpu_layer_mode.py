@@ -109,10 +109,18 @@ def check_layer_mode(wl, seed, sample=None, row_stride=None):
             ok &= bool((tok[k:] == -1).all() and (par[k:] == -1).all())
         if ok:
             exact += 1
-        else:
-            assert t.margins.near > 0, f"tree {b}: frontier differs from the oracle without a near-tie"
-            exempt += 1
-    assert exempt <= 0.1 * len(idx) + 1
+            continue
+        # the first layer whose frontier differs must follow a near-tie the oracle logged at or
+        # before that layer's ranking: an order gap of a frontier cut, or a probe draw of a row
+        # expanded before it
+        first = next(layer for layer in range(wl.depth - 1)
+                     if fronts[layer][0][b][:len(t.frontiers[layer])].tolist() != [x for x, _ in t.frontiers[layer]]
+                     or fronts[layer][1][b][:len(t.frontiers[layer])].tolist() != [x for _, x in t.frontiers[layer]])
+        located = [w for kind, w, _ in t.margins.ties
+                   if (kind == "rank" and w[1] != "final" and w[1] <= first + 1)
+                   or (kind == "probe_sample" and w[1] < 1 + first * wl.W)]
+        assert located, f"tree {b}: frontier {first} differs from the oracle without a near-tie before it"
+        exempt += 1
     return exact, exempt
 
 

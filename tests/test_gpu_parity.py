@@ -13,9 +13,14 @@ pytestmark = pytest.mark.gpu
 import parity  # noqa: E402  (loads the native library; fails loudly if absent)
 
 
-def _report(name, out):
-    print(f"{name}: build exact {out['build_exact']} exempt {out['build_exempt']}; "
-          f"verify exact {out.get('verify_exact')} exempt {out.get('verify_exempt')}")
+def _report(name, out, replays_allowed=True):
+    """Print the counts; where no near-tie replay is expected, fail with them."""
+    msg = (f"{name}: build {out['build_exact']} equal, {out['build_replayed']} with adopted near-ties; "
+           f"verify {out['verify_exact']} equal, {out['verify_replayed']} with adopted near-ties; "
+           f"decisions {out['adopted'][:8]}")
+    print(msg)
+    if not replays_allowed:
+        assert not out["adopted"], msg
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2])
@@ -37,16 +42,17 @@ def test_llama3_parity():
     _report("llama3", parity.run_parity(wl, 3))
 
 
-def test_rl_large_batch_sampled():
-    """RL-rollout workload at full size (64 trees, V = 151936, T = 0.7); oracle on sampled trees."""
+def test_rl_large_batch_every_tree():
+    """RL-rollout workload at full size (64 trees, V = 151936, T = 0.7), every tree against the oracle."""
     wl = WL.WORKLOADS["rl"]
-    _report("rl", parity.run_parity(wl, 4, sample=[0, 17, 40, 63]))
+    _report("rl", parity.run_parity(wl, 4), replays_allowed=False)
 
 
-def test_bench_workload_sampled():
-    """The timed workload (LLaMA-3 vocab, 64 trees) in the bench's launch configuration."""
+def test_bench_workload_every_tree():
+    """The timed workload (LLaMA-3 vocab, 64 trees) in the bench's launch configuration, every tree
+    against the oracle: equal without a single adopted near-tie."""
     wl = WL.BENCH_WORKLOAD
-    _report("bench", parity.run_parity(wl, 5, sample=[0, 31, 63]))
+    _report("bench", parity.run_parity(wl, 5), replays_allowed=False)
 
 
 @pytest.mark.parametrize("seed", [0, 1])
@@ -146,7 +152,8 @@ def _parity_on_draft(wl, draft, seed=0):
     case.latent = draft.float()
     trees = parity.oracle_build(case, range(wl.B))
     g = parity.run_gpu(case, None)
-    return parity.compare_build(g, trees, min(wl.support, wl.V))
+    out = parity.compare_case(g, case, range(wl.B), None, trees)
+    return out["build_exact"], out["build_replayed"]
 
 
 def test_heavy_ties_and_constant_rows():
@@ -186,9 +193,8 @@ def test_rows_whose_cut_jumps():
     trees = parity.oracle_build(case, sample)
     out = parity.run_gpu(case, None)
     assert out["status"] == 0, out["status"]
-    ex, exm = parity.compare_build(out, trees, min(wl.support, wl.V))
-    print(f"cut jumps: exact {ex} exempt {exm} of {len(sample)}")
-    assert exm <= 0.1 * len(sample) + 1
+    res = parity.compare_case(out, case, sample, None, trees)
+    _report("cut jumps", res)
 
 
 def test_queue_path_with_ragged_vocabulary():
@@ -234,7 +240,7 @@ def test_nan_row_sets_status_and_stays_in_bounds():
     assert g["status"] & B.S_NONFINITE_DRAFT
     # the other tree is untouched by the bad row
     trees = parity.oracle_build(case, [1])
-    assert parity.compare_build(g, trees, min(wl.support, wl.V))[0] == 1
+    assert parity.compare_case(g, case, [1], None, trees)["build_exact"] == 1
 
 
 def test_probe_survival_independent_of_identity_gpu():
