@@ -31,7 +31,7 @@ DEFAULT_SUPPORT = 128
 EXPORTS = ("spec_tree_rows_needed", "spec_tree_check_params", "spec_tree_select_expand", "spec_tree_rank",
            "spec_tree_build", "spec_tree_verify", "spec_tree_layer_state_bytes", "spec_tree_layer_rows",
            "spec_tree_layer", "spec_tree_finish", "spec_tree_layer_static", "spec_tree_smart_fit",
-           "spec_tree_strerror")
+           "spec_tree_wait_selftest", "spec_tree_strerror")
 
 
 class SpecTreeError(RuntimeError):
@@ -73,6 +73,7 @@ def _load():
     lib.spec_tree_layer_static.argtypes = [P, i32, i32, i32, i32, vp, i64, vp, T, vp, vp, vp, vp]
     dp = ctypes.POINTER(ctypes.c_double)
     lib.spec_tree_smart_fit.argtypes = [i32, dp, dp, dp, ctypes.c_double, dp, P, dp, dp]
+    lib.spec_tree_wait_selftest.argtypes = [ctypes.c_uint32, vp, vp, vp]
     lib.spec_tree_strerror.argtypes = [i32]
     lib.spec_tree_strerror.restype = ctypes.c_char_p
     for name in EXPORTS:
@@ -308,3 +309,9 @@ class VerifyOutputs:
         self.out_tok = torch.empty((B, params.depth + 1), dtype=torch.int32, device=device)
         self.out_node = torch.empty((B, params.depth + 1), dtype=torch.int32, device=device)
         self.margins = torch.zeros((2,), dtype=torch.int32, device=device)
+
+
+def spec_tree_wait_selftest(polls: int, status: torch.Tensor, result: torch.Tensor, stream=None):
+    """Let one CTA-scope and one cluster-scope bounded wait run out (`polls` polls each) on a barrier
+    nothing arrives on; result (4 x int32 on the device) = gave up / polls made, per CTA."""
+    _check(_lib.spec_tree_wait_selftest(polls, _ptr(status), _ptr(result), _stream(stream)))

@@ -1143,6 +1143,13 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
           atomicExch(a.sched + 1, 0u);
         }
       }
+      // before the producer leaves, every copy it issued has landed (a bounded
+      // wait on each stage's last phase): the CTA never exits with a bulk copy
+      // still writing into its shared memory, even after a consumer gave up
+      for (int j = 0; j < SX_STAGES && j < g; ++j) {
+        const int64_t last = ((g - 1 - j) / SX_STAGES) * SX_STAGES + j;
+        if (!mbar_wait(&s.full[j], static_cast<uint32_t>((last / SX_STAGES) & 1))) timed_out = true;
+      }
       if (timed_out) s.timeout = 1;
     }
     return;

@@ -70,19 +70,55 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
-// Bounded wait on the phase with the given parity.  Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait on the phase with the given parity: at most `limit` polls.
+// Returns false on timeout; `polls` (if given) receives the polls made.
+__device__ __forceinline__ bool mbar_wait_n(uint64_t* bar, uint32_t parity, uint32_t limit,
+                                            uint32_t* polls = nullptr) {
   const uint32_t addr = smem_u32(bar);
-  for (uint32_t it = 0; it < WAIT_LIMIT; ++it) {
+  for (uint32_t it = 0; it < limit; ++it) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
         : "r"(addr), "r"(parity), "r"(WAIT_SUSPEND_NS)
         : "memory");
-    if (done) return true;
+    if (done) {
+      if (polls) *polls = it + 1;
+      return true;
+    }
   }
+  if (polls) *polls = limit;
   return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_n(bar, parity, WAIT_LIMIT);
+}
+
+// The same with acquire at cluster scope, so that stores another CTA of the
+// cluster released before its remote arrive are visible after the wait.
+__device__ __forceinline__ bool mbar_wait_cluster_n(uint64_t* bar, uint32_t parity, uint32_t limit,
+                                                    uint32_t* polls = nullptr) {
+  const uint32_t addr = smem_u32(bar);
+  for (uint32_t it = 0; it < limit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(addr), "r"(parity), "r"(WAIT_SUSPEND_NS)
+        : "memory");
+    if (done) {
+      if (polls) *polls = it + 1;
+      return true;
+    }
+  }
+  if (polls) *polls = limit;
+  return false;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_cluster_n(bar, parity, WAIT_LIMIT);
 }
 
 // L2 policy for data read again soon: evict last.

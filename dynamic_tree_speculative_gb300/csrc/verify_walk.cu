@@ -300,23 +300,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
 
-// Bounded wait (as mbar_wait) with acquire at cluster scope, so that stores
-// made by other CTAs before their arrivals are visible.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
-  const uint32_t addr = smem_u32(bar);
-  for (uint32_t it = 0; it < WAIT_LIMIT; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(addr), "r"(parity), "r"(WAIT_SUSPEND_NS)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-
 // Support rank of the child in sibling slot `slot` (DET 0..m-1 -> ranks
 // 0..m-1, PROBE m -> the probe's rank, FILL -> next tail ranks skipping the probe).
 __device__ __forceinline__ int rank_of_slot(int slot, int m, int pp) {
@@ -476,7 +459,8 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
           if (probe_node >= 0 && !probe_last) {
             const float p = s.p_sup[pp], qt = s.qt_sup[pp];
             const float u = uv[0];
-            if (L.margins && fabsf(u * qt - p) < static_cast<float>(MASS_MARGIN)) atomicAdd(L.margins, 1u);
+            // near-tie: |u - ratio| < 1e-6 with ratio = p / q~_T
+            if (L.margins && fabsf(u * qt - p) < static_cast<float>(MASS_MARGIN) * qt) atomicAdd(L.margins, 1u);
             if (u * qt < p) {
               accepted = probe_node;
             } else {
@@ -498,7 +482,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
               const int r = rank_of_slot(slot, m, pp);
               const float w = s.w_sup[r];
               const float u = uv[j];
-              if (L.margins && fabsf(u * Zr - w) < static_cast<float>(MASS_MARGIN)) atomicAdd(L.margins, 1u);
+              if (L.margins && fabsf(u * Zr - w) < static_cast<float>(MASS_MARGIN) * Zr) atomicAdd(L.margins, 1u);
               if (u * Zr < w) {
                 accepted = kid;
                 break;
@@ -514,7 +498,8 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
               } else {
                 const float w = s.w_sup[pp], qt = s.qt_sup[pp];
                 const float u = uv[j];
-                if (L.margins && fabsf(u * qt - w / Zr) < static_cast<float>(MASS_MARGIN)) atomicAdd(L.margins, 1u);
+                if (L.margins && fabsf(u * qt * Zr - w) < static_cast<float>(MASS_MARGIN) * qt * Zr)
+                  atomicAdd(L.margins, 1u);
                 if (u * qt * Zr < w) {
                   accepted = probe_node;
                 } else {
@@ -650,6 +635,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
     {
       const int ncorr = s.ncorr;
       const float tr = s.bonus_target;
+      const float tie = static_cast<float>(MASS_MARGIN) * s.Zr;  // a draw within 1e-6 * Zr of a boundary
       float base_run = 0.0f;
       int last_pos = -1;
       for (int cb = t0; cb < t1; cb += VER_THREADS * VEC) {
@@ -698,7 +684,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
               const float nx = acc + w[j];
               if (tr < nx) {
                 pick = v0 + j;
-                if (L.margins && (tr - acc < static_cast<float>(MASS_MARGIN) || nx - tr < static_cast<float>(MASS_MARGIN)))
+                if (L.margins && (tr - acc < tie || nx - tr < tie))
                   atomicAdd(L.margins + 1, 1u);
               }
               acc = nx;

@@ -238,8 +238,11 @@ int spec_tree_build(const spec_tree_params* p, int B, int V, int dtype,
  *   accept_len: device [B]; out_tok, out_node: device [B][depth + 1]
  *   (accepted tokens then the bonus token; accepted node indices then -1;
  *   unused entries -1).
- *   margins: device uint32[2] or NULL; counts decisions whose float32 margin
- *   is below 1e-6 in probability mass ([0] accept tests, [1] bonus draws).
+ *   margins: device uint32[2] or NULL; counts near-tie decisions, whose
+ *   float32 outcome could differ from an exact computation: [0] accept tests
+ *   with |u - ratio| < 1e-6 (ratio = the accept probability before the
+ *   min(1, .)), [1] bonus draws whose target u * Zr lies within 1e-6 * Zr of
+ *   a boundary of the residual's cumulative mass.  Added to, never cleared.
  */
 int spec_tree_verify(const spec_tree_params* p, int B, int V, int dtype,
                      const void* target_logits, int64_t row_stride,
@@ -321,7 +324,10 @@ int spec_tree_finish(const spec_tree_params* p, int B, int V, const spec_tree_t*
  *   - the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.  A failed lookup returns
- *     SPEC_TREE_E_CUDA.
+ *     SPEC_TREE_E_CUDA.  The cached address belongs to the device's primary
+ *     context at that first call: a cudaDeviceReset of that device afterwards
+ *     (which unloads the library's module and may place the array elsewhere
+ *     when it is loaded again) is not supported by this entry point.
  * It calls no cudaMalloc, cudaFree or other allocating routine.  Everything
  * else (arguments, rows, frontier outputs, status bits, results bit for bit)
  * is as for spec_tree_layer followed, after the last layer, by
@@ -357,6 +363,25 @@ int spec_tree_layer_static(const spec_tree_params* p, int B, int V, int layer, i
  */
 int spec_tree_smart_fit(int npts, const double* n, const double* t_draft, const double* t_verify,
                         double t_base, const double* w, spec_tree_params* p, double* coef, double* rms);
+
+/*
+ * spec_tree_wait_selftest: a failure-detection check, not a step of the
+ * method (the pages have no counterpart).  Every wait inside the library's
+ * kernels (on a bulk copy, a ring slot, another warp or another CTA of a
+ * cluster) is bounded: after its poll limit it gives up, the kernel ORs
+ * SPEC_TREE_S_TIMEOUT into `status`, finishes without waiting again and
+ * returns, so that the context stays usable.  This entry point exercises
+ * exactly that: one cluster of two CTAs each waits, with `polls` polls (each
+ * poll suspends the thread for at most 20 us), on an mbarrier that nothing
+ * arrives on, CTA 0 with the CTA-scope wait, CTA 1 with the cluster-scope
+ * wait; no copy is in flight.  Each gives up and reports it.
+ *   polls:  1 .. 65536 (the kernels' own limit);
+ *   status: device uint32, SPEC_TREE_S_TIMEOUT is OR-ed in;
+ *   result: device uint32[4]: [2 r] = 1 if CTA r's wait gave up, [2 r + 1] =
+ *           the polls it made.
+ * Returns SPEC_TREE_E_PARAM for a null pointer or polls out of range.
+ */
+int spec_tree_wait_selftest(uint32_t polls, uint32_t* status, uint32_t* result, spec_tree_stream_t stream);
 
 /* Message for a return code (static string). */
 const char* spec_tree_strerror(int code);

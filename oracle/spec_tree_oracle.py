@@ -44,7 +44,7 @@ import numpy as np
 ROOT, DET, PROBE, FILL = 0, 1, 2, 3
 
 # Decision margins below these values are near-ties (see `Margins`).
-MASS_MARGIN = 1e-6      # |u * Z - cumulative mass|, in probability units
+MASS_MARGIN = 1e-6      # |u - ratio| of an accept test; |u * Z - cumulative mass| / Z of a CDF draw
 SCORE_MARGIN = 1e-5     # relative gap between two compared path scores
 SMART_MARGIN = 1e-5     # |lhs - rhs| / rhs of the SMART keep test
 
@@ -189,17 +189,17 @@ class Expansion:
     margins: Margins
 
 
-def _draw_accepts(cum: np.ndarray, weights: np.ndarray, target: float, k: int) -> bool:
-    """Whether index k is a choice of the inverse-CDF draw `target` within MASS_MARGIN.
+def _draw_accepts(cum: np.ndarray, weights: np.ndarray, target: float, k: int, total: float) -> bool:
+    """Whether index k is a choice of the inverse-CDF draw `target` = u * total within the near-tie margin.
 
     k is a valid choice of another implementation when its own cumulative
-    interval [cum[k-1], cum[k]) holds the target up to the near-tie margin and
-    its weight is positive.
+    interval [cum[k-1], cum[k]) holds the target up to MASS_MARGIN * total
+    and its weight is positive.
     """
     if not 0 <= k < cum.shape[0] or not weights[k] > 0.0:
         return False
     lo = cum[k - 1] if k > 0 else 0.0
-    return lo - MASS_MARGIN <= target < cum[k] + MASS_MARGIN
+    return lo - MASS_MARGIN * total <= target < cum[k] + MASS_MARGIN * total
 
 
 def expand_row(row, p: Params, u_probe: float, force_probe_pos: Optional[int] = None,
@@ -253,10 +253,10 @@ def expand_row(row, p: Params, u_probe: float, force_probe_pos: Optional[int] = 
                 k = int(np.nonzero(qT[m:] > 0)[0][-1])
             probe_pos = m + k
             lo = cum[k - 1] if k > 0 else 0.0
-            mg.add("probe_sample", min(target - lo, cum[k] - target), MASS_MARGIN, ("probe", row_index))
+            mg.add("probe_sample", min(target - lo, cum[k] - target) / zT, MASS_MARGIN, ("probe", row_index))
             if replay is not None and row_index in replay.probe and replay.probe[row_index] != probe_pos:
                 other = int(replay.probe[row_index])
-                if not _draw_accepts(cum, qT[m:], target, other - m):
+                if not _draw_accepts(cum, qT[m:], target, other - m, zT):
                     raise ReplayRefused(f"probe of row {row_index}: rank {other} is not a near-tie of {probe_pos}")
                 probe_pos = other
                 replay.adopted.append(("probe", row_index))
@@ -337,7 +337,8 @@ def _ranked(cands: Sequence[_Cand], replay: Optional[Replay], where) -> List[_Ca
 
     replay.before holds (a, b) creation-key pairs that another implementation
     ranked a before b.  Such a pair is adopted only when the two path scores
-    lie within SCORE_MARGIN (relative) of each other.
+    differ, by at most SCORE_MARGIN (relative): equal scores are ordered by the
+    creation index everywhere.
     """
     ordered = sorted(cands, key=_Cand.key)
     if not replay or not replay.before:
@@ -352,8 +353,9 @@ def _ranked(cands: Sequence[_Cand], replay: Optional[Replay], where) -> List[_Ca
             return natural
         want = -1 if (ka, kb) in replay.before else 1
         if want != natural:
-            top = max(a.score, b.score)
-            if top > 0 and abs(a.score - b.score) > SCORE_MARGIN * top:
+            # equal scores are ordered by the creation index on every implementation
+            gap = abs(a.score - b.score)
+            if not 0.0 < gap <= SCORE_MARGIN * max(a.score, b.score):
                 raise ReplayRefused(f"order of {ka} and {kb} at {where}: scores {a.score} and {b.score}")
         return want
     out = sorted(cands, key=functools.cmp_to_key(cmp))
@@ -687,11 +689,12 @@ def verify(tree: Tree, target_rows, u_verify, u_bonus: float, p: Params, mode: s
                                             [int(tree.kind[j]) for j in kids], mode)
             for j, (kind, x, a, w_before, Z_before) in enumerate(steps):
                 u = float(u_verify[level][j])
+                # the near-tie margin of an accept test is |u - ratio|
                 if kind == PROBE:
                     qt = tail_q_tilde(ex, p.m, p_full.shape[0])[x]
-                    margin = u * qt - w_before[x] / Z_before
+                    margin = u - (w_before[x] / Z_before) / qt
                 else:
-                    margin = u * Z_before - w_before[x]
+                    margin = u - w_before[x] / Z_before
                 mg.add("accept", margin, MASS_MARGIN, ("accept", level, j))
                 accept = u < a
                 if replay is not None and (level, j) in replay.accept and replay.accept[(level, j)] != accept:
@@ -718,10 +721,10 @@ def verify(tree: Tree, target_rows, u_verify, u_bonus: float, p: Params, mode: s
         if v >= cum.shape[0]:
             v = int(np.nonzero(w > 0)[0][-1])
         lo = cum[v - 1] if v > 0 else 0.0
-        mg.add("bonus", min(target - lo, cum[v] - target), MASS_MARGIN, ("bonus", level))
+        mg.add("bonus", min(target - lo, cum[v] - target) / Zr, MASS_MARGIN, ("bonus", level))
         if replay is not None and level in replay.bonus and replay.bonus[level] != v:
             other = int(replay.bonus[level])
-            if not _draw_accepts(cum, w, target, other):
+            if not _draw_accepts(cum, w, target, other, Zr):
                 raise ReplayRefused(f"bonus at level {level}: token {other} is not a near-tie of {v}")
             v = other
             replay.adopted.append(("bonus", level))

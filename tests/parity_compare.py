@@ -8,9 +8,9 @@ float64):
   * support ids are compared bit for bit and are never exempt;
   * node topology, tokens, kinds, slots, expansion rows, accepted tokens and
     nodes, accept lengths: bit for bit, except at a decision where the oracle
-    itself logged a near-tie (a probe or bonus draw within 1e-6 of probability
-    mass of a CDF boundary, an accept test within 1e-6, two path scores within
-    1e-5 relative, a SMART keep test within 1e-5 relative);
+    itself logged a near-tie (a probe or bonus draw u * Z within 1e-6 * Z of a
+    CDF boundary, an accept test with |u - ratio| < 1e-6, two path scores
+    within 1e-5 relative, a SMART keep test within 1e-5 relative);
   * at such a decision the oracle adopts the other side's choice (replay mode,
     `oracle.Replay`) and the comparison goes on downstream, so a difference is
     exempt only at the decision where it starts, and only when that decision is

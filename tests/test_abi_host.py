@@ -92,6 +92,10 @@ def test_bad_arguments_fail_before_any_launch(binding):
                                 ctypes.byref(t), ctypes.c_void_p(256), ctypes.c_void_p(256), None, None, None,
                                 None, None, None) == binding.E_PARAM
     assert binding._lib.spec_tree_strerror(binding.E_LAYOUT).startswith(b"unsupported")
+    # the bounded-wait self-test: null pointers and poll counts out of range
+    assert lib.spec_tree_wait_selftest(64, None, ctypes.c_void_p(256), None) == binding.E_PARAM
+    assert lib.spec_tree_wait_selftest(0, ctypes.c_void_p(256), ctypes.c_void_p(256), None) == binding.E_PARAM
+    assert lib.spec_tree_wait_selftest(65537, ctypes.c_void_p(256), ctypes.c_void_p(256), None) == binding.E_PARAM
 
 
 def test_layer_rows_and_state(binding):
@@ -107,6 +111,8 @@ def test_layer_rows_and_state(binding):
     assert binding.spec_tree_layer_rows(P(K=8, m=1, W=8, depth=8, R=60, builder=binding.BUILDER_SMART), 0) == 0
     n = binding.spec_tree_layer_state_bytes()
     assert n > 0 and n % 16 == 0
+    # the allocation-free entry point reserves 56 KiB of its array per tree for this state
+    assert n <= 56 * 1024
 
 
 def test_layer_mode_bad_arguments(binding):
@@ -179,12 +185,14 @@ def test_binding_structs_match_the_c_header(binding, tmp_path):
         for f, _ in cls._fields_:
             c = cname.get(f, f)
             src.append(f'  printf("{st}.{f} %zu\\n", offsetof({st}, {c}));')
+    src.append('  printf("SPEC_TREE_STATIC_MAX_TREES %d\\n", (int)SPEC_TREE_STATIC_MAX_TREES);')
     src += ["  return 0;", "}"]
     c_file, exe = tmp_path / "abi.c", tmp_path / "abi"
     c_file.write_text("\n".join(src) + "\n")
     subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(c_file), "-o", str(exe)], check=True)
     got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
                                                        check=True).stdout.splitlines())
+    assert int(got["SPEC_TREE_STATIC_MAX_TREES"]) == binding.STATIC_MAX_TREES
     for st, cls in fields.items():
         assert int(got[st]) == ctypes.sizeof(cls), st
         for f, _ in cls._fields_:

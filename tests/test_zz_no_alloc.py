@@ -10,7 +10,11 @@ trees as spec_tree_layer + spec_tree_finish with a caller-owned state: node
 arrays and score bits, every expanded support row and every frontier, bit for
 bit (the tolerance of the other layer-mode tests), on two builds in a row, so
 that the second one runs over what the first left in the shared array.  It also
-checks that a batch above the array's limit is refused before any launch.
+checks that a batch above the array's limit is refused before any launch, that
+a whole build changes the device's free memory by nothing (after a first build
+has loaded the library's module and its array), that a one-layer build (whose
+only call is also the last) matches too, and that an empty batch on the last
+layer is accepted.
 
 The file is named to be collected last, so that a failure here comes after
 every other test has run.
@@ -114,3 +118,59 @@ def test_static_state_refuses_too_many_trees():
         B.spec_tree_layer_static(params, wl.V, 0, d, u, tree, None, None, status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+
+
+def test_static_build_allocates_nothing():
+    """A whole static build leaves the device's free memory unchanged (every input, output and
+    frontier buffer allocated beforehand; a first build has loaded the module and its array)."""
+    wl = WL.WORKLOADS["vicuna"].with_(B=16, V=8000, depth=4, R=24)
+    case = parity.make_case(wl, 44)
+    params = B.Params.from_workload(wl)
+    tree = _tree(params, wl)
+    ftok = torch.full((wl.B, wl.W), -7, dtype=torch.int32, device="cuda")
+    fpar = torch.full((wl.B, wl.W), -7, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    draft, u = case.draft.cuda(), case.u_probe.cuda()
+    layers = []
+    for layer in range(wl.depth):
+        rows, r0 = B.spec_tree_layer_rows(params, layer), _row0(wl, layer)
+        layers.append((layer, draft[:, r0:r0 + rows].contiguous(), u[:, r0:r0 + rows].contiguous()))
+
+    def build():
+        for layer, d, uu in layers:
+            B.spec_tree_layer_static(params, wl.V, layer, d, uu, tree, ftok, fpar, status)
+
+    build()
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    build()
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    assert free1 == free0, (free0, free1)
+    assert int(status.item()) == 0 and (tree.n_nodes.cpu() > 1).all()
+
+
+def test_static_one_layer_build():
+    """depth 1: the first call is also the last, so it expands the root and cuts the tree."""
+    wl = WL.WORKLOADS["vicuna"].with_(B=8, V=6000, depth=1, R=8)
+    case = parity.make_case(wl, 45)
+    params, ref, ref_fronts = _build(case, static=False)
+    _, got, got_fronts = _build(case, static=True)
+    _same(wl, params, got, ref)
+    assert (got["n_nodes"] == wl.R + 1).all()
+
+
+def test_static_empty_batch_on_the_last_layer():
+    """B = 0 on the last layer: only the argument checks run, and they pass."""
+    import ctypes
+    wl = WL.WORKLOADS["vicuna"].with_(B=4, V=6000, depth=3, R=12)
+    params = B.Params.from_workload(wl)
+    tree = B.TreeBuffers(params, wl.B)
+    d = torch.zeros((wl.B, wl.W, wl.V), dtype=torch.bfloat16, device="cuda")
+    u = torch.zeros((wl.B, wl.W), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = B._lib.spec_tree_layer_static(ctypes.byref(params.c()), 0, wl.V, wl.depth - 1, B.BF16,
+                                       ctypes.c_void_p(d.data_ptr()), wl.V, ctypes.c_void_p(u.data_ptr()),
+                                       ctypes.byref(tree.c()), None, None, ctypes.c_void_p(status.data_ptr()), None)
+    torch.cuda.synchronize()
+    assert rc == B.OK and int(status.item()) == 0
