@@ -25,13 +25,15 @@ OK, E_PARAM, E_LAYOUT, E_CUDA = 0, -1, -3, -4
 S_NONFINITE_DRAFT, S_NONFINITE_TARGET, S_RESIDUAL_EMPTY = 1, 2, 4
 S_OVERFLOW, S_TIMEOUT, S_ROWS, S_LAYERS = 8, 16, 32, 64
 MAX_SUPPORT = 1024
+SUPPORT_DENSE = 0x40000000   # |S| = V for any vocabulary
+DENSE_MAX_K = 64
 STATIC_MAX_TREES = 64
 DEFAULT_SUPPORT = 128
 
 EXPORTS = ("spec_tree_rows_needed", "spec_tree_check_params", "spec_tree_select_expand", "spec_tree_rank",
            "spec_tree_build", "spec_tree_verify", "spec_tree_layer_state_bytes", "spec_tree_layer_rows",
            "spec_tree_layer", "spec_tree_finish", "spec_tree_layer_static", "spec_tree_smart_fit",
-           "spec_tree_wait_selftest", "spec_tree_strerror")
+           "spec_tree_wait_selftest", "spec_tree_verify_dense", "spec_tree_strerror")
 
 
 class SpecTreeError(RuntimeError):
@@ -65,6 +67,7 @@ def _load():
     lib.spec_tree_rank.argtypes = [P, i32, i32, T, vp, vp]
     lib.spec_tree_build.argtypes = [P, i32, i32, i32, vp, i64, vp, T, vp, vp]
     lib.spec_tree_verify.argtypes = [P, i32, i32, i32, vp, i64, T, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.spec_tree_verify_dense.argtypes = [P, i32, i32, i32, vp, i64, vp, i64, T, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.spec_tree_layer_state_bytes.argtypes = []
     lib.spec_tree_layer_state_bytes.restype = ctypes.c_size_t
     lib.spec_tree_layer_rows.argtypes = [P, i32]
@@ -140,13 +143,17 @@ def _check(rc: int):
 class TreeBuffers:
     """Device buffers of a batch of trees (the spec_tree_t of the C ABI)."""
 
-    def __init__(self, params: Params, B: int, n_rows: Optional[int] = None, device="cuda"):
+    def __init__(self, params: Params, B: int, n_rows: Optional[int] = None, device="cuda", V: Optional[int] = None):
         i32, f32 = torch.int32, torch.float32
         self.B = B
         self.n_rows = n_rows if n_rows is not None else rows_needed(params)
         self.max_nodes = params.R + 1
-        # support arrays hold |S| = min(support, V) ranks per row; at least 128 wide
-        self.sup_stride = max(DEFAULT_SUPPORT, params.support or DEFAULT_SUPPORT)
+        # support arrays hold |S| = min(support, V) ranks per row, at least 128 wide; a dense
+        # support of a vocabulary above MAX_SUPPORT tokens keeps K ranks and the probe
+        if params.support == SUPPORT_DENSE:
+            self.sup_stride = MAX_SUPPORT if V is None or V <= MAX_SUPPORT else max(DEFAULT_SUPPORT, params.K + 1)
+        else:
+            self.sup_stride = max(DEFAULT_SUPPORT, params.support or DEFAULT_SUPPORT)
         mk = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)  # noqa: E731
         n = (B, self.max_nodes)
         self.node_token, self.node_parent, self.node_depth = mk(n, i32), mk(n, i32), mk(n, i32)
@@ -221,6 +228,24 @@ def spec_tree_verify(params: Params, V: int, target: torch.Tensor, tree: TreeBuf
                                  _row_stride(target, tree.max_nodes), ctypes.byref(tree.c()), _ptr(u_verify),
                                  _ptr(u_bonus), _ptr(accept_len), _ptr(out_tok), _ptr(out_node), _ptr(margins),
                                  _ptr(status), _stream(stream)))
+
+
+def spec_tree_verify_dense(params: Params, V: int, target: torch.Tensor, draft: torch.Tensor, tree: TreeBuffers,
+                           u_verify: torch.Tensor, u_bonus: torch.Tensor, accept_len: torch.Tensor,
+                           out_tok: torch.Tensor, out_node: torch.Tensor, margins: Optional[torch.Tensor],
+                           status: torch.Tensor, stream=None):
+    """spec_tree_verify for trees built on the dense support of a vocabulary above MAX_SUPPORT tokens: it
+    reads the node's draft row (the tensor the tree was built from) for the tail law."""
+    _check(_lib.spec_tree_verify_dense(ctypes.byref(_cp(params)), tree.B, V, _dtype_code(target), _ptr(target),
+                                       _row_stride(target, tree.max_nodes), _ptr(draft),
+                                       _row_stride(draft, tree.n_rows), ctypes.byref(tree.c()), _ptr(u_verify),
+                                       _ptr(u_bonus), _ptr(accept_len), _ptr(out_tok), _ptr(out_node),
+                                       _ptr(margins), _ptr(status), _stream(stream)))
+
+
+def is_dense(params: Params, V: int) -> bool:
+    """The dense support of a vocabulary too large for the support arrays (verify with spec_tree_verify_dense)."""
+    return params.support == SUPPORT_DENSE and V > MAX_SUPPORT
 
 
 def spec_tree_layer_state_bytes() -> int:

@@ -13,7 +13,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libspec_tree.so")
 SOURCES = ["api.cu", "select_expand.cu", "rank_tree.cu", "verify_walk.cu", "select_wide.cu", "smart_fit.cpp",
-           "layer_static.cu", "wait_selftest.cu"]
+           "layer_static.cu", "wait_selftest.cu", "verify_dense.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -30,8 +30,19 @@ int num_sms_of_current_device() {
 constexpr int DEFAULT_SUPPORT = 128;
 
 int support_size(const spec_tree_params* p, int V) {
+  if (p->support == SPEC_TREE_SUPPORT_DENSE) return V;
   const int s = p->support == 0 ? DEFAULT_SUPPORT : p->support;
   return s < V ? s : V;
+}
+
+// the dense support of a vocabulary too large for the support arrays
+bool dense_support(const spec_tree_params* p, int V) {
+  return p->support == SPEC_TREE_SUPPORT_DENSE && V > SPEC_TREE_MAX_SUPPORT;
+}
+
+// entries of a row's support arrays: |S|, or K + 1 for a dense support
+int support_entries(const spec_tree_params* p, int V) {
+  return dense_support(p, V) ? p->K + 1 : support_size(p, V);
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
@@ -49,7 +60,7 @@ int check_rows(int dtype, const void* logits, int64_t row_stride, int V) {
 
 int check_tree(const spec_tree_params* p, const spec_tree_t* t, int V, bool need_nodes, bool need_sup) {
   if (t == nullptr) return SPEC_TREE_E_PARAM;
-  const int S = support_size(p, V);
+  const int S = support_entries(p, V);
   if (need_sup && (t->sup_id == nullptr || t->sup_q == nullptr || t->sup_qT == nullptr || t->sup_z == nullptr ||
                    t->sup_zT == nullptr || t->probe_pos == nullptr || t->sup_stride < S))
     return SPEC_TREE_E_PARAM;
@@ -65,9 +76,19 @@ int check_tree(const spec_tree_params* p, const spec_tree_t* t, int V, bool need
 cudaStream_t as_stream(spec_tree_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
 // the streaming kernel for supports of up to 128 tokens, else one CTA per row
+// (the dense support of a large vocabulary by its own kernel)
 cudaError_t launch_select(int dtype, const st::SelLaunch& L, cudaStream_t stream) {
+  if (L.dense) return st::launch_select_dense(dtype, L, stream);
   return L.S <= 128 ? st::launch_select_expand(dtype, L, stream) : st::launch_select_wide(dtype, L, stream);
 }
+
+// support entries the selection writes: |S|, or the K ranks kept of a dense support
+void set_support(st::SelLaunch& L, const spec_tree_params* p, int V) {
+  L.dense = dense_support(p, V);
+  L.S = L.dense ? p->K : support_size(p, V);
+}
+
+int probe_entry_cap(const spec_tree_params* p, int V) { return dense_support(p, V) ? p->K : INT32_MAX; }
 
 }  // namespace
 
@@ -82,9 +103,11 @@ int spec_tree_rows_needed(const spec_tree_params* p) {
 int spec_tree_check_params(const spec_tree_params* p, int V) {
   if (p == nullptr) return SPEC_TREE_E_PARAM;
   if (V < 1 || V >= (1 << 24)) return SPEC_TREE_E_PARAM;
-  if (p->support < 0 || p->support > SPEC_TREE_MAX_SUPPORT) return SPEC_TREE_E_PARAM;
+  if (p->support < 0 || (p->support > SPEC_TREE_MAX_SUPPORT && p->support != SPEC_TREE_SUPPORT_DENSE))
+    return SPEC_TREE_E_PARAM;
   const int S = support_size(p, V);
   if (p->K < 1 || p->K > S || p->m < 0 || p->m > p->K) return SPEC_TREE_E_PARAM;
+  if (dense_support(p, V) && p->K > SPEC_TREE_DENSE_MAX_K) return SPEC_TREE_E_PARAM;
   if (p->verify_order != SPEC_TREE_PROBE_FIRST && p->verify_order != SPEC_TREE_PROBE_LAST) return SPEC_TREE_E_PARAM;
   if (p->depth < 1 || p->depth > 255 || p->R < 1 || p->R + 1 > SPEC_TREE_MAX_NODES) return SPEC_TREE_E_PARAM;
   if (!(p->temperature > 0.0f) || !isfinite(p->temperature)) return SPEC_TREE_E_PARAM;
@@ -123,7 +146,7 @@ int spec_tree_select_expand(const spec_tree_params* p, int B, int V, int dtype, 
   L.rows_used = needed < tree->n_rows ? needed : tree->n_rows;
   L.B = B;
   L.V = V;
-  L.S = support_size(p, V);
+  set_support(L, p, V);
   L.m = p->m;
   L.draw_probe = p->m < p->K;
   L.temperature = p->temperature;
@@ -157,6 +180,7 @@ int spec_tree_rank(const spec_tree_params* p, int B, int V, const spec_tree_t* t
   L.rows_avail = needed < tree->n_rows ? needed : tree->n_rows;
   L.tree = *tree;
   L.status = status;
+  L.probe_entry_cap = probe_entry_cap(p, V);
   L.layer = 0;
   L.state = nullptr;
   L.frontier_token = nullptr;
@@ -211,7 +235,7 @@ int spec_tree_layer(const spec_tree_params* p, int B, int V, int layer, int dtyp
   S.rows_used = rows;
   S.B = B;
   S.V = V;
-  S.S = support_size(p, V);
+  set_support(S, p, V);
   S.m = p->m;
   S.draw_probe = p->m < p->K;
   S.temperature = p->temperature;
@@ -236,6 +260,7 @@ int spec_tree_layer(const spec_tree_params* p, int B, int V, int layer, int dtyp
   L.rows_avail = rows;
   L.tree = *tree;
   L.status = status;
+  L.probe_entry_cap = probe_entry_cap(p, V);
   L.layer = layer;
   L.state = state;
   L.frontier_token = frontier_token;
@@ -257,6 +282,7 @@ int spec_tree_finish(const spec_tree_params* p, int B, int V, const spec_tree_t*
   L.rows_avail = 0;
   L.tree = *tree;
   L.status = status;
+  L.probe_entry_cap = probe_entry_cap(p, V);
   L.layer = p->depth;
   L.state = const_cast<void*>(state);
   L.frontier_token = nullptr;
@@ -273,6 +299,7 @@ int spec_tree_verify(const spec_tree_params* p, int B, int V, int dtype, const v
   if (B < 0 || u_verify == nullptr || u_bonus == nullptr || accept_len == nullptr || out_tok == nullptr ||
       out_node == nullptr)
     return SPEC_TREE_E_PARAM;
+  if (dense_support(p, V)) return SPEC_TREE_E_PARAM;  // spec_tree_verify_dense reads the draft rows too
   if ((rc = check_rows(dtype, target_logits, row_stride, V))) return rc;
   if ((rc = check_tree(p, tree, V, true, true))) return rc;
   st::VerifyLaunch L;
@@ -292,8 +319,47 @@ int spec_tree_verify(const spec_tree_params* p, int B, int V, int dtype, const v
   L.margins = margins;
   L.status = status;
   L.num_sms = num_sms_of_current_device();
+  L.draft = nullptr;
+  L.draft_row_stride = 0;
   if (L.num_sms <= 0) return SPEC_TREE_E_CUDA;
   return st::launch_verify(L, as_stream(stream)) == cudaSuccess ? SPEC_TREE_OK : SPEC_TREE_E_CUDA;
+}
+
+int spec_tree_verify_dense(const spec_tree_params* p, int B, int V, int dtype, const void* target_logits,
+                           int64_t row_stride, const void* draft_logits, int64_t draft_row_stride,
+                           const spec_tree_t* tree, const float* u_verify, const float* u_bonus,
+                           int32_t* accept_len, int32_t* out_tok, int32_t* out_node, uint32_t* margins,
+                           uint32_t* status, spec_tree_stream_t stream) {
+  int rc = spec_tree_check_params(p, V);
+  if (rc) return rc;
+  if (!dense_support(p, V)) return SPEC_TREE_E_PARAM;
+  if (B < 0 || u_verify == nullptr || u_bonus == nullptr || accept_len == nullptr || out_tok == nullptr ||
+      out_node == nullptr)
+    return SPEC_TREE_E_PARAM;
+  if ((rc = check_rows(dtype, target_logits, row_stride, V))) return rc;
+  if ((rc = check_rows(dtype, draft_logits, draft_row_stride, V))) return rc;
+  if ((rc = check_tree(p, tree, V, true, true))) return rc;
+  st::VerifyLaunch L;
+  L.p = *p;
+  L.B = B;
+  L.V = V;
+  L.S = V;
+  L.dtype = dtype;
+  L.target = target_logits;
+  L.row_stride = row_stride;
+  L.tree = *tree;
+  L.u_verify = u_verify;
+  L.u_bonus = u_bonus;
+  L.accept_len = accept_len;
+  L.out_tok = out_tok;
+  L.out_node = out_node;
+  L.margins = margins;
+  L.status = status;
+  L.num_sms = num_sms_of_current_device();
+  L.draft = draft_logits;
+  L.draft_row_stride = draft_row_stride;
+  if (L.num_sms <= 0) return SPEC_TREE_E_CUDA;
+  return st::launch_verify_dense(L, as_stream(stream)) == cudaSuccess ? SPEC_TREE_OK : SPEC_TREE_E_CUDA;
 }
 
 const char* spec_tree_strerror(int code) {

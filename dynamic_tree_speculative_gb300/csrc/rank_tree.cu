@@ -58,7 +58,7 @@ struct RankShared {
   int16_t pos[SPEC_TREE_MAX_CAND];     // canonical node index, -1 = pruned
   // child table of every expanded row (entry row * K + slot)
   float ch_lp[SPEC_TREE_MAX_CAND];    // local probability used for the path score
-  int32_t ch_rk[SPEC_TREE_MAX_CAND];  // support rank | kind << 16
+  int32_t ch_rk[SPEC_TREE_MAX_CAND];  // support rank (low 16 bits) | kind << 16
   union {
     int32_t ord[SPEC_TREE_MAX_CAND];     // SMART, during the layers: the current layer by rank
     int32_t ch_tok[SPEC_TREE_MAX_CAND];  // after the layers: token id of each child-table entry
@@ -160,9 +160,11 @@ __device__ __forceinline__ void load_children(RankShared& s, const RankLaunch& L
         lp = rank == slot ? qa[u] : qb[u];
       }
       s.ch_lp[e0 + idx] = lp;
-      s.ch_rk[e0 + idx] = rank | (kind << 16);
+      s.ch_rk[e0 + idx] = (rank & 0xffff) | (kind << 16);
       const int64_t row = static_cast<int64_t>(b) * t.n_rows + r;
-      tok.v[u] = t.sup_id[row * t.sup_stride + rank];
+      // a dense support keeps ranks 0..K-1 and the probe at entry K
+      const int entry = kind == SPEC_TREE_PROBE && rank > L.probe_entry_cap ? L.probe_entry_cap : rank;
+      tok.v[u] = t.sup_id[row * t.sup_stride + entry];
     }
   }
 }

@@ -42,8 +42,11 @@ constexpr int SW_CAP = 2048;   // table path: candidates
 
 struct WideShared {
   union {
-    uint16_t tbl[SW_TBL];           // table path: 16-bit order key of each vector's maximum
-    uint32_t whist[SW_WARPS][256];  // radix path: per-warp digit histograms
+    uint16_t tbl[SW_TBL];  // table path: 16-bit order key of each vector's maximum
+    struct {
+      uint32_t whist[SW_WARPS][256];                // radix path: per-warp digit histograms
+      unsigned long long wmass[SW_WARPS][256];      // dense support: per-warp fixed-point weights
+    };
   };
   uint64_t cand[SW_CAP];            // candidates; at the end the top-|S| in rank order
   uint32_t list[SW_CAP];            // table path: vectors to gather
@@ -59,6 +62,11 @@ struct WideShared {
   int cnt;
   int probe;
   int last_pos;
+  // dense support
+  unsigned long long hmass[256];
+  unsigned long long red64[2][SW_WARPS];
+  unsigned long long above_mass;
+  int nth_id;
 };
 
 // Calls f(key, id) for every element of the row that thread tid owns: the
@@ -558,6 +566,314 @@ __global__ void __launch_bounds__(SW_THREADS, 2) select_wide_kernel(SelLaunch a,
   const int n = min(s.n_cand, a.S);
   wide_epilogue<T>(s, a, out_row, in_row, n);
   if (nonfinite) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
+}
+
+// ------------------------------------------------------------ dense support ---
+// |S| = V for a vocabulary of more than SPEC_TREE_MAX_SUPPORT tokens
+// (RheoSampling notes, Key design 1: the dense row of the support-size
+// ablation; Key design 2 over the whole vocabulary).  One CTA per draft row.
+// A row's support arrays hold ranks 0..K-1 (every child but the probe lives
+// there: DET ranks 0..m-1, fillers below rank K) and, at entry K, the probe,
+// whose rank (probe_pos) may lie anywhere in the tail.
+//   ranks 0..K-1: the radix select, collect and sort above with |S| = K;
+//   sums: with l_max the rank-0 logit, fixed-point sums (units of 2^-40 of
+//     the largest weight) of e = exp(l - l_max) and e_T = exp((l - l_max) / T);
+//   probe: the tail's inverse CDF in rank order as a weighted radix select.
+//     On the fixed-point scale the target is the DET mass plus u times the
+//     tail mass (every DET element precedes every tail element in rank order).
+//     One 8-bit digit of the key at a time from the top, per-warp histograms of
+//     the weights locate the digit whose cumulative interval holds the target
+//     (at the last digit a bin is one key, all of whose elements weigh the
+//     same, so counts suffice); the probe is element j, in id order, of that
+//     key k*, j = (target - weight above k*) / weight(k*), and its rank is the
+//     number of elements above k* plus j.  The weights are integers, so the
+//     interval arithmetic is exact: the float32 exponentials are the only
+//     rounding.
+
+constexpr float SD_FX_SCALE = 1099511627776.0f;  // 2^40
+
+// Fixed-point weight exp2((l - lmax) * c) in units of 2^-40: at most 2^40, so
+// the sum over a row of up to 2^24 elements fits 64 bits.  NaN weighs 0.
+__device__ __forceinline__ unsigned long long dense_wfx(float l, float lmax, float c) {
+  const float w = exp2f((l - lmax) * c);
+  return w > 0.0f ? __float2ull_rn(w * SD_FX_SCALE) : 0ull;
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  return v;
+}
+
+// The element at which the fixed-point weight, accumulated in rank order (key
+// descending, id ascending), first exceeds `target` (< the row's total): its
+// key, the number of elements above that key and their weight.  All threads call it.
+template <typename T>
+__device__ void dense_weighted_select(WideShared& s, const uint8_t* row, int V, int nvec, float lmax, float c,
+                                      unsigned long long target, bool& nonfinite, uint32_t& key_out,
+                                      uint32_t& above_cnt, unsigned long long& above_mass) {
+  constexpr int KEY_BITS = Elem<T>::KEY_BITS, LEVELS = KEY_BITS / 8;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = 0u, pmask = 0u, acnt = 0u;
+  unsigned long long amass = 0ull;
+  for (int d = 0; d < LEVELS; ++d) {
+    const int shift = KEY_BITS - 8 * (d + 1);
+    const bool last = d == LEVELS - 1;
+    for (int i = tid; i < SW_WARPS * 256; i += SW_THREADS) {
+      (&s.whist[0][0])[i] = 0u;
+      (&s.wmass[0][0])[i] = 0ull;
+    }
+    __syncthreads();
+    uint32_t* wh = s.whist[warp];
+    unsigned long long* wm = s.wmass[warp];
+    const uint32_t pf = prefix, pm = pmask;
+    // a thread adds a run of elements in one bin to the histogram when the run ends
+    int run_bin = -1;
+    unsigned long long run_mass = 0ull;
+    for_each_elem<T>(row, V, nvec, nonfinite, [&](uint32_t key, uint32_t) {
+      if ((key & pm) != pf) return;
+      const int bin = static_cast<int>((key >> shift) & 0xffu);
+      atomicAdd(&wh[bin], 1u);
+      if (!last) {
+        if (bin != run_bin) {
+          if (run_bin >= 0 && run_mass != 0ull) atomicAdd(&wm[run_bin], run_mass);
+          run_bin = bin;
+          run_mass = 0ull;
+        }
+        run_mass += dense_wfx(key_value<T>(key), lmax, c);
+      }
+    });
+    if (run_bin >= 0 && run_mass != 0ull) atomicAdd(&wm[run_bin], run_mass);
+    __syncthreads();
+    if (tid < 256) {
+      uint32_t cnt = 0u;
+      unsigned long long mass = 0ull;
+      for (int w = 0; w < SW_WARPS; ++w) {
+        cnt += s.whist[w][tid];
+        mass += s.wmass[w][tid];
+      }
+      if (last) mass = cnt ? cnt * dense_wfx(key_value<T>(prefix | (static_cast<uint32_t>(tid) << shift)), lmax, c) : 0ull;
+      s.hist[tid] = cnt;
+      s.hmass[tid] = mass;
+    }
+    if (tid == 0) s.bin = -1;
+    __syncthreads();
+    if (warp == 0) {
+      // bins from the top: lane l holds bins 255 - 8 l - j
+      unsigned long long hm[8], tot = 0ull;
+      uint32_t hc[8], ctot = 0u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        hm[j] = s.hmass[255 - 8 * lane - j];
+        hc[j] = s.hist[255 - 8 * lane - j];
+        tot += hm[j];
+        ctot += hc[j];
+      }
+      unsigned long long incl = tot;
+      uint32_t cincl = ctot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(FULL, incl, o);
+        const uint32_t cy = __shfl_up_sync(FULL, cincl, o);
+        if (lane >= o) {
+          incl += y;
+          cincl += cy;
+        }
+      }
+      const unsigned long long need = target - amass;
+      unsigned long long acc = incl - tot;
+      uint32_t cacc = cincl - ctot;
+      if (acc <= need && need < incl) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (acc <= need && need < acc + hm[j]) {
+            s.bin = 255 - 8 * lane - j;
+            s.above_mass = acc;
+            s.above = static_cast<int>(cacc);
+            s.cnt = static_cast<int>(hc[j]);
+          }
+          acc += hm[j];
+          cacc += hc[j];
+        }
+      }
+    }
+    __syncthreads();
+    const int bin = s.bin;
+    if (bin < 0) break;  // not reached: the target is below the row's total (block-uniform)
+    amass += s.above_mass;
+    acnt += static_cast<uint32_t>(s.above);
+    prefix |= static_cast<uint32_t>(bin) << shift;
+    pmask |= 0xffu << shift;
+    __syncthreads();  // every thread has read the bin
+  }
+  key_out = prefix;
+  above_cnt = acnt;
+  above_mass = amass;
+}
+
+// Id of element j (0-based, in id order) among the row's elements with order key `key`.
+template <typename T>
+__device__ int nth_with_key(WideShared& s, const uint8_t* row, int V, int nvec, uint32_t key, int j, bool& nonfinite) {
+  constexpr int VEC = Elem<T>::VEC;
+  const int tid = threadIdx.x;
+  if (tid == 0) s.nth_id = -1;
+  __syncthreads();
+  int taken = 0;
+  const int rounds = (nvec + SW_THREADS - 1) / SW_THREADS + 1;  // the last round: the scalar tail
+  for (int r = 0; r < rounds; ++r) {
+    uint32_t keys[VEC];
+    uint32_t id0;
+    int nel = 0;
+    if (r + 1 < rounds) {
+      const int vi = r * SW_THREADS + tid;
+      id0 = static_cast<uint32_t>(vi * VEC);
+      if (vi < nvec) {
+        const uint4 v = ldg_stream(row + static_cast<int64_t>(vi) * 16);
+#pragma unroll
+        for (int q = 0; q < VEC; ++q) keys[q] = elem_key<T>(v, q, nonfinite);
+        nel = VEC;
+      }
+    } else {
+      const int id = nvec * VEC + tid;
+      id0 = static_cast<uint32_t>(id);
+      if (id < V) {
+        keys[0] = scalar_key<T>(row, id, nonfinite);
+        nel = 1;
+      }
+    }
+    int cnt = 0;
+#pragma unroll
+    for (int q = 0; q < VEC; ++q) cnt += (q < nel && keys[q] == key);
+    int total;
+    int rank = block_excl_scan(s, cnt, &total) + taken;
+    if (rank <= j && j < rank + cnt) {
+#pragma unroll
+      for (int q = 0; q < VEC; ++q)
+        if (q < nel && keys[q] == key) {
+          if (rank == j) s.nth_id = static_cast<int>(id0 + q);
+          ++rank;
+        }
+    }
+    taken += total;
+    if (taken > j) break;
+  }
+  __syncthreads();
+  return s.nth_id;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(SW_THREADS, 2) select_dense_kernel(SelLaunch a, int64_t row_bytes) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  WideShared& s = *reinterpret_cast<WideShared*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t g = blockIdx.x;
+  const int64_t b = g / a.rows_used, e = g % a.rows_used;
+  const int64_t out_row = b * a.n_rows + a.sup_row0 + e;
+  const int64_t in_row = b * a.in_rows + e;
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const uint8_t* row = static_cast<const uint8_t*>(a.logits) + in_row * row_bytes;
+  const int nvec = static_cast<int>((static_cast<int64_t>(a.V) * Elem<T>::ES) / 16);
+  bool nonfinite = false;
+  const int K = a.S;  // support ranks kept: 0..K-1
+
+  // ranks 0..K-1
+  uint32_t prefix, pmask;
+  int need;
+  bool exact;
+  radix_select_row<T>(s, row, a.V, nvec, K, nonfinite, prefix, pmask, need, exact);
+  collect_row<T>(s, row, a.V, nvec, prefix, pmask, need, exact, nonfinite);
+  const int n = min(s.n_cand, K);
+  sort_cand_desc(s, n);
+
+  // fixed-point sums of e and e_T over the row
+  const float lmax = key_value<T>(static_cast<uint32_t>(s.cand[0] >> 32));
+  const float c1 = 1.4426950408889634f;
+  const float cT = a.temperature == 1.0f ? c1 : c1 / a.temperature;
+  const bool same = a.temperature == 1.0f;
+  unsigned long long se = 0ull, seT = 0ull;
+  for_each_elem<T>(row, a.V, nvec, nonfinite, [&](uint32_t key, uint32_t) {
+    const float l = key_value<T>(key);
+    const unsigned long long w1 = dense_wfx(l, lmax, c1);
+    se += w1;
+    seT += same ? w1 : dense_wfx(l, lmax, cT);
+  });
+  se = warp_sum_u64(se);
+  seT = warp_sum_u64(seT);
+  if (lane == 0) {
+    s.red64[0][warp] = se;
+    s.red64[1][warp] = seT;
+  }
+  __syncthreads();
+  se = 0ull;
+  seT = 0ull;
+  for (int w = 0; w < SW_WARPS; ++w) {
+    se += s.red64[0][w];
+    seT += s.red64[1][w];
+  }
+  // the DET elements (ranks 0..m-1) and their weights
+  unsigned long long det1 = 0ull, detT = 0ull;
+  for (int r = 0; r < a.m && r < n; ++r) {
+    const float l = key_value<T>(static_cast<uint32_t>(s.cand[r] >> 32));
+    det1 += dense_wfx(l, lmax, c1);
+    detT += dense_wfx(l, lmax, cT);
+  }
+  const unsigned long long tailT = seT - detT;
+  const bool draw = a.draw_probe && a.m < a.V && tailT > 0ull;  // block-uniform
+  int probe_rank = -1, probe_id = -1;
+  float probe_l = 0.0f;
+  if (draw) {
+    const float u = a.u_probe[in_row];
+    unsigned long long target = detT + static_cast<unsigned long long>(static_cast<double>(u) *
+                                                                       static_cast<double>(tailT));
+    if (target >= seT) target = seT - 1ull;
+    uint32_t kstar, acnt;
+    unsigned long long amass;
+    dense_weighted_select<T>(s, row, a.V, nvec, lmax, cT, target, nonfinite, kstar, acnt, amass);
+    const unsigned long long wk = dense_wfx(key_value<T>(kstar), lmax, cT);
+    int j = wk ? static_cast<int>((target - amass) / wk) : 0;
+    if (j > s.cnt - 1) j = s.cnt - 1;  // s.cnt: elements of key k*
+    if (j < 0) j = 0;
+    probe_id = nth_with_key<T>(s, row, a.V, nvec, kstar, j, nonfinite);
+    probe_rank = static_cast<int>(acnt) + j;
+    probe_l = key_value<T>(kstar);
+  }
+  const double inv1 = 1.0 / static_cast<double>(se), invT = 1.0 / static_cast<double>(seT);
+  const int64_t base = out_row * a.sup_stride;
+  for (int r = tid; r < n; r += SW_THREADS) {
+    const uint64_t x = s.cand[r];
+    const float l = key_value<T>(static_cast<uint32_t>(x >> 32));
+    a.sup_id[base + r] = static_cast<int32_t>(~static_cast<uint32_t>(x));
+    a.sup_q[base + r] = static_cast<float>(static_cast<double>(dense_wfx(l, lmax, c1)) * inv1);
+    a.sup_qT[base + r] = static_cast<float>(static_cast<double>(dense_wfx(l, lmax, cT)) * invT);
+  }
+  if (tid == 0) {
+    a.sup_id[base + K] = probe_id;
+    a.sup_q[base + K] = draw ? static_cast<float>(static_cast<double>(dense_wfx(probe_l, lmax, c1)) * inv1) : 0.0f;
+    a.sup_qT[base + K] = draw ? static_cast<float>(static_cast<double>(dense_wfx(probe_l, lmax, cT)) * invT) : 0.0f;
+    a.sup_z[out_row] = static_cast<float>(static_cast<double>(se - det1) * inv1);
+    a.sup_zT[out_row] = static_cast<float>(static_cast<double>(tailT) * invT);
+    a.probe_pos[out_row] = draw && probe_id >= 0 ? probe_rank : -1;
+    if (!(lmax < INFINITY) || (draw && probe_id < 0)) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
+  }
+  if (nonfinite) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
+}
+
+cudaError_t launch_select_dense(int dtype, const SelLaunch& L, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(L.B) * L.rows_used;
+  if (rows == 0) return cudaSuccess;
+  const int smem = static_cast<int>(sizeof(WideShared));
+  if (dtype == SPEC_TREE_BF16) {
+    cudaError_t err = cudaFuncSetAttribute(select_dense_kernel<__nv_bfloat16>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(select_dense_kernel<__nv_bfloat16>, dim3(static_cast<unsigned>(rows)), dim3(SW_THREADS),
+                      static_cast<size_t>(smem), stream, L, L.row_stride * static_cast<int64_t>(2));
+  }
+  cudaError_t err = cudaFuncSetAttribute(select_dense_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(select_dense_kernel<float>, dim3(static_cast<unsigned>(rows)), dim3(SW_THREADS),
+                    static_cast<size_t>(smem), stream, L, L.row_stride * static_cast<int64_t>(4));
 }
 
 cudaError_t launch_select_wide(int dtype, const SelLaunch& L, cudaStream_t stream) {

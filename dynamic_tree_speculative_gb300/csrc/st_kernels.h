@@ -31,6 +31,7 @@ struct SelLaunch {
   int num_sms;
   int ctas_per_sm;
   int32_t* sched;  // the tree's row counter (or NULL)
+  bool dense;      // |S| = V > SPEC_TREE_MAX_SUPPORT: S is K, the ranks kept, plus the probe at entry K
 };
 
 struct RankLaunch {
@@ -39,6 +40,7 @@ struct RankLaunch {
   int64_t rows_avail;  // rows per tree that were expanded
   spec_tree_t tree;
   uint32_t* status;
+  int probe_entry_cap;  // support entry of a probe of deeper rank: K for a dense support, else INT32_MAX
   // layer mode only
   int layer;
   void* state;
@@ -60,17 +62,23 @@ struct VerifyLaunch {
   uint32_t* margins;
   uint32_t* status;
   int num_sms;
+  // dense support: the draft rows the tree was built from
+  const void* draft;
+  int64_t draft_row_stride;  // elements
 };
 
 size_t select_expand_smem_bytes();
 cudaError_t launch_select_expand(int dtype, const SelLaunch& L, cudaStream_t stream);
 // supports of 129 to 1024 tokens
 cudaError_t launch_select_wide(int dtype, const SelLaunch& L, cudaStream_t stream);
+// the dense support of a vocabulary above SPEC_TREE_MAX_SUPPORT tokens
+cudaError_t launch_select_dense(int dtype, const SelLaunch& L, cudaStream_t stream);
 cudaError_t launch_rank_topr(const RankLaunch& L, cudaStream_t stream);
 cudaError_t launch_rank_smart(const RankLaunch& L, cudaStream_t stream);
 size_t layer_state_bytes();
 cudaError_t launch_layer_topr(const RankLaunch& L, cudaStream_t stream);
 cudaError_t launch_layer_finish(const RankLaunch& L, cudaStream_t stream);
 cudaError_t launch_verify(const VerifyLaunch& L, cudaStream_t stream);
+cudaError_t launch_verify_dense(const VerifyLaunch& L, cudaStream_t stream);
 
 }  // namespace st

@@ -86,6 +86,13 @@ typedef struct CUstream_st* spec_tree_stream_t;
 
 /* Limits of this build. */
 #define SPEC_TREE_MAX_SUPPORT 1024
+/* support = SPEC_TREE_SUPPORT_DENSE: |S| = V, the whole vocabulary (the
+ * pages' "full dense" support).  Above SPEC_TREE_MAX_SUPPORT tokens the
+ * support arrays keep only ranks 0..K-1 and the probe (see spec_tree_t), K is
+ * at most SPEC_TREE_DENSE_MAX_K, and verification takes the draft rows too
+ * (spec_tree_verify_dense). */
+#define SPEC_TREE_SUPPORT_DENSE 0x40000000
+#define SPEC_TREE_DENSE_MAX_K 64
 #define SPEC_TREE_MAX_CAND 2048 /* K + (depth-1)*W*K for the top-R builder; K*R for SMART */
 #define SPEC_TREE_MAX_NODES 512 /* R + 1 */
 
@@ -101,7 +108,8 @@ typedef struct CUstream_st* spec_tree_stream_t;
  *            node budget (SMART).  Node arrays hold R + 1 entries.
  *   support  |S| = min(support, V); 0 means 128.  1 <= support <= 1024 (the
  *            pages' ablation: 128, 256, 512, 1024; support >= V is the dense
- *            support of a vocabulary of at most 1024 tokens).
+ *            support of a vocabulary of at most 1024 tokens), or
+ *            SPEC_TREE_SUPPORT_DENSE: |S| = V for any vocabulary.
  *   temperature T > 0: probe sampling and verification use q_T and
  *            p = softmax(t / T); ranking uses untempered q.
  *   builder  SPEC_TREE_BUILDER_TOPR or SPEC_TREE_BUILDER_SMART.
@@ -142,6 +150,11 @@ typedef struct spec_tree_params {
  *   untempered / tempered truncated softmax; sup_z / sup_zT tail masses over
  *   ranks m..|S|-1; probe_pos rank of the probe in S (-1: no probe).
  *   `sup_stride` is the per-row capacity of sup_id/sup_q/sup_qT (>= |S|).
+ *   Dense support of V > SPEC_TREE_MAX_SUPPORT tokens: entries 0..K-1 hold
+ *   support ranks 0..K-1 (all children but the probe come from there) and
+ *   entry K the probe (its id, q and q_T; probe_pos is still its rank in the
+ *   whole vocabulary), so sup_stride >= K + 1; q, q_T and the tail masses are
+ *   over the whole vocabulary.
  * Row schedule (optional, may be NULL):
  *   sched        device uint32[2], zero before the first call that uses it.
  *                The support selection hands draft rows to its CTAs on demand
@@ -249,6 +262,30 @@ int spec_tree_verify(const spec_tree_params* p, int B, int V, int dtype,
                      const spec_tree_t* tree, const float* u_verify, const float* u_bonus,
                      int32_t* accept_len, int32_t* out_tok, int32_t* out_node,
                      uint32_t* margins, uint32_t* status, spec_tree_stream_t stream);
+
+/*
+ * spec_tree_verify for a tree built on the dense support of a vocabulary of
+ * more than SPEC_TREE_MAX_SUPPORT tokens (support = SPEC_TREE_SUPPORT_DENSE;
+ * RheoSampling notes, Key design 3 with Key design 1's dense support).  The
+ * tail law q~_T(v) = q_T(v) / z_T then covers every token but the m
+ * deterministic ones, and the tree's support arrays keep only its first
+ * ranks, so the kernel recomputes q_T(v) = exp((d_v - d_max) / T) q_T(x_1)
+ * from the node's draft row d (d_max its rank-0 logit): the residual mass
+ * 1 - sum_tail min(p, q~_T) and the bonus then take a pass over the target
+ * and the draft row of the node.
+ *   draft_logits: the draft rows the tree was built from, [B][tree->n_rows]
+ *                 [draft_row_stride] of dtype, 16-byte aligned rows; only the
+ *                 rows of accepted-path nodes whose probe was rejected are read.
+ * Everything else is as for spec_tree_verify.  Returns SPEC_TREE_E_PARAM for
+ * a tree whose support is not dense, or V <= SPEC_TREE_MAX_SUPPORT (where
+ * spec_tree_verify handles the dense support).
+ */
+int spec_tree_verify_dense(const spec_tree_params* p, int B, int V, int dtype,
+                           const void* target_logits, int64_t row_stride,
+                           const void* draft_logits, int64_t draft_row_stride,
+                           const spec_tree_t* tree, const float* u_verify, const float* u_bonus,
+                           int32_t* accept_len, int32_t* out_tok, int32_t* out_node,
+                           uint32_t* margins, uint32_t* status, spec_tree_stream_t stream);
 
 /*
  * Layer mode: the top-R tree of spec_tree_build, built one layer per call so

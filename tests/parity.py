@@ -68,14 +68,20 @@ def target_for(case: Case, trees: dict, seed: int):
 def run_gpu(case: Case, target=None, device="cuda"):
     wl = case.wl
     params = B.Params.from_workload(wl)
-    tree = B.TreeBuffers(params, wl.B, device=device)
+    tree = B.TreeBuffers(params, wl.B, device=device, V=wl.V)
     status = torch.zeros(1, dtype=torch.int32, device=device)
-    B.spec_tree_build(params, wl.V, case.draft.to(device), case.u_probe.to(device), tree, status)
+    draft = case.draft.to(device)
+    B.spec_tree_build(params, wl.V, draft, case.u_probe.to(device), tree, status)
     res = {"tree": tree, "status": status}
     if target is not None:
         out = B.VerifyOutputs(params, wl.B, device=device)
-        B.spec_tree_verify(params, wl.V, target.to(device), tree, case.u_verify.to(device),
-                           case.u_bonus.to(device), out.accept_len, out.out_tok, out.out_node, out.margins, status)
+        if B.is_dense(params, wl.V):
+            B.spec_tree_verify_dense(params, wl.V, target.to(device), draft, tree, case.u_verify.to(device),
+                                     case.u_bonus.to(device), out.accept_len, out.out_tok, out.out_node, out.margins,
+                                     status)
+        else:
+            B.spec_tree_verify(params, wl.V, target.to(device), tree, case.u_verify.to(device),
+                               case.u_bonus.to(device), out.accept_len, out.out_tok, out.out_node, out.margins, status)
         res["verify"] = out
     torch.cuda.synchronize()
     host = {k: getattr(tree, k).cpu().numpy() for k in (

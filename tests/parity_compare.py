@@ -41,18 +41,31 @@ class ParityError(AssertionError):
 
 # ------------------------------------------------------------------ build ---
 
-def _support_diffs(g, b, t: O.Tree, S: int):
-    """Rows of the oracle's tree whose support ids, probabilities or masses differ."""
+def _support_diffs(g, b, t: O.Tree, S: int, K: int):
+    """Rows of the oracle's tree whose support ids, probabilities or masses differ.
+
+    A dense support of a vocabulary larger than the GPU's support arrays keeps
+    support ranks 0..K-1 and, at entry K, the probe: those are compared.
+    """
     ids, probs, probes = [], [], []
+    dense = S > g["sup_id"].shape[2]
+    n = K if dense else S
     for e, ex in t.expansions.items():
-        if not np.array_equal(g["sup_id"][b, e, :S].astype(np.int64), ex.sup_id):
+        if not np.array_equal(g["sup_id"][b, e, :n].astype(np.int64), ex.sup_id[:n]):
             ids.append(e)
-        if not (np.allclose(g["sup_q"][b, e, :S], ex.q, atol=PROB_TOL, rtol=0)
-                and np.allclose(g["sup_qT"][b, e, :S], ex.qT, atol=PROB_TOL, rtol=0)
+        if not (np.allclose(g["sup_q"][b, e, :n], ex.q[:n], atol=PROB_TOL, rtol=0)
+                and np.allclose(g["sup_qT"][b, e, :n], ex.qT[:n], atol=PROB_TOL, rtol=0)
                 and abs(g["sup_z"][b, e] - ex.z) <= PROB_TOL and abs(g["sup_zT"][b, e] - ex.zT) <= PROB_TOL):
             probs.append(e)
-        if int(g["probe_pos"][b, e]) != ex.probe_pos:
+        pp = int(g["probe_pos"][b, e])
+        if pp != ex.probe_pos:
             probes.append(e)
+        elif dense and pp >= 0:
+            # the probe entry: the oracle's token, q and q_T at that rank
+            if int(g["sup_id"][b, e, K]) != int(ex.sup_id[pp]):
+                ids.append(e)
+            elif abs(g["sup_q"][b, e, K] - ex.q[pp]) > PROB_TOL or abs(g["sup_qT"][b, e, K] - ex.qT[pp]) > PROB_TOL:
+                probs.append(e)
     return ids, probs, probes
 
 
@@ -145,7 +158,7 @@ def compare_build_tree(g, b: int, rows, u_probe, op: O.Params, S: int, first: O.
             t = first if (first is not None and not rp) else O.build(rows, u_probe, op, rp if rp else None)
         except O.ReplayRefused as e:
             raise ParityError(f"tree {b}: difference not at a near-tie: {e}") from None
-        ids, probs, probes = _support_diffs(g, b, t, S)
+        ids, probs, probes = _support_diffs(g, b, t, S, op.K)
         if ids:
             raise ParityError(f"tree {b}: support ids differ in rows {ids[:8]}")
         if probs:

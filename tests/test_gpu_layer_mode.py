@@ -79,6 +79,8 @@ def check_layer_mode(wl, seed, sample=None, row_stride=None):
     # the support rows each call expanded
     rows = _written_rows(params, wl)
     S = min(wl.support, wl.V)
+    if S > B.MAX_SUPPORT:
+        S = wl.K + 1  # a dense support keeps ranks 0..K-1 and the probe
     for f in SUP_FIELDS:
         a, o = lay[f][:, rows], one[f][:, rows]
         if f in ("sup_id", "sup_q", "sup_qT"):
@@ -134,6 +136,8 @@ LAYER_CASES = {
     "f32_ragged": ("vicuna", dict(B=8, V=4099, K=6, W=3, depth=3, R=10, dtype="f32", stride=4100), None),
     "depth1": ("vicuna", dict(B=8, V=3000, depth=1, R=8), None),
     "llama3": ("llama3", dict(), [0, 5]),
+    # the dense support of a large vocabulary (ranks 0..K-1 and the probe kept per row)
+    "dense": ("vicuna", dict(B=4, V=20000, depth=4, R=20, support=0x40000000), None),
 }
 
 

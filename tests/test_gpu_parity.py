@@ -140,6 +140,45 @@ def test_edge_cases(name):
     _report(name, parity.run_parity(wl, 11, row_stride=stride))
 
 
+DENSE = 0x40000000  # support = the whole vocabulary (SPEC_TREE_SUPPORT_DENSE)
+
+DENSE_CASES = {
+    # the pages' "full dense" support at the pages' vocabularies
+    "vicuna": dict(B=4),
+    "m0": dict(B=6, V=20000, K=4, m=0, W=4, depth=4, R=16),
+    "m2": dict(B=6, V=20000, K=6, m=2, W=3, depth=4, R=16),
+    "probe_last_no_fillers": dict(B=8, V=20000, K=2, m=1, W=2, depth=5, R=14, verify_order="rrsw"),
+    "probe_last": dict(B=6, V=20000, K=4, m=1, W=4, depth=4, R=16, verify_order="rrsw"),
+    "f32_ragged": dict(B=4, V=5003, K=6, m=1, W=3, depth=3, R=10, dtype="f32", stride=5004),
+    "bf16_ragged": dict(B=4, V=4099, K=6, m=1, W=3, depth=3, R=10, stride=4104),
+    "cold": dict(B=6, V=20000, K=6, m=1, W=3, depth=4, R=16, temperature=0.5),
+    "hot": dict(B=6, V=20000, K=6, m=1, W=3, depth=4, R=16, temperature=1.7),
+    "topk_m_eq_K": dict(B=4, V=20000, K=4, m=4, W=4, depth=4, R=16),
+    "smart": dict(B=6, V=32000, builder="smart"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DENSE_CASES))
+def test_dense_support(name):
+    """|S| = V (the support-size ablation's dense row): ranks 0..K-1 and the probe drawn from the whole
+    tempered tail in rank order, verification against q~_T over the whole vocabulary."""
+    kw = dict(DENSE_CASES[name])
+    stride = kw.pop("stride", None)
+    wl = WL.WORKLOADS["vicuna"].with_(support=DENSE, **kw)
+    out = parity.run_parity(wl, 31, row_stride=stride)
+    _report(f"dense_{name}", out)
+    # the probes come from deep in the tail too, not only from the first 128 ranks
+    pp = out["gpu"]["probe_pos"]
+    if name == "vicuna":
+        assert (pp >= 128).any(), pp.max()
+
+
+def test_dense_support_llama_vocab():
+    """The dense support at the LLaMA-3 vocabulary (V = 128256), every tree of a small batch."""
+    wl = WL.WORKLOADS["llama3"].with_(B=3, support=DENSE)
+    _report("dense_llama3", parity.run_parity(wl, 32))
+
+
 def test_wide_support_llama_vocab():
     """Support 1024 at the LLaMA-3 vocabulary (V = 128256), every tree of a small batch."""
     wl = WL.WORKLOADS["llama3"].with_(B=4, support=1024)

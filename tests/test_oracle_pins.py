@@ -398,6 +398,21 @@ def test_losslessness_exact_first_token(seed, R, m, T):
     np.testing.assert_allclose(law, p_full, atol=1e-12, rtol=0)
 
 
+@pytest.mark.parametrize("m,T", [(1, 1.0), (0, 0.8), (2, 1.3)])
+def test_losslessness_exact_first_token_dense_support(m, T):
+    """The dense support (|S| = V = 300, a tail reaching past rank 128): summed over probe identities,
+    the first emitted token has law p exactly (Key design 1's dense row with Key design 3)."""
+    p = O.Params(K=4, m=m, W=4, depth=2, R=6, temperature=T, support=1 << 30)
+    n_rows = 1 + (p.depth - 1) * p.W
+    rows = _tiny_rows(500 + m, n_rows, V=300)
+    u_rest = np.random.default_rng(m).random(n_rows)
+    target = WL.to_numpy_f64(WL.latent_rows((m, "tgt-dense"), 1, 300, 1.2, 0.5))[0]
+    ex = O.expand_row(rows[0], p, 0.5)
+    assert len(ex.sup_id) == 300 and ex.qT[128:].sum() > 1e-3
+    law, p_full = _first_token_law(rows, u_rest, p, target)
+    np.testing.assert_allclose(law, p_full, atol=1e-12, rtol=0)
+
+
 def test_rrsw_without_fillers_is_lossless():
     """Probe-last (RRSw schedule) is a valid sampler when the candidates do not depend on the probe.
 
