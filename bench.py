@@ -29,6 +29,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "verified trees/sec and logit GB/s (fraction of GB300 HBM peak) at 128K vocab"
+DENSE = 0x40000000  # support = the whole vocabulary
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -47,6 +48,7 @@ def parse_args():
     ap.add_argument("--sweep", action="store_true",
                     help="one JSON line per configuration: the workloads, the batch sweep with both builders, "
                          "the wide supports (single GPU; not the contract line)")
+    ap.add_argument("--only", default=None, help="--sweep: configurations whose name contains this text")
     return ap.parse_args()
 
 
@@ -472,6 +474,9 @@ def sweep_configs():
             cfgs.append(base.with_(name=f"sweep_{builder}_b{b}", B=b, builder=builder))
     for sup in (256, 512, 1024):
         cfgs.append(WL.BENCH_WORKLOAD.with_(name=f"llama3_b64_support{sup}", support=sup))
+    # the dense support (|S| = V)
+    cfgs.append(WL.BENCH_WORKLOAD.with_(name="llama3_b64_dense", support=DENSE))
+    cfgs.append(WL.BENCH_WORKLOAD.with_(name="llama3_b8_dense", B=8, support=DENSE))
     return cfgs
 
 
@@ -484,13 +489,15 @@ def run_sweep(args):
     hbm, peak_kind = peaks()
     steps = min(args.steps, 200)
     for wl in sweep_configs():
+        if args.only and args.only not in wl.name:
+            continue
         params = B.Params.from_workload(wl)
         cp = params.c()
         n_rows = B.rows_needed(params)
         draft, latent = WL.draft_logits(wl, args.seed, n_rows=n_rows, device=dev)
         u_probe = WL.build_uniforms(wl, args.seed, n_rows, device=dev)
         uv, ub = WL.verify_uniforms(wl, args.seed, device=dev)
-        tree = B.TreeBuffers(params, wl.B, device=dev)
+        tree = B.TreeBuffers(params, wl.B, device=dev, V=wl.V)
         out = B.VerifyOutputs(params, wl.B, device=dev)
         status = torch.zeros(1, dtype=torch.int32, device=dev)
         B.spec_tree_build(cp, wl.V, draft, u_probe, tree, status)
@@ -498,6 +505,7 @@ def run_sweep(args):
         target = WL.target_logits(wl, args.seed, latent, tree.node_exp_row, device=dev)
         del latent
         stream = torch.cuda.current_stream()
+        dense = B.is_dense(params, wl.V)
 
         def step(ev=None):
             if ev is not None:
@@ -506,8 +514,12 @@ def run_sweep(args):
             if ev is not None:
                 ev[1].record(stream)
             B.spec_tree_rank(cp, wl.V, tree, status, stream)
-            B.spec_tree_verify(cp, wl.V, target, tree, uv, ub, out.accept_len, out.out_tok, out.out_node, None,
-                               status, stream)
+            if dense:
+                B.spec_tree_verify_dense(cp, wl.V, target, draft, tree, uv, ub, out.accept_len, out.out_tok,
+                                         out.out_node, None, status, stream)
+            else:
+                B.spec_tree_verify(cp, wl.V, target, tree, uv, ub, out.accept_len, out.out_tok, out.out_node, None,
+                                   status, stream)
 
         for _ in range(max(args.warmup, 3)):
             step()
@@ -524,6 +536,8 @@ def run_sweep(args):
         acc = out.accept_len.cpu()
         es = 2 if wl.dtype == "bf16" else 4
         S = min(wl.support, wl.V)
+        if dense:
+            S = wl.K + 1  # ranks 0..K-1 and the probe are written
         draft_bytes = wl.B * n_rows * wl.V * es
         sup_bytes = wl.B * n_rows * (S * 12 + 12)
         step_bytes = draft_bytes + sup_bytes + int((acc.long() + 1).sum()) * wl.V * es
@@ -539,6 +553,8 @@ def run_sweep(args):
         del draft, target, tree, out
         torch.cuda.empty_cache()
     for b in (8, 64):
+        if args.only and args.only not in f"layer_mode_b{b}":
+            continue
         print(json.dumps(sweep_layer_mode(WL.BENCH_WORKLOAD.with_(name=f"layer_mode_b{b}", B=b), args)), flush=True)
     return 0
 
