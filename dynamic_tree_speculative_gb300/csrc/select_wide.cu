@@ -605,13 +605,64 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
   return v;
 }
 
+// Per-thread run of elements that fall in one histogram bin: counted (and
+// weighed) once when the run ends, so that the bins most elements share (the
+// tail's few exponents) take one shared atomic per run, not per element.
+struct BinRun {
+  int bin = -1;
+  uint32_t cnt = 0u;
+  unsigned long long mass = 0ull;
+  __device__ __forceinline__ void add(int b, unsigned long long w, uint32_t* wh, unsigned long long* wm) {
+    if (b != bin) {
+      flush(wh, wm);
+      bin = b;
+    }
+    ++cnt;
+    mass += w;
+  }
+  __device__ __forceinline__ void flush(uint32_t* wh, unsigned long long* wm) {
+    if (cnt) atomicAdd(&wh[bin], cnt);
+    if (mass) atomicAdd(&wm[bin], mass);
+    cnt = 0u;
+    mass = 0ull;
+  }
+};
+
+__device__ __forceinline__ void dense_clear_hist(WideShared& s) {
+  for (int i = threadIdx.x; i < SW_WARPS * 256; i += SW_THREADS) {
+    (&s.whist[0][0])[i] = 0u;
+    (&s.wmass[0][0])[i] = 0ull;
+  }
+}
+
+// The per-warp histograms summed into s.hist (counts) and s.hmass (weights);
+// at the last digit a bin is one key, weighed as its count times its weight.
+template <typename T>
+__device__ __forceinline__ void dense_reduce_hist(WideShared& s, bool last, uint32_t prefix, int shift, float lmax,
+                                                  float c) {
+  const int tid = threadIdx.x;
+  if (tid < 256) {
+    uint32_t cnt = 0u;
+    unsigned long long mass = 0ull;
+    for (int w = 0; w < SW_WARPS; ++w) {
+      cnt += s.whist[w][tid];
+      mass += s.wmass[w][tid];
+    }
+    if (last) mass = cnt ? cnt * dense_wfx(key_value<T>(prefix | (static_cast<uint32_t>(tid) << shift)), lmax, c) : 0ull;
+    s.hist[tid] = cnt;
+    s.hmass[tid] = mass;
+  }
+}
+
 // The element at which the fixed-point weight, accumulated in rank order (key
 // descending, id ascending), first exceeds `target` (< the row's total): its
-// key, the number of elements above that key and their weight.  All threads call it.
+// key, the number of elements above that key and their weight.  With
+// `level0_ready` the first digit's histograms are in s.hist / s.hmass already.
+// All threads call it.
 template <typename T>
 __device__ void dense_weighted_select(WideShared& s, const uint8_t* row, int V, int nvec, float lmax, float c,
-                                      unsigned long long target, bool& nonfinite, uint32_t& key_out,
-                                      uint32_t& above_cnt, unsigned long long& above_mass) {
+                                      unsigned long long target, bool level0_ready, bool& nonfinite,
+                                      uint32_t& key_out, uint32_t& above_cnt, unsigned long long& above_mass) {
   constexpr int KEY_BITS = Elem<T>::KEY_BITS, LEVELS = KEY_BITS / 8;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t prefix = 0u, pmask = 0u, acnt = 0u;
@@ -619,42 +670,20 @@ __device__ void dense_weighted_select(WideShared& s, const uint8_t* row, int V, 
   for (int d = 0; d < LEVELS; ++d) {
     const int shift = KEY_BITS - 8 * (d + 1);
     const bool last = d == LEVELS - 1;
-    for (int i = tid; i < SW_WARPS * 256; i += SW_THREADS) {
-      (&s.whist[0][0])[i] = 0u;
-      (&s.wmass[0][0])[i] = 0ull;
-    }
-    __syncthreads();
-    uint32_t* wh = s.whist[warp];
-    unsigned long long* wm = s.wmass[warp];
-    const uint32_t pf = prefix, pm = pmask;
-    // a thread adds a run of elements in one bin to the histogram when the run ends
-    int run_bin = -1;
-    unsigned long long run_mass = 0ull;
-    for_each_elem<T>(row, V, nvec, nonfinite, [&](uint32_t key, uint32_t) {
-      if ((key & pm) != pf) return;
-      const int bin = static_cast<int>((key >> shift) & 0xffu);
-      atomicAdd(&wh[bin], 1u);
-      if (!last) {
-        if (bin != run_bin) {
-          if (run_bin >= 0 && run_mass != 0ull) atomicAdd(&wm[run_bin], run_mass);
-          run_bin = bin;
-          run_mass = 0ull;
-        }
-        run_mass += dense_wfx(key_value<T>(key), lmax, c);
-      }
-    });
-    if (run_bin >= 0 && run_mass != 0ull) atomicAdd(&wm[run_bin], run_mass);
-    __syncthreads();
-    if (tid < 256) {
-      uint32_t cnt = 0u;
-      unsigned long long mass = 0ull;
-      for (int w = 0; w < SW_WARPS; ++w) {
-        cnt += s.whist[w][tid];
-        mass += s.wmass[w][tid];
-      }
-      if (last) mass = cnt ? cnt * dense_wfx(key_value<T>(prefix | (static_cast<uint32_t>(tid) << shift)), lmax, c) : 0ull;
-      s.hist[tid] = cnt;
-      s.hmass[tid] = mass;
+    if (!(d == 0 && level0_ready)) {
+      dense_clear_hist(s);
+      __syncthreads();
+      uint32_t* wh = s.whist[warp];
+      unsigned long long* wm = s.wmass[warp];
+      const uint32_t pf = prefix, pm = pmask;
+      BinRun run;
+      for_each_elem<T>(row, V, nvec, nonfinite, [&](uint32_t key, uint32_t) {
+        if ((key & pm) != pf) return;
+        run.add(static_cast<int>((key >> shift) & 0xffu), last ? 0ull : dense_wfx(key_value<T>(key), lmax, c), wh, wm);
+      });
+      run.flush(wh, wm);
+      __syncthreads();
+      dense_reduce_hist<T>(s, last, prefix, shift, lmax, c);
     }
     if (tid == 0) s.bin = -1;
     __syncthreads();
@@ -709,6 +738,23 @@ __device__ void dense_weighted_select(WideShared& s, const uint8_t* row, int V, 
   key_out = prefix;
   above_cnt = acnt;
   above_mass = amass;
+}
+
+// The (r+1)-th largest, with multiplicity, of the KEY_BITS-bit keys x held
+// one per thread (0 <= r < blockDim.x), its bits fixed from the top by
+// block-wide counts.  All threads call it.
+template <int KEY_BITS>
+__device__ __forceinline__ uint32_t block_kth_largest_bits(uint32_t x, int r) {
+  uint32_t prefix = 0u;
+  int need = r + 1;
+  for (int bit = KEY_BITS - 1; bit >= 0; --bit) {
+    const uint32_t cand = prefix | (1u << bit);
+    const uint32_t hi = ~((1u << bit) - 1u);
+    const int cnt = __syncthreads_count((x & hi) == cand);
+    if (cnt >= need) prefix = cand;
+    else need -= cnt;
+  }
+  return prefix;
 }
 
 // Id of element j (0-based, in id order) among the row's elements with order key `key`.
@@ -776,28 +822,49 @@ __global__ void __launch_bounds__(SW_THREADS, 2) select_dense_kernel(SelLaunch a
   const int nvec = static_cast<int>((static_cast<int64_t>(a.V) * Elem<T>::ES) / 16);
   bool nonfinite = false;
   const int K = a.S;  // support ranks kept: 0..K-1
-
-  // ranks 0..K-1
-  uint32_t prefix, pmask;
-  int need;
-  bool exact;
-  radix_select_row<T>(s, row, a.V, nvec, K, nonfinite, prefix, pmask, need, exact);
-  collect_row<T>(s, row, a.V, nvec, prefix, pmask, need, exact, nonfinite);
-  const int n = min(s.n_cand, K);
-  sort_cand_desc(s, n);
-
-  // fixed-point sums of e and e_T over the row
-  const float lmax = key_value<T>(static_cast<uint32_t>(s.cand[0] >> 32));
+  constexpr int KEY_BITS = Elem<T>::KEY_BITS;
   const float c1 = 1.4426950408889634f;
   const float cT = a.temperature == 1.0f ? c1 : c1 / a.temperature;
   const bool same = a.temperature == 1.0f;
+
+  // pass 1 (from HBM): each thread's largest key; the row maximum
+  uint32_t tmax = 0u;
+  for_each_elem<T>(row, a.V, nvec, nonfinite, [&](uint32_t key, uint32_t) { tmax = max(tmax, key); });
+  uint32_t kmax = tmax;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(FULL, kmax, o));
+  if (lane == 0) s.hist[warp] = kmax;
+  __syncthreads();
+  kmax = 0u;
+  for (int w = 0; w < SW_WARPS; ++w) kmax = max(kmax, s.hist[w]);
+  const float lmax = key_value<T>(kmax);
+  // the K-th largest thread maximum: at least K elements reach it (thread maxima are distinct elements)
+  const uint32_t bound = block_kth_largest_bits<KEY_BITS>(tmax, K - 1);
+
+  // pass 2: every element at or above the bound as a candidate, the fixed-point
+  // sums of e and e_T, and the first digit's weighted histograms for the probe
+  if (tid == 0) s.n_cand = 0;
+  dense_clear_hist(s);
+  __syncthreads();
   unsigned long long se = 0ull, seT = 0ull;
-  for_each_elem<T>(row, a.V, nvec, nonfinite, [&](uint32_t key, uint32_t) {
-    const float l = key_value<T>(key);
-    const unsigned long long w1 = dense_wfx(l, lmax, c1);
-    se += w1;
-    seT += same ? w1 : dense_wfx(l, lmax, cT);
-  });
+  {
+    uint32_t* wh = s.whist[warp];
+    unsigned long long* wm = s.wmass[warp];
+    BinRun run;
+    for_each_elem<T>(row, a.V, nvec, nonfinite, [&](uint32_t key, uint32_t id) {
+      const float l = key_value<T>(key);
+      const unsigned long long w1 = dense_wfx(l, lmax, c1);
+      const unsigned long long wT = same ? w1 : dense_wfx(l, lmax, cT);
+      se += w1;
+      seT += wT;
+      if (key >= bound) {
+        const int pos = atomicAdd(&s.n_cand, 1);
+        if (pos < SW_CAP) s.cand[pos] = make_comp(key, id);
+      }
+      run.add(static_cast<int>(key >> (KEY_BITS - 8)), wT, wh, wm);
+    });
+    run.flush(wh, wm);
+  }
   se = warp_sum_u64(se);
   seT = warp_sum_u64(seT);
   if (lane == 0) {
@@ -811,6 +878,24 @@ __global__ void __launch_bounds__(SW_THREADS, 2) select_dense_kernel(SelLaunch a
     se += s.red64[0][w];
     seT += s.red64[1][w];
   }
+  dense_reduce_hist<T>(s, KEY_BITS == 8, 0u, KEY_BITS - 8, lmax, cT);
+  // ranks 0..K-1: the sorted candidates, or (massive ties at the bound) the exact radix path
+  const int nc = s.n_cand;
+  bool level0_ready = true;
+  if (nc >= K && nc <= SW_CAP) {
+    sort_cand_desc(s, nc);
+  } else {
+    __syncthreads();  // the radix path reuses the histograms' storage
+    uint32_t prefix, pmask;
+    int need;
+    bool exact;
+    radix_select_row<T>(s, row, a.V, nvec, K, nonfinite, prefix, pmask, need, exact);
+    collect_row<T>(s, row, a.V, nvec, prefix, pmask, need, exact, nonfinite);
+    sort_cand_desc(s, min(s.n_cand, K));
+    level0_ready = false;
+  }
+  const int n = min(nc >= K && nc <= SW_CAP ? nc : s.n_cand, K);
+
   // the DET elements (ranks 0..m-1) and their weights
   unsigned long long det1 = 0ull, detT = 0ull;
   for (int r = 0; r < a.m && r < n; ++r) {
@@ -829,7 +914,7 @@ __global__ void __launch_bounds__(SW_THREADS, 2) select_dense_kernel(SelLaunch a
     if (target >= seT) target = seT - 1ull;
     uint32_t kstar, acnt;
     unsigned long long amass;
-    dense_weighted_select<T>(s, row, a.V, nvec, lmax, cT, target, nonfinite, kstar, acnt, amass);
+    dense_weighted_select<T>(s, row, a.V, nvec, lmax, cT, target, level0_ready, nonfinite, kstar, acnt, amass);
     const unsigned long long wk = dense_wfx(key_value<T>(kstar), lmax, cT);
     int j = wk ? static_cast<int>((target - amass) / wk) : 0;
     if (j > s.cnt - 1) j = s.cnt - 1;  // s.cnt: elements of key k*
