@@ -47,6 +47,10 @@ struct WideShared {
       uint32_t whist[SW_WARPS][256];                // radix path: per-warp digit histograms
       unsigned long long wmass[SW_WARPS][256];      // dense support: per-warp fixed-point weights
     };
+    struct {
+      uint64_t grp[SW_CAP];                         // counting sort: candidates grouped by key
+      uint32_t cur[SW_CAP];                         //   and each key bin's next free slot
+    };
   };
   uint64_t cand[SW_CAP];            // candidates; at the end the top-|S| in rank order
   uint32_t list[SW_CAP];            // table path: vectors to gather
@@ -62,6 +66,8 @@ struct WideShared {
   int cnt;
   int probe;
   int last_pos;
+  uint32_t kmin_w[SW_WARPS];  // counting sort: per-warp smallest candidate key
+  int sort_ok;
   // dense support
   unsigned long long hmass[256];
   unsigned long long red64[2][SW_WARPS];
@@ -280,9 +286,127 @@ __device__ void collect_row(WideShared& s, const uint8_t* row, int V, int nvec, 
   __syncthreads();
 }
 
-// Bitonic sort of s.cand[0..n) descending, padded with 0 (below every
-// composite) to the next power of two P <= SW_CAP.
-__device__ void sort_cand_desc(WideShared& s, int n) {
+// Appends x to buf (when pred) at an index taken from the counter *n, one
+// shared atomic per warp (lanes ordered within the warp).  Every lane of the
+// warp calls it together.
+__device__ __forceinline__ void warp_append(bool pred, uint64_t x, uint64_t* buf, int* n, int cap) {
+  const int lane = threadIdx.x & 31;
+  const unsigned mask = __ballot_sync(FULL, pred);
+  if (mask == 0u) return;
+  const int leader = __ffs(mask) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(n, __popc(mask));
+  base = __shfl_sync(FULL, base, leader);
+  if (pred) {
+    const int pos = base + __popc(mask & ((1u << lane) - 1u));
+    if (pos < cap) buf[pos] = x;
+  }
+}
+
+__device__ __forceinline__ void warp_append_u32(bool pred, uint32_t x, uint32_t* buf, int* n, int cap) {
+  const int lane = threadIdx.x & 31;
+  const unsigned mask = __ballot_sync(FULL, pred);
+  if (mask == 0u) return;
+  const int leader = __ffs(mask) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(n, __popc(mask));
+  base = __shfl_sync(FULL, base, leader);
+  if (pred) {
+    const int pos = base + __popc(mask & ((1u << lane) - 1u));
+    if (pos < cap) buf[pos] = x;
+  }
+}
+
+// Counting sort of s.cand[0..n) descending.  One bin per key for the keys
+// within SW_CAP steps of the smallest candidate key (where nearly all
+// candidates sit), and one group, ordered by a rank count, for the few keys
+// above them (a row's largest logits, which may lie far away in key space, on
+// the other side of zero).  A block scan of the bin counts from the top gives
+// each bin's first place after the group; the candidates are grouped by bin,
+// and inside a bin (one key) a count of the larger composites orders them by
+// id.  Returns false (nothing changed) when the group or a bin holds more than
+// 128 candidates; block-uniform.
+__device__ bool counting_sort_cand(WideShared& s, int n) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s.sort_ok = 1;
+    s.n_list = 0;  // the group's size
+  }
+  uint32_t kmin = 0xffffffffu;
+  for (int i = tid; i < n; i += SW_THREADS) kmin = min(kmin, static_cast<uint32_t>(s.cand[i] >> 32));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kmin = min(kmin, __shfl_xor_sync(FULL, kmin, o));
+  if (lane == 0) s.kmin_w[warp] = kmin;
+  for (int b = tid; b < SW_CAP; b += SW_THREADS) s.list[b] = 0u;
+  __syncthreads();
+  uint32_t kmn = 0xffffffffu;
+  for (int w = 0; w < SW_WARPS; ++w) kmn = min(kmn, s.kmin_w[w]);
+  // bin b holds key kmn + SW_CAP - 1 - b (bin 0 the largest key in range)
+  auto bin_of = [&](uint64_t x) -> int {
+    const uint32_t d = static_cast<uint32_t>(x >> 32) - kmn;
+    return d < static_cast<uint32_t>(SW_CAP) ? SW_CAP - 1 - static_cast<int>(d) : -1;
+  };
+  for (int i = tid; i < n; i += SW_THREADS) {
+    const int b = bin_of(s.cand[i]);
+    if (b >= 0) atomicAdd(&s.list[b], 1u);
+    else atomicAdd(&s.n_list, 1);
+  }
+  __syncthreads();
+  const int ng = s.n_list;
+  // exclusive scan of the bin counts: thread t owns bins [t*per, (t+1)*per)
+  constexpr int per = SW_CAP / SW_THREADS;
+  const int b0 = tid * per;
+  uint32_t run = 0u, big = 0u;
+#pragma unroll
+  for (int k = 0; k < per; ++k) {
+    run += s.list[b0 + k];
+    big = max(big, s.list[b0 + k]);
+  }
+  int total;
+  const int before = block_excl_scan(s, static_cast<int>(run), &total);
+  if (big > 128u || ng > 128) s.sort_ok = 0;
+  uint32_t acc = static_cast<uint32_t>(ng + before);
+#pragma unroll
+  for (int k = 0; k < per; ++k) {
+    const uint32_t c = s.list[b0 + k];
+    s.list[b0 + k] = acc;  // the bin's first place
+    s.cur[b0 + k] = acc;
+    acc += c;
+  }
+  if (tid == 0) s.count = 0;  // the group's fill
+  __syncthreads();
+  if (!s.sort_ok) {
+    __syncthreads();
+    return false;
+  }
+  for (int i = tid; i < n; i += SW_THREADS) {
+    const uint64_t x = s.cand[i];
+    const int b = bin_of(x);
+    s.grp[b >= 0 ? static_cast<int>(atomicAdd(&s.cur[b], 1u)) : atomicAdd(&s.count, 1)] = x;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += SW_THREADS) {
+    const uint64_t x = s.grp[i];
+    const int b = bin_of(x);
+    const int lo = b >= 0 ? static_cast<int>(s.list[b]) : 0;
+    const int hi = b >= 0 ? (b + 1 < SW_CAP ? static_cast<int>(s.list[b + 1]) : n) : ng;
+    int rk = 0;
+    for (int q = lo; q < hi; ++q) rk += s.grp[q] > x;
+    s.cand[lo + rk] = x;
+  }
+  __syncthreads();
+  return true;
+}
+
+constexpr int SW_BITONIC_MAX = 2048;  // the largest power of two within SW_CAP
+
+// Sorts s.cand[0..n) descending: the counting sort, else a bitonic sort
+// padded with 0 (below every composite) to the next power of two, which needs
+// n <= SW_BITONIC_MAX.  Returns false (unsorted) only when neither applies;
+// block-uniform.
+__device__ bool sort_cand_desc(WideShared& s, int n) {
+  if (n > 32 && counting_sort_cand(s, n)) return true;
+  if (n > SW_BITONIC_MAX) return false;
   const int tid = threadIdx.x;
   int P = 1;
   while (P < n) P <<= 1;
@@ -302,6 +426,7 @@ __device__ void sort_cand_desc(WideShared& s, int n) {
     }
   }
   __syncthreads();
+  return true;
 }
 
 // The (r+1)-th largest, with multiplicity, of the 16-bit values x held one
@@ -353,11 +478,12 @@ __device__ __forceinline__ uint32_t vec_max_key16<float>(const uint4& v, bool& n
 }
 
 // Table path: one pass stores every vector's maximum key; the bound is a rank
-// of a sample of the table expected to leave about 1.5 |S| entries at
+// of a sample of the table expected to leave about 1.25 |S| entries at
 // or above it, accepted once an exact count shows between |S| and SW_CAP
 // entries there (each entry is a distinct element, so at least |S| elements
 // reach the bound); the listed vectors are re-read and every element that
-// reaches the bound becomes a candidate; the candidates are sorted, so the
+// reaches the bound becomes a candidate (appended one shared atomic per warp);
+// the candidates are sorted (counting sort by key), so the
 // first |S| are the top-|S|.  Returns false (nothing decided) when no sample
 // rank passes the count, or the candidates are too few (NaN) or too many
 // (ties); block-uniform.
@@ -380,7 +506,7 @@ __device__ bool table_select(WideShared& s, const uint8_t* row, int V, int nvec,
   }
   __syncthreads();
   const uint32_t sample = s.tbl[static_cast<int64_t>(tid) * nvec / SW_THREADS];
-  int r = static_cast<int>(ceilf(1.5f * S * SW_THREADS / nvec)) - 1;
+  int r = static_cast<int>(ceilf(1.25f * S * SW_THREADS / nvec)) - 1;
   r = r < 0 ? 0 : (r > SW_THREADS - 1 ? SW_THREADS - 1 : r);
   uint32_t b16 = 0u;
   bool ok = false;
@@ -400,17 +526,12 @@ __device__ bool table_select(WideShared& s, const uint8_t* row, int V, int nvec,
     s.n_cand = 0;
   }
   __syncthreads();
-  for (int vi = tid; vi < nvec; vi += SW_THREADS)
-    if (s.tbl[vi] >= b16) {
-      const int pos = atomicAdd(&s.n_list, 1);
-      if (pos < SW_CAP) s.list[pos] = static_cast<uint32_t>(vi);
-    }
+  for (int vb = 0; vb < nvec; vb += SW_THREADS) {  // warp-uniform trip count
+    const int vi = vb + tid;
+    warp_append_u32(vi < nvec && s.tbl[vi] >= b16, static_cast<uint32_t>(vi), s.list, &s.n_list, SW_CAP);
+  }
   __syncthreads();
   const int nl = min(s.n_list, SW_CAP);
-  auto push = [&](uint32_t key, uint32_t id) {
-    const int pos = atomicAdd(&s.n_cand, 1);
-    if (pos < SW_CAP) s.cand[pos] = make_comp(key, id);
-  };
   // the listed vectors, two per thread with both loads in flight
   for (int i0 = 0; i0 < nl; i0 += 2 * SW_THREADS) {
     uint4 v[2];
@@ -423,23 +544,25 @@ __device__ bool table_select(WideShared& s, const uint8_t* row, int V, int nvec,
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u)
-      if (vi[u] >= 0)
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-          const uint32_t key = elem_key<T>(v[u], j, nonfinite);
-          if (key >= bound) push(key, static_cast<uint32_t>(vi[u] * VEC + j));
-        }
+      for (int j = 0; j < VEC; ++j) {
+        const uint32_t key = vi[u] >= 0 ? elem_key<T>(v[u], j, nonfinite) : 0u;
+        warp_append(vi[u] >= 0 && key >= bound, make_comp(key, static_cast<uint32_t>(vi[u] * VEC + j)), s.cand,
+                    &s.n_cand, SW_CAP);
+      }
   }
   const int id = nvec * VEC + tid;  // elements past the last whole vector
   if (id < V) {
     const uint32_t key = scalar_key<T>(row, id, nonfinite);
-    if (key >= bound) push(key, static_cast<uint32_t>(id));
+    if (key >= bound) {
+      const int pos = atomicAdd(&s.n_cand, 1);
+      if (pos < SW_CAP) s.cand[pos] = make_comp(key, static_cast<uint32_t>(id));
+    }
   }
   __syncthreads();
   const int n = s.n_cand;
   if (n < S || n > SW_CAP) return false;
-  sort_cand_desc(s, n);
-  return true;
+  return sort_cand_desc(s, n);  // false: the radix path takes the row
 }
 
 // Softmaxes, tail masses and the probe of a row from its sorted support
@@ -882,8 +1005,7 @@ __global__ void __launch_bounds__(SW_THREADS, 2) select_dense_kernel(SelLaunch a
   // ranks 0..K-1: the sorted candidates, or (massive ties at the bound) the exact radix path
   const int nc = s.n_cand;
   bool level0_ready = true;
-  if (nc >= K && nc <= SW_CAP) {
-    sort_cand_desc(s, nc);
+  if (nc >= K && nc <= SW_CAP && sort_cand_desc(s, nc)) {
   } else {
     __syncthreads();  // the radix path reuses the histograms' storage
     uint32_t prefix, pmask;
@@ -894,7 +1016,7 @@ __global__ void __launch_bounds__(SW_THREADS, 2) select_dense_kernel(SelLaunch a
     sort_cand_desc(s, min(s.n_cand, K));
     level0_ready = false;
   }
-  const int n = min(nc >= K && nc <= SW_CAP ? nc : s.n_cand, K);
+  const int n = min(level0_ready ? nc : s.n_cand, K);
 
   // the DET elements (ranks 0..m-1) and their weights
   unsigned long long det1 = 0ull, detT = 0ull;
