@@ -165,8 +165,9 @@ class TreeBuffers:
         self.sup_q = mk(r + (self.sup_stride,), f32)
         self.sup_qT = mk(r + (self.sup_stride,), f32)
         self.sup_z, self.sup_zT, self.probe_pos = mk(r, f32), mk(r, f32), mk(r, i32)
-        # row counter of the support selection (zero; every call leaves it zero)
-        self.sched = torch.zeros((2,), dtype=i32, device=device)
+        # row counter of the support selection (zero; every call leaves it zero) and the latest
+        # call's cut key, a threshold hint for the next call's first rows
+        self.sched = torch.zeros((3,), dtype=i32, device=device)
 
     def c(self) -> c_tree:
         if getattr(self, "_c", None) is None:

@@ -608,6 +608,7 @@ struct SelArgs {
   int sup_stride;
   uint32_t* status;
   unsigned int* sched;  // [2]: next row to hand out, producers done (NULL: static order)
+  unsigned int* hint;   // the cut key of a row of the previous launch (0: none; NULL: not kept)
 };
 
 // Robust selection of a row straight from global memory, in id order: keep
@@ -1042,9 +1043,15 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
     s.count[0] = s.count[1] = 0;
   }
   for (int i = tid; i < 2 * 256; i += SX_THREADS) s.khist[i >> 8][i & 255] = 0u;
-  __syncthreads();  // the last CTA-wide barrier: the roles split below
   grid_dependency_wait();
   grid_dependents_launch();
+  if (tid == 0 && a.hint != nullptr) {
+    // the first row's queue threshold from the previous launch's cut (the cut
+    // barely moves between rows of a workload; a miss costs the exact path)
+    const uint32_t h = *a.hint;
+    if (h >= 0x80u + SX_QMARGIN) s.thr_row[0] = h - SX_QMARGIN;
+  }
+  __syncthreads();  // the last CTA-wide barrier: the roles split below
 
   if (warp == SX_SEL_WARP) {
     // ------------------------------------------------------------ selector ---
@@ -1084,6 +1091,8 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
       if (lane == 0) mbar_arrive(&s.cempty[q]);
     }
     if (timed_out && lane == 0) set_status(a.status, SPEC_TREE_S_TIMEOUT);
+    // a cut for the next launch's first rows (one writer)
+    if (blockIdx.x == 0 && lane == 0 && a.hint != nullptr && s.last_cut != 0u) *a.hint = s.last_cut;
     return;
   }
 
@@ -1444,6 +1453,7 @@ cudaError_t launch_select_expand(int dtype, const SelLaunch& L, cudaStream_t str
   // rows on demand once a CTA has several; with one or two rows a CTA the
   // fixed order spreads the second rows evenly over the SMs
   a.sched = a.total_rows >= 4 * grid ? reinterpret_cast<unsigned int*>(L.sched) : nullptr;
+  a.hint = L.sched != nullptr ? reinterpret_cast<unsigned int*>(L.sched) + 2 : nullptr;
   if (dtype == SPEC_TREE_BF16) {
     cudaError_t err = cudaFuncSetAttribute(select_expand_kernel<__nv_bfloat16>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -156,11 +156,15 @@ typedef struct spec_tree_params {
  *   whole vocabulary), so sup_stride >= K + 1; q, q_T and the tail masses are
  *   over the whole vocabulary.
  * Row schedule (optional, may be NULL):
- *   sched        device uint32[2], zero before the first call that uses it.
- *                The support selection hands draft rows to its CTAs on demand
- *                from this counter (a CTA that runs ahead takes more rows, so
- *                they finish together) and leaves it at zero again when it
- *                ends.  NULL: rows are dealt to the CTAs in a fixed order.
+ *   sched        device uint32[3], zero before the first call that uses it.
+ *                [0], [1]: the support selection hands draft rows to its CTAs
+ *                on demand from this counter (a CTA that runs ahead takes
+ *                more rows, so they finish together) and leaves both words at
+ *                zero again when it ends.  [2]: the top-|S| cut key of a row
+ *                of the latest call, which the next call's first rows take as
+ *                their predicted threshold (a hint only: a wrong value costs
+ *                time, never a different result; any value is valid).  NULL:
+ *                rows are dealt to the CTAs in a fixed order, no hint is kept.
  *                Calls that overlap on the GPU must not share one counter.
  */
 typedef struct spec_tree_t {

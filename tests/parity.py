@@ -92,7 +92,7 @@ def run_gpu(case: Case, target=None, device="cuda"):
                     out_node=out.out_node.cpu().numpy(), margins=out.margins.cpu().numpy())
     host["status"] = int(status.item())
     # the support selection hands rows out from the tree's counter and leaves it at zero
-    assert tree.sched.cpu().tolist() == [0, 0], tree.sched
+    assert tree.sched.cpu().tolist()[:2] == [0, 0], tree.sched
     return host
 
 

@@ -247,6 +247,31 @@ def test_rows_whose_cut_jumps():
     _report("cut jumps", res)
 
 
+def test_cut_hint_from_the_previous_call():
+    """The row schedule keeps a cut key of the latest call as the next call's first-row threshold.
+    The second call's rows here differ wildly from the first's (scaled by 3, shifted by 5), so the hint
+    misses and the exact path must take over; a third call on the same rows hits it.  Every call
+    equals the oracle."""
+    from dynamic_tree_speculative_gb300 import binding as B
+    wl = WL.WORKLOADS["vicuna"].with_(B=8, V=32000)
+    params = B.Params.from_workload(wl)
+    tree = B.TreeBuffers(params, wl.B)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for i, (scale, shift) in enumerate([(1.0, 0.0), (3.0, 5.0), (3.0, 5.0)]):
+        case = parity.make_case(wl, 70 + i)
+        case.draft = (case.draft.float() * scale + shift).to(torch.bfloat16)
+        B.spec_tree_build(params, wl.V, case.draft.cuda(), case.u_probe.cuda(), tree, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        hint = int(tree.sched[2].item())
+        assert hint != 0  # a cut was kept for the next call
+        g = {k: getattr(tree, k).cpu().numpy() for k in (
+            "node_token", "node_parent", "node_depth", "node_kind", "node_slot", "node_exp_row", "node_score",
+            "n_nodes", "sup_id", "sup_q", "sup_qT", "sup_z", "sup_zT", "probe_pos")}
+        out = parity.compare_case(g, case, range(wl.B))
+        assert out["build_exact"] + out["build_replayed"] == wl.B
+
+
 def test_queue_path_with_ragged_vocabulary():
     """Many rows per CTA (the predicted-threshold queue path and rows handed out on demand) on a
     vocabulary that is not a multiple of the vector width: the elements past the last whole vector
