@@ -40,7 +40,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama3_b64")
-    ap.add_argument("--batch", type=int, default=None, help="override trees per GPU")
+    ap.add_argument("--batch", type=int, default=None, help="override trees per GPU (also of --sweep lines)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-e2e", action="store_true")
@@ -491,6 +491,8 @@ def run_sweep(args):
     for wl in sweep_configs():
         if args.only and args.only not in wl.name:
             continue
+        if args.batch:
+            wl = wl.with_(B=args.batch)
         params = B.Params.from_workload(wl)
         cp = params.c()
         n_rows = B.rows_needed(params)
