@@ -48,7 +48,8 @@ def parse_args():
     ap.add_argument("--sweep", action="store_true",
                     help="one JSON line per configuration: the workloads, the batch sweep with both builders, "
                          "the wide supports (single GPU; not the contract line)")
-    ap.add_argument("--only", default=None, help="--sweep: configurations whose name contains this text")
+    ap.add_argument("--only", default=None,
+                    help="--sweep: configurations whose name contains one of these comma-separated texts")
     return ap.parse_args()
 
 
@@ -488,8 +489,13 @@ def run_sweep(args):
     dev = torch.device("cuda")
     hbm, peak_kind = peaks()
     steps = min(args.steps, 200)
+    only = [x for x in args.only.split(",") if x] if args.only else None
+
+    def wanted(name: str) -> bool:
+        return only is None or any(x in name for x in only)
+
     for wl in sweep_configs():
-        if args.only and args.only not in wl.name:
+        if not wanted(wl.name):
             continue
         if args.batch:
             wl = wl.with_(B=args.batch)
@@ -555,7 +561,7 @@ def run_sweep(args):
         del draft, target, tree, out
         torch.cuda.empty_cache()
     for b in (8, 64):
-        if args.only and args.only not in f"layer_mode_b{b}":
+        if not wanted(f"layer_mode_b{b}"):
             continue
         print(json.dumps(sweep_layer_mode(WL.BENCH_WORKLOAD.with_(name=f"layer_mode_b{b}", B=b), args)), flush=True)
     return 0

@@ -11,8 +11,10 @@
 //
 // The walk is sequential in depth, so the latency of one level is what
 // matters: every level's target row is split over the C CTAs of the tree's
-// cluster (C chosen so that the whole batch fits in one wave).  Each of the
-// 32*C warps owns a contiguous slice of the row, loads all of it in one batch
+// cluster (C and the CTA size chosen so that the whole batch fits in one
+// wave with as many SMs per tree as that allows: the per-element exp2 of a
+// slice runs at the SM's special-function rate).  Each warp of the cluster
+// owns a contiguous slice of the row, loads all of it in one batch
 // of predicated 16-byte loads (one memory latency per level) and keeps the
 // slice's maximum and sum of exp2((t - max) * log2(e) / T) with packed
 // float32x2 arithmetic.  Each warp pushes its two numbers into the leader
@@ -38,8 +40,8 @@ namespace cg = cooperative_groups;
 
 namespace st {
 
-constexpr int VER_THREADS = 1024;
-constexpr int VER_WARPS = VER_THREADS / 32;
+constexpr int VER_MAX_THREADS = 1024;  // threads of a CTA: 256, 512 or 1024 (an SM runs 1024 at 64 registers)
+constexpr int VER_WARPS = VER_MAX_THREADS / 32;
 constexpr int VER_MAX_CLUSTER = 8;
 constexpr int VER_MAX_SLICES = VER_WARPS * VER_MAX_CLUSTER;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -310,11 +312,12 @@ __device__ __forceinline__ int rank_of_slot(int slot, int m, int pp) {
   return r;
 }
 
-template <typename T, int C>
-__global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) verify_kernel(VerifyLaunch L) {
+template <typename T, int C, int NT>
+__global__ void __launch_bounds__(NT, VER_MAX_THREADS / NT) __cluster_dims__(C, 1, 1) verify_kernel(VerifyLaunch L) {
   using E = VElem<T>;
   constexpr int VEC = E::VEC;
-  constexpr int NS = VER_WARPS * C;  // slices per row
+  constexpr int NW = NT / 32;   // warps of a CTA
+  constexpr int NS = NW * C;    // slices per row
   extern __shared__ __align__(16) uint8_t smem_raw[];
   VerShared& s = *reinterpret_cast<VerShared*>(smem_raw);
   cg::cluster_group cluster = cg::this_cluster();
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
     fence_mbar_init();
   }
   if (leader) {
-    for (int i = tid; i < n_nodes; i += VER_THREADS) {
+    for (int i = tid; i < n_nodes; i += NT) {
       s.nd_parent[i] = t.node_parent[nb + i];
       s.nd_slot[i] = t.node_slot[nb + i];
       s.nd_exp_row[i] = t.node_exp_row[nb + i];
@@ -354,10 +357,10 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
   int32_t* ot = L.out_tok + static_cast<int64_t>(b) * (D + 1);
   int32_t* on = L.out_node + static_cast<int64_t>(b) * (D + 1);
   // where this warp's slice statistics go in the leader's shared memory
-  const uint32_t lead_m0 = cluster_addr(&s.all_m[0][cr * VER_WARPS + warp], 0);
-  const uint32_t lead_m1 = cluster_addr(&s.all_m[1][cr * VER_WARPS + warp], 0);
-  const uint32_t lead_s0 = cluster_addr(&s.all_s[0][cr * VER_WARPS + warp], 0);
-  const uint32_t lead_s1 = cluster_addr(&s.all_s[1][cr * VER_WARPS + warp], 0);
+  const uint32_t lead_m0 = cluster_addr(&s.all_m[0][cr * NW + warp], 0);
+  const uint32_t lead_m1 = cluster_addr(&s.all_m[1][cr * NW + warp], 0);
+  const uint32_t lead_s0 = cluster_addr(&s.all_s[0][cr * NW + warp], 0);
+  const uint32_t lead_s1 = cluster_addr(&s.all_s[1][cr * NW + warp], 0);
   const uint32_t lead_bar0 = cluster_addr(&s.stats_bar[0], 0);
   const uint32_t lead_bar1 = cluster_addr(&s.stats_bar[1], 0);
   // support of the current node's draft row (leader): prefetched when the
@@ -384,7 +387,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
     // below (its reads of the previous level's are done)
     if (er >= 0 && tid < K) s.uv_lv[tid] = L.u_verify[(static_cast<int64_t>(b) * D + level) * K + tid];
     float wm, ws;
-    slice_stats<T>(row, V, cr * VER_WARPS + warp, NS, c, nonfinite, wm, ws);
+    slice_stats<T>(row, V, cr * NW + warp, NS, c, nonfinite, wm, ws);
     // target logits of the support tokens, landing while the slices arrive
     float t_sup = 0.0f;
     if (er >= 0 && tid < S) t_sup = E::load(row, sup_v);
@@ -424,7 +427,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
       // children of the node by sibling slot; a node at depth D is a leaf
       // (which also bounds the walk for malformed trees)
       if (er >= 0)
-        for (int i = tid + 1; i < n_nodes; i += VER_THREADS)
+        for (int i = tid + 1; i < n_nodes; i += NT)
           if (s.nd_parent[i] == node) {
             const int slot = s.nd_slot[i];
             if (slot >= 0 && slot < K) s.kid_by_slot[slot] = i;
@@ -556,7 +559,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
     // ------------------------------------------------------------- bonus ---
     const int nk = s.nkids;
     const float M = s.M, invZp = s.invZp;
-    for (int g = tid; g < NS; g += VER_THREADS) s.slice_corr[g] = 0.0f;
+    for (int g = tid; g < NS; g += NT) s.slice_corr[g] = 0.0f;
     __syncthreads();
     const bool corrected = nk > 0 && tid < S && s.w_sup[tid] != s.p_sup[tid];
     if (corrected) atomicAdd(&s.slice_corr[slice_of_token(sup_v, NS, nvec, VEC)], s.p_sup[tid] - s.w_sup[tid]);
@@ -638,7 +641,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
       const float tie = static_cast<float>(MASS_MARGIN) * s.Zr;  // a draw within 1e-6 * Zr of a boundary
       float base_run = 0.0f;
       int last_pos = -1;
-      for (int cb = t0; cb < t1; cb += VER_THREADS * VEC) {
+      for (int cb = t0; cb < t1; cb += NT * VEC) {
         const int v0 = cb + tid * VEC;
         float w[VEC];
         if (v0 + VEC <= t1 && v0 / VEC < nvec) {
@@ -667,7 +670,7 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
         if (lane == 31) s.scan_w[warp] = incl;
         __syncthreads();
         float wbefore = 0.0f, total = 0.0f;
-        for (int k = 0; k < VER_WARPS; ++k) {
+        for (int k = 0; k < NW; ++k) {
           const float x = s.scan_w[k];
           if (k < warp) wbefore += x;
           total += x;
@@ -719,37 +722,47 @@ __global__ void __launch_bounds__(VER_THREADS, 1) __cluster_dims__(C, 1, 1) veri
   cluster.sync();
 }
 
-template <typename T, int C>
+template <typename T, int C, int NT>
 cudaError_t launch_verify_c(const VerifyLaunch& L, cudaStream_t stream) {
   const int smem = static_cast<int>(sizeof(VerShared));
-  cudaError_t err = cudaFuncSetAttribute(verify_kernel<T, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t err = cudaFuncSetAttribute(verify_kernel<T, C, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(verify_kernel<T, C>, dim3(L.B * C), dim3(VER_THREADS), smem, stream, L);
+  return launch_pdl(verify_kernel<T, C, NT>, dim3(L.B * C), dim3(NT), smem, stream, L);
+}
+
+template <typename T, int NT>
+cudaError_t launch_verify_n(const VerifyLaunch& L, int C, cudaStream_t stream) {
+  switch (C) {
+    case 8:
+      return launch_verify_c<T, 8, NT>(L, stream);
+    case 4:
+      return launch_verify_c<T, 4, NT>(L, stream);
+    case 2:
+      return launch_verify_c<T, 2, NT>(L, stream);
+    default:
+      return launch_verify_c<T, 1, NT>(L, stream);
+  }
 }
 
 template <typename T>
 cudaError_t launch_verify_t(const VerifyLaunch& L, cudaStream_t stream) {
-  // the largest cluster (<= 8 CTAs, one per SM) that keeps the batch in one
-  // wave; a cluster shape the device cannot place is refused at launch, and
-  // the next smaller one is tried
-  int C = 1;
-  while (C < VER_MAX_CLUSTER && static_cast<int64_t>(L.B) * C * 2 <= L.num_sms) C *= 2;
+  // Threads per tree: the most (<= 8 x 1024) that keep the batch in one wave
+  // (an SM runs 1024 threads at 64 registers), spread over the largest
+  // cluster (<= 8 CTAs) whose CTAs keep >= 256 threads and one thread per
+  // support token.  More CTAs per tree put more SMs, and their exp2 units, on
+  // the row of the slowest tree; the slices (warps x CTAs) stay as many.
+  // A cluster shape the device cannot place is refused at launch, and the
+  // next smaller one is tried.
+  const int nt_min = L.S <= 256 ? 256 : L.S <= 512 ? 512 : VER_MAX_THREADS;
+  const int64_t budget = static_cast<int64_t>(L.num_sms) * VER_MAX_THREADS / L.B;
+  int per_tree = VER_MAX_CLUSTER * VER_MAX_THREADS;
+  while (per_tree > nt_min && per_tree > budget) per_tree /= 2;
   cudaError_t err = cudaErrorInvalidValue;
-  for (; C >= 1; C /= 2) {
-    switch (C) {
-      case 8:
-        err = launch_verify_c<T, 8>(L, stream);
-        break;
-      case 4:
-        err = launch_verify_c<T, 4>(L, stream);
-        break;
-      case 2:
-        err = launch_verify_c<T, 2>(L, stream);
-        break;
-      default:
-        err = launch_verify_c<T, 1>(L, stream);
-        break;
-    }
+  for (int C = min(VER_MAX_CLUSTER, per_tree / nt_min); C >= 1; C /= 2) {
+    const int nt = max(nt_min, min(VER_MAX_THREADS, per_tree / C));
+    err = nt == 256   ? launch_verify_n<T, 256>(L, C, stream)
+          : nt == 512 ? launch_verify_n<T, 512>(L, C, stream)
+                      : launch_verify_n<T, VER_MAX_THREADS>(L, C, stream);
     if (err == cudaSuccess) break;
   }
   return err;
