@@ -11,11 +11,12 @@
 // barrier per chunk and the next row is already landing while a row's tail
 // work runs.
 //
-//   pass (HBM; a CTA's first row kept in L2 for its gather, later rows
-//     streamed with an evict-first hint): each consumer thread
-//     reduces its four vectors of every chunk to their maximum with one
-//     packed bf16x2 tree and writes it, as a 16-bit order key, to a table
-//     in shared memory (thread x chunk); it also keeps its running maximum.
+//   pass (HBM; a CTA's first row kept in L2 for its gather when no earlier
+//     launch left a cut, other rows streamed with an evict-first hint): each
+//     consumer thread reduces its four vectors of every chunk to their
+//     maximum with one packed bf16x2 tree and writes it, as a 16-bit order
+//     key, to a table in shared memory (thread x chunk); it also keeps its
+//     running maximum.
 //   bound: thread maxima are distinct elements of the row, so if warp w's
 //     j-th largest thread maximum is b_w, with j * (consumer warps) >= |S|,
 //     then min_w b_w is a lower bound of the |S|-th largest logit.
@@ -1099,12 +1100,13 @@ __global__ void __launch_bounds__(SX_THREADS, 2) select_expand_kernel(SelArgs a)
   if (warp == SX_PROD_WARP) {
     // ------------------------------------------------------------ producer ---
     if (lane == 0 && nch > 0) {
-      // L2 hints: a CTA's first row takes the bound-and-gather path, which
-      // re-reads a few vectors, so it is kept (evict last); later rows mostly
-      // take the queue path and are read once, so they leave L2 first (kept
-      // rows crowd out the other kernels' data: 0.86 -> 0.92 of the measured
-      // bandwidth at 64 trees in the bench's step)
-      const uint64_t keep_first_row = l2_evict_last_policy();
+      // L2 hints: with no cut from an earlier launch a CTA's first row takes
+      // the bound-and-gather path, which re-reads a few vectors, so it is kept
+      // (evict last); every other row mostly takes the queue path and is read
+      // once, so it leaves L2 first (kept rows crowd out the other kernels'
+      // data: 0.86 -> 0.92 of the measured bandwidth at 64 trees in the
+      // bench's step, and 0.93 -> 0.96 once the first rows follow too)
+      const uint64_t keep_first_row = s.thr_row[0] != 0u ? l2_evict_first_policy() : l2_evict_last_policy();
       const uint64_t stream_once = l2_evict_first_policy();
       int st = 0;
       uint32_t phase = 0;
