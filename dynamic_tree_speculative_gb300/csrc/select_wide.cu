@@ -39,6 +39,7 @@ constexpr int SW_MAX_S = SPEC_TREE_MAX_SUPPORT;
 constexpr int SW_RPT = (SW_MAX_S + SW_THREADS - 1) / SW_THREADS;  // support ranks a thread owns in the epilogue
 constexpr int SW_TBL = 32768;  // table path: rows of up to 32768 vectors (256K bf16 / 128K f32 tokens)
 constexpr int SW_CAP = 2048;   // table path: candidates
+constexpr int SW_QW = SW_TBL * 2 / 16 / SW_WARPS;  // queue path: vectors queued per warp (the table's storage)
 
 struct WideShared {
   union {
@@ -51,9 +52,13 @@ struct WideShared {
       uint64_t grp[SW_CAP];                         // counting sort: candidates grouped by key
       uint32_t cur[SW_CAP];                         //   and each key bin's next free slot
     };
+    uint4 qvec[SW_WARPS][SW_QW];                    // queue path: each warp's queued vectors
   };
   uint64_t cand[SW_CAP];            // candidates; at the end the top-|S| in rank order
-  uint32_t list[SW_CAP];            // table path: vectors to gather
+  union {
+    uint32_t list[SW_CAP];            // table path: vectors to gather
+    uint16_t qvid[SW_WARPS][SW_QW];   // queue path: the queued vectors' indices in the row
+  };
   uint32_t hist[256];
   float red[4][SW_WARPS];         // block reductions
   float scan[SW_RPT][SW_WARPS];   // block scans of the tail weights, one per rank block
@@ -565,6 +570,79 @@ __device__ bool table_select(WideShared& s, const uint8_t* row, int V, int nvec,
   return sort_cand_desc(s, n);  // false: the radix path takes the row
 }
 
+// Queue path (bf16 rows of 2048 to SW_TBL vectors): the cut of the support
+// (the key of its |S|-th largest logit) barely moves from row to row of a
+// workload, so a threshold a few key steps below the cut of a recent row
+// predicts which vectors can hold a candidate.  In the one pass over the row
+// each warp copies every vector whose maximum reaches the threshold into its
+// own queue in shared memory (a ballot per vector, no atomics); afterwards
+// each warp appends the queued elements that reach the threshold as
+// candidates, and the candidates are sorted as on the table path.  Exact: a
+// vector holding an element that reaches the threshold has its maximum above
+// it, so every such element is a candidate, and when at least |S| of them
+// exist they hold the top-|S|.  Returns false (nothing decided) when fewer
+// than |S| or more than SW_CAP elements reach the threshold, a warp's queue
+// overflows or a NaN is seen; the table path then takes the row.
+// Block-uniform.
+__device__ __forceinline__ uint32_t wide_queue_margin(int S) { return S <= 256 ? 16u : S <= 512 ? 10u : 6u; }
+
+template <typename T>
+__device__ bool queue_select(WideShared& s, const uint8_t* row, int V, int nvec, int S, uint32_t thr,
+                             bool& nonfinite) {
+  constexpr int VEC = Elem<T>::VEC, U = 8;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  if (tid == 0) s.n_cand = 0;
+  int nq = 0;  // this warp's queued vectors (warp-uniform)
+  bool nan = false;
+  for (int vb = 0; vb < nvec; vb += U * SW_THREADS) {  // warp-uniform trip count
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int vi = vb + u * SW_THREADS + tid;
+      if (vi < nvec) v[u] = ldg_stream(row + static_cast<int64_t>(vi) * 16);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int vi = vb + u * SW_THREADS + tid;
+      const bool pass = vi < nvec && vec_max_key16<T>(v[u], nan) >= thr;
+      const unsigned bal = __ballot_sync(FULL, pass);
+      if (bal != 0u) {
+        const int slot = nq + __popc(bal & lt);
+        if (pass && slot < SW_QW) {
+          s.qvec[warp][slot] = v[u];
+          s.qvid[warp][slot] = static_cast<uint16_t>(vi);
+        }
+        nq += __popc(bal);
+      }
+    }
+  }
+  if (__syncthreads_or(nan || nq > SW_QW)) return false;
+  for (int i0 = 0; i0 < nq; i0 += 32) {  // warp-uniform trip count
+    const int i = i0 + lane;
+    const bool valid = i < nq;
+    const uint4 v = valid ? s.qvec[warp][i] : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t id0 = valid ? static_cast<uint32_t>(s.qvid[warp][i]) * VEC : 0u;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+      const uint32_t key = valid ? elem_key<T>(v, j, nonfinite) : 0u;
+      warp_append(valid && key >= thr, make_comp(key, id0 + j), s.cand, &s.n_cand, SW_CAP);
+    }
+  }
+  const int id = nvec * VEC + tid;  // elements past the last whole vector
+  if (id < V) {
+    const uint32_t key = scalar_key<T>(row, id, nonfinite);
+    if (key >= thr) {
+      const int pos = atomicAdd(&s.n_cand, 1);
+      if (pos < SW_CAP) s.cand[pos] = make_comp(key, static_cast<uint32_t>(id));
+    }
+  }
+  __syncthreads();
+  const int n = s.n_cand;
+  if (n < S || n > SW_CAP) return false;
+  return sort_cand_desc(s, n);
+}
+
 // Softmaxes, tail masses and the probe of a row from its sorted support
 // s.cand[0..n): thread t owns support ranks t, t + SW_THREADS, ...
 // RheoSampling Key design 2; the probe is the first tail rank k with
@@ -674,9 +752,18 @@ __global__ void __launch_bounds__(SW_THREADS, 2) select_wide_kernel(SelLaunch a,
   const uint8_t* row = static_cast<const uint8_t*>(a.logits) + in_row * row_bytes;
   const int nvec = static_cast<int>((static_cast<int64_t>(a.V) * Elem<T>::ES) / 16);
   bool nonfinite = false;
-  // rows of 2048 to SW_TBL vectors: the table path; otherwise, or when it
-  // declines, the exact radix select
-  bool done = nvec >= 2 * SW_THREADS && nvec <= SW_TBL && table_select<T>(s, row, a.V, nvec, a.S, nonfinite);
+  // rows of 2048 to SW_TBL vectors: the queue path when a recent row's cut is
+  // known (bf16), else or when it declines the table path; otherwise, or when
+  // that declines, the exact radix select
+  const bool tabled = nvec >= 2 * SW_THREADS && nvec <= SW_TBL;
+  uint32_t* hint = a.sched != nullptr ? reinterpret_cast<uint32_t*>(a.sched) + 2 : nullptr;
+  const uint32_t h = hint != nullptr && sizeof(T) == 2 && tabled ? *reinterpret_cast<volatile uint32_t*>(hint) : 0u;
+  const uint32_t margin = wide_queue_margin(a.S);
+  bool done = h > margin && queue_select<T>(s, row, a.V, nvec, a.S, h - margin, nonfinite);
+  if (!done && tabled) {
+    __syncthreads();  // the queue shares its storage with the table
+    done = table_select<T>(s, row, a.V, nvec, a.S, nonfinite);
+  }
   if (!done) {
     __syncthreads();  // the table shares its storage with the radix histograms
     uint32_t prefix, pmask;
@@ -687,6 +774,10 @@ __global__ void __launch_bounds__(SW_THREADS, 2) select_wide_kernel(SelLaunch a,
     sort_cand_desc(s, min(s.n_cand, a.S));
   }
   const int n = min(s.n_cand, a.S);
+  // this row's cut predicts the next rows' (any recent row will do: one
+  // plain store, read by CTAs that start later and by the next launch)
+  if (threadIdx.x == 0 && hint != nullptr && sizeof(T) == 2 && n == a.S)
+    *reinterpret_cast<volatile uint32_t*>(hint) = static_cast<uint32_t>(s.cand[n - 1] >> 32);
   wide_epilogue<T>(s, a, out_row, in_row, n);
   if (nonfinite) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
 }

@@ -247,17 +247,19 @@ def test_rows_whose_cut_jumps():
     _report("cut jumps", res)
 
 
-def test_cut_hint_from_the_previous_call():
-    """The row schedule keeps a cut key of the latest call as the next call's first-row threshold.
-    The second call's rows here differ wildly from the first's (scaled by 3, shifted by 5), so the hint
-    misses and the exact path must take over; a third call on the same rows hits it.  Every call
-    equals the oracle."""
+@pytest.mark.parametrize("support", [128, 256, 1024])
+def test_cut_hint_from_the_previous_call(support):
+    """The row schedule keeps a cut key of the latest call (of the latest row, for supports above 128)
+    as the predicted queue threshold of the next rows.  The second call's rows here differ wildly from
+    the first's (scaled by 3, shifted by 5), so the hint lies far below their cut and the exact path must
+    take over; a third call on the same rows hits it; a fourth on rows like the first's gets a hint far
+    above their cut.  Every call equals the oracle."""
     from dynamic_tree_speculative_gb300 import binding as B
-    wl = WL.WORKLOADS["vicuna"].with_(B=8, V=32000)
+    wl = WL.WORKLOADS["vicuna"].with_(B=8, V=32000, support=support)
     params = B.Params.from_workload(wl)
     tree = B.TreeBuffers(params, wl.B)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for i, (scale, shift) in enumerate([(1.0, 0.0), (3.0, 5.0), (3.0, 5.0)]):
+    for i, (scale, shift) in enumerate([(1.0, 0.0), (3.0, 5.0), (3.0, 5.0), (1.0, 0.0)]):
         case = parity.make_case(wl, 70 + i)
         case.draft = (case.draft.float() * scale + shift).to(torch.bfloat16)
         B.spec_tree_build(params, wl.V, case.draft.cuda(), case.u_probe.cuda(), tree, status)
@@ -270,6 +272,29 @@ def test_cut_hint_from_the_previous_call():
             "n_nodes", "sup_id", "sup_q", "sup_qT", "sup_z", "sup_zT", "probe_pos")}
         out = parity.compare_case(g, case, range(wl.B))
         assert out["build_exact"] + out["build_replayed"] == wl.B
+
+
+def test_wide_support_queue_path_at_full_size():
+    """|S| = 1024 at the LLaMA-3 vocabulary, 64 trees: the first call leaves a cut, so every row of the
+    second call (the same rows) takes the predicted-threshold queue path; sampled trees of both calls
+    equal the oracle."""
+    from dynamic_tree_speculative_gb300 import binding as B
+    wl = WL.BENCH_WORKLOAD.with_(support=1024)
+    params = B.Params.from_workload(wl)
+    tree = B.TreeBuffers(params, wl.B)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    case = parity.make_case(wl, 23)
+    sample = [0, 21, 42, 63]
+    for _ in range(2):
+        B.spec_tree_build(params, wl.V, case.draft.cuda(), case.u_probe.cuda(), tree, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert int(tree.sched[2].item()) != 0
+        g = {k: getattr(tree, k).cpu().numpy() for k in (
+            "node_token", "node_parent", "node_depth", "node_kind", "node_slot", "node_exp_row", "node_score",
+            "n_nodes", "sup_id", "sup_q", "sup_qT", "sup_z", "sup_zT", "probe_pos")}
+        out = parity.compare_case(g, case, sample)
+        assert out["build_exact"] + out["build_replayed"] == len(sample)
 
 
 def test_queue_path_with_ragged_vocabulary():
