@@ -17,14 +17,15 @@
 // owns a contiguous slice of the row, loads all of it in one batch
 // of predicated 16-byte loads (one memory latency per level) and keeps the
 // slice's maximum and sum of exp2((t - max) * log2(e) / T) with packed
-// float32x2 arithmetic.  Each warp pushes its two numbers into the leader
-// CTA's shared memory (distributed shared memory) and arrives on the leader's
-// mbarrier; no cluster-wide barrier is taken per level.  The leader forms the
+// float32x2 arithmetic.  Each warp stores its two numbers into the leader
+// CTA's shared memory with asynchronous cluster stores that complete bytes of
+// the leader's mbarrier (no fence on the sending side); no cluster-wide
+// barrier is taken per level.  The leader forms the
 // row normaliser, turns the target logits of the node's <= |S| support tokens
 // (loaded at the start of the level, with the support itself prefetched when
 // the previous level decided) into exact p, forms the residual in parallel and
-// lets thread 0 take the <= K decisions, which it pushes to the other CTAs
-// with a remote mbarrier arrival.  For the bonus token the slice masses locate
+// lets thread 0 take the <= K decisions, which reach the other CTAs the same
+// way.  For the bonus token the slice masses locate
 // the slice that holds it, and the leader reads only that slice again,
 // scanning it in token-id order.
 #include <cooperative_groups.h>
@@ -288,18 +289,13 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t ran
   return r;
 }
 
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
-  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-// Arrival on an mbarrier of a CTA of the cluster, ordered after this
-// thread's earlier stores (release at cluster scope).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+// Asynchronous store of 4 bytes into the shared memory of a CTA of the
+// cluster, completing 4 bytes of the transaction count of an mbarrier there
+// (no fence: the data is visible to a thread that observes the phase).
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
+               "r"(bar)
+               : "memory");
 }
 
 // Support rank of the child in sibling slot `slot` (DET 0..m-1 -> ranks
@@ -337,7 +333,7 @@ __global__ void __launch_bounds__(NT, VER_MAX_THREADS / NT) __cluster_dims__(C, 
   const int nvec = static_cast<int>((static_cast<int64_t>(V) * E::ES) / 16);
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.stats_bar[i], NS);  // one arrival per warp of the cluster
+      mbar_init(&s.stats_bar[i], 1);  // the leader's expectation; the slices complete its bytes
       mbar_init(&s.dec_bar[i], 1);
     }
     fence_mbar_init();
@@ -386,15 +382,21 @@ __global__ void __launch_bounds__(NT, VER_MAX_THREADS / NT) __cluster_dims__(C, 
     // the level's accept uniforms, for thread 0's decisions after the barriers
     // below (its reads of the previous level's are done)
     if (er >= 0 && tid < K) s.uv_lv[tid] = L.u_verify[(static_cast<int64_t>(b) * D + level) * K + tid];
+    // this level's expected bytes: every slice's two statistics (leader), the
+    // decision (the others); a store may land before its expectation
+    if (tid == 0) {
+      if (leader) mbar_expect_tx(&s.stats_bar[par], static_cast<uint32_t>(NS) * 8u);
+      else mbar_expect_tx(&s.dec_bar[par], 4u);
+    }
     float wm, ws;
     slice_stats<T>(row, V, cr * NW + warp, NS, c, nonfinite, wm, ws);
     // target logits of the support tokens, landing while the slices arrive
     float t_sup = 0.0f;
     if (er >= 0 && tid < S) t_sup = E::load(row, sup_v);
     if (lane == 0) {
-      st_cluster_f32(par ? lead_m1 : lead_m0, wm);
-      st_cluster_f32(par ? lead_s1 : lead_s0, ws);
-      mbar_arrive_cluster(par ? lead_bar1 : lead_bar0);
+      const uint32_t bar = par ? lead_bar1 : lead_bar0;
+      st_async_b32(par ? lead_m1 : lead_m0, __float_as_uint(wm), bar);
+      st_async_b32(par ? lead_s1 : lead_s0, __float_as_uint(ws), bar);
     }
     int acc;
     if (leader) {
@@ -540,10 +542,8 @@ __global__ void __launch_bounds__(NT, VER_MAX_THREADS / NT) __cluster_dims__(C, 
       __syncthreads();
       acc = s.accepted;
       // publish the decision to the other CTAs of the cluster
-      if (tid >= 1 && tid < C) {
-        st_cluster_s32(cluster_addr(&s.dec[par], tid), acc);
-        mbar_arrive_cluster(cluster_addr(&s.dec_bar[par], tid));
-      }
+      if (tid >= 1 && tid < C)
+        st_async_b32(cluster_addr(&s.dec[par], tid), static_cast<uint32_t>(acc), cluster_addr(&s.dec_bar[par], tid));
       // the next node's support, while the decision travels
       if (acc >= 0) load_support(level + 1 < D ? s.nd_exp_row[acc] : -1);
     } else {
