@@ -325,12 +325,6 @@ __global__ void __launch_bounds__(NT, VER_MAX_THREADS / NT) __cluster_dims__(C, 
   const float Tmp = L.p.temperature;
   const float c = LOG2E / Tmp;
   const int64_t nb = static_cast<int64_t>(b) * t.max_nodes;
-  grid_dependency_wait();  // the tree comes from the previous kernel
-  grid_dependents_launch();
-  const int n_nodes = min(t.n_nodes[b], t.max_nodes);
-  const int64_t row_bytes = L.row_stride * E::ES;
-  const uint8_t* tgt = static_cast<const uint8_t*>(L.target);
-  const int nvec = static_cast<int>((static_cast<int64_t>(V) * E::ES) / 16);
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.stats_bar[i], 1);  // the leader's expectation; the slices complete its bytes
@@ -338,8 +332,20 @@ __global__ void __launch_bounds__(NT, VER_MAX_THREADS / NT) __cluster_dims__(C, 
     }
     fence_mbar_init();
   }
+  // barriers initialised cluster-wide before any remote arrival (this needs
+  // nothing from the previous kernel, so it overlaps that kernel's tail)
+  cluster.sync();
+  grid_dependency_wait();  // the tree comes from the previous kernel
+  grid_dependents_launch();
+  const int n_nodes = min(t.n_nodes[b], t.max_nodes);
+  const int64_t row_bytes = L.row_stride * E::ES;
+  const uint8_t* tgt = static_cast<const uint8_t*>(L.target);
+  const int nvec = static_cast<int>((static_cast<int64_t>(V) * E::ES) / 16);
   if (leader) {
-    for (int i = tid; i < n_nodes; i += NT) {
+    // every entry of the node arrays (unused ones hold -1), so that these
+    // loads need not wait for the node count
+    const int nmax = min(t.max_nodes, SPEC_TREE_MAX_NODES);
+    for (int i = tid; i < nmax; i += NT) {
       s.nd_parent[i] = t.node_parent[nb + i];
       s.nd_slot[i] = t.node_slot[nb + i];
       s.nd_exp_row[i] = t.node_exp_row[nb + i];
@@ -347,7 +353,7 @@ __global__ void __launch_bounds__(NT, VER_MAX_THREADS / NT) __cluster_dims__(C, 
     }
     if (tid == 0) s.u_bonus = L.u_bonus[b];
   }
-  cluster.sync();  // barriers initialised cluster-wide before any remote arrival
+  __syncthreads();  // the leader's node arrays
   bool nonfinite = false, timed_out = false;
   int node = 0, level = 0;
   int32_t* ot = L.out_tok + static_cast<int64_t>(b) * (D + 1);
