@@ -592,7 +592,6 @@ __device__ bool queue_select(WideShared& s, const uint8_t* row, int V, int nvec,
   constexpr int VEC = Elem<T>::VEC, U = 8;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt = (1u << lane) - 1u;
-  if (tid == 0) s.n_cand = 0;
   int nq = 0;  // this warp's queued vectors (warp-uniform)
   bool nan = false;
   for (int vb = 0; vb < nvec; vb += U * SW_THREADS) {  // warp-uniform trip count
@@ -618,28 +617,35 @@ __device__ bool queue_select(WideShared& s, const uint8_t* row, int V, int nvec,
     }
   }
   if (__syncthreads_or(nan || nq > SW_QW)) return false;
-  for (int i0 = 0; i0 < nq; i0 += 32) {  // warp-uniform trip count
-    const int i = i0 + lane;
-    const bool valid = i < nq;
-    const uint4 v = valid ? s.qvec[warp][i] : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t id0 = valid ? static_cast<uint32_t>(s.qvid[warp][i]) * VEC : 0u;
+  // the queued elements that reach the threshold: counted per lane (lane l
+  // takes its warp's queued vectors l, l + 32, ...; thread t also the element
+  // past the last whole vector, if any), placed by a block scan of the counts
+  // and written in order, so no shared counter is contended
+  const int id = nvec * VEC + tid;  // elements past the last whole vector
+  uint32_t tail_key = 0u;
+  if (id < V) tail_key = scalar_key<T>(row, id, nonfinite);
+  const bool tail = id < V && tail_key >= thr;
+  int cnt = tail ? 1 : 0;
+  for (int i = lane; i < nq; i += 32) {
+    const uint4 v = s.qvec[warp][i];
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) cnt += elem_key<T>(v, j, nonfinite) >= thr;
+  }
+  int n;
+  int pos = block_excl_scan(s, cnt, &n);
+  if (n < S || n > SW_CAP) return false;  // block-uniform
+  for (int i = lane; i < nq; i += 32) {
+    const uint4 v = s.qvec[warp][i];
+    const uint32_t id0 = static_cast<uint32_t>(s.qvid[warp][i]) * VEC;
 #pragma unroll
     for (int j = 0; j < VEC; ++j) {
-      const uint32_t key = valid ? elem_key<T>(v, j, nonfinite) : 0u;
-      warp_append(valid && key >= thr, make_comp(key, id0 + j), s.cand, &s.n_cand, SW_CAP);
+      const uint32_t key = elem_key<T>(v, j, nonfinite);
+      if (key >= thr) s.cand[pos++] = make_comp(key, id0 + j);
     }
   }
-  const int id = nvec * VEC + tid;  // elements past the last whole vector
-  if (id < V) {
-    const uint32_t key = scalar_key<T>(row, id, nonfinite);
-    if (key >= thr) {
-      const int pos = atomicAdd(&s.n_cand, 1);
-      if (pos < SW_CAP) s.cand[pos] = make_comp(key, static_cast<uint32_t>(id));
-    }
-  }
+  if (tail) s.cand[pos] = make_comp(tail_key, static_cast<uint32_t>(id));
+  if (tid == 0) s.n_cand = n;
   __syncthreads();
-  const int n = s.n_cand;
-  if (n < S || n > SW_CAP) return false;
   return sort_cand_desc(s, n);
 }
 
