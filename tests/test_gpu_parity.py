@@ -66,6 +66,54 @@ def test_bench_workload_every_tree():
     _full_batch("bench", WL.BENCH_WORKLOAD, 5, 3)
 
 
+@pytest.mark.parametrize("builder", ["topr", "smart"])
+def test_sweep_one_tree(builder):
+    """The batch sweep's smallest batch (one tree: one row per select CTA, one verify cluster of 8 CTAs
+    of 1024 threads), build and verify against the oracle."""
+    base = WL.WORKLOADS["sweep_smart"] if builder == "smart" else WL.BENCH_WORKLOAD
+    _report(f"sweep_{builder}_b1", parity.run_parity(base.with_(B=1), 31))
+
+
+class _Trees:
+    """Host copies of some trees of a device batch, indexed like the batch."""
+
+    def __init__(self, x, idx):
+        self.rows = {b: x[b].cpu() for b in idx}
+
+    def __getitem__(self, k):
+        if isinstance(k, tuple):
+            return self.rows[k[0]][k[1:]]
+        return self.rows[k]
+
+
+@pytest.mark.parametrize("builder", ["topr", "smart"])
+def test_sweep_256_trees_build_sampled(builder):
+    """The batch sweep's largest batch (256 trees, 48 draft rows per select CTA handed out on demand),
+    in the bench's launch configuration: inputs generated on the device, sampled trees' builds against
+    the oracle on host copies of their rows."""
+    from dynamic_tree_speculative_gb300 import binding as B
+    base = WL.WORKLOADS["sweep_smart"] if builder == "smart" else WL.BENCH_WORKLOAD
+    wl = base.with_(B=256)
+    params = B.Params.from_workload(wl)
+    n_rows = B.rows_needed(params)
+    draft, _ = WL.draft_logits(wl, 41, n_rows=n_rows, device="cuda")
+    u = WL.build_uniforms(wl, 41, n_rows=n_rows, device="cuda")
+    tree = B.TreeBuffers(params, wl.B)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.spec_tree_build(params, wl.V, draft, u, tree, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sample = [0, 85, 170, 255]
+    case = parity.Case(wl, _Trees(draft, sample), None, _Trees(u, sample), None, None, wl.V)
+    g = {k: getattr(tree, k).cpu().numpy() for k in (
+        "node_token", "node_parent", "node_depth", "node_kind", "node_slot", "node_exp_row", "node_score",
+        "n_nodes", "sup_id", "sup_q", "sup_qT", "sup_z", "sup_zT", "probe_pos")}
+    del draft
+    out = parity.compare_case(g, case, sample)
+    _report(f"sweep_{builder}_b256", out)
+    assert out["build_exact"] + out["build_replayed"] == len(sample)
+
+
 @pytest.mark.parametrize("seed", [0, 1])
 def test_smart_parity(seed):
     wl = WL.WORKLOADS["sweep_smart"].with_(B=6, V=32000)
