@@ -1451,7 +1451,12 @@ cudaError_t launch_select_expand(int dtype, const SelLaunch& L, cudaStream_t str
   a.status = L.status;
   if (a.total_rows == 0) return cudaSuccess;
   const size_t smem = sizeof(SelShared);
-  const int64_t grid = min64(a.total_rows, static_cast<int64_t>(L.num_sms) * L.ctas_per_sm);
+  // as many CTAs as give every CTA the same number of rows (e.g. 456 rows
+  // on 228 CTAs, two each, rather than on 304 with a second wave of 152 rows
+  // streamed by half the CTAs, too few bytes in flight to fill the HBM)
+  const int64_t max_ctas = static_cast<int64_t>(L.num_sms) * L.ctas_per_sm;
+  const int64_t per_cta = (a.total_rows + max_ctas - 1) / max_ctas;
+  const int64_t grid = (a.total_rows + per_cta - 1) / per_cta;
   // rows on demand once a CTA has several; with one or two rows a CTA the
   // fixed order spreads the second rows evenly over the SMs
   a.sched = a.total_rows >= 4 * grid ? reinterpret_cast<unsigned int*>(L.sched) : nullptr;
