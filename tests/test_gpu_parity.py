@@ -295,24 +295,25 @@ def test_rows_whose_cut_jumps():
     _report("cut jumps", res)
 
 
-@pytest.mark.parametrize("support,V,stride", [(128, 32000, None), (256, 32000, None), (1024, 32000, None),
-                                              (256, 32001, 32008)])
-def test_cut_hint_from_the_previous_call(support, V, stride):
+@pytest.mark.parametrize("support,V,stride,B", [(128, 32000, None, 8), (256, 32000, None, 8), (1024, 32000, None, 8),
+                                                (256, 32001, 32008, 8), (128, 128256, None, 2)])
+def test_cut_hint_from_the_previous_call(support, V, stride, B):
     """The row schedule keeps a cut key of the latest call (of the latest row, for supports above 128)
     as the predicted queue threshold of the next rows.  The second call's rows here differ wildly from
     the first's (scaled by 3, shifted by 5), so the hint lies far below their cut and the exact path must
     take over; a third call on the same rows hits it; a fourth on rows like the first's gets a hint far
     above their cut.  Every call equals the oracle.  A vocabulary that is not a multiple of the vector
-    width sends its last elements through their own branch."""
-    from dynamic_tree_speculative_gb300 import binding as B
-    wl = WL.WORKLOADS["vicuna"].with_(B=8, V=V, support=support)
-    params = B.Params.from_workload(wl)
-    tree = B.TreeBuffers(params, wl.B)
+    width sends its last elements through their own branch; two trees of the LLaMA-3 vocabulary (114
+    rows, no more than SMs) run one CTA per SM with the deep ring."""
+    from dynamic_tree_speculative_gb300 import binding
+    wl = WL.WORKLOADS["vicuna"].with_(B=B, V=V, support=support)
+    params = binding.Params.from_workload(wl)
+    tree = binding.TreeBuffers(params, wl.B)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     for i, (scale, shift) in enumerate([(1.0, 0.0), (3.0, 5.0), (3.0, 5.0), (1.0, 0.0)]):
         case = parity.make_case(wl, 70 + i, row_stride=stride)
         case.draft = (case.draft.float() * scale + shift).to(torch.bfloat16)
-        B.spec_tree_build(params, wl.V, case.draft.cuda(), case.u_probe.cuda(), tree, status)
+        binding.spec_tree_build(params, wl.V, case.draft.cuda(), case.u_probe.cuda(), tree, status)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         hint = int(tree.sched[2].item())
