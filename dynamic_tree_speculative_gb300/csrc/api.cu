@@ -75,10 +75,16 @@ int check_tree(const spec_tree_params* p, const spec_tree_t* t, int V, bool need
 
 cudaStream_t as_stream(spec_tree_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// bf16 rows of 8192 to 262144 tokens: the queue path's range
+constexpr int SPLIT_MIN_V = 8192, SPLIT_MAX_V = 262144;
+
 // the streaming kernel for supports of up to 128 tokens, else one CTA per row
-// (the dense support of a large vocabulary by its own kernel)
+// (the dense support of a large vocabulary by its own kernel); batches with
+// fewer rows than CTA slots split each row over a cluster of CTAs
 cudaError_t launch_select(int dtype, const st::SelLaunch& L, cudaStream_t stream) {
   if (L.dense) return st::launch_select_dense(dtype, L, stream);
+  if (dtype == SPEC_TREE_BF16 && L.V >= SPLIT_MIN_V && L.V <= SPLIT_MAX_V && st::select_split_parts(L) > 1)
+    return st::launch_select_split(dtype, L, stream);
   return L.S <= 128 ? st::launch_select_expand(dtype, L, stream) : st::launch_select_wide(dtype, L, stream);
 }
 

@@ -30,6 +30,7 @@
 #include "st_common.cuh"
 #include "st_keys.cuh"
 #include "st_kernels.h"
+#include "st_epilogue.cuh"
 
 namespace st {
 
@@ -78,6 +79,7 @@ struct WideShared {
   unsigned long long red64[2][SW_WARPS];
   unsigned long long above_mass;
   int nth_id;
+  int part_n[8];  // split rows (leader): each part's candidate count, -1 if it declined
 };
 
 // Calls f(key, id) for every element of the row that thread tid owns: the
@@ -586,25 +588,30 @@ __device__ bool table_select(WideShared& s, const uint8_t* row, int V, int nvec,
 // Block-uniform.
 __device__ __forceinline__ uint32_t wide_queue_margin(int S) { return S <= 256 ? 16u : S <= 512 ? 10u : 6u; }
 
+// The queue path's candidates of the vectors [v0, v1) of a row (and, with
+// `tail`, of the elements past its last whole vector): every element that
+// reaches thr, in s.cand[0..n).  Returns n, or -1 when a warp's queue
+// overflows, a NaN is seen or more than SW_CAP elements reach thr.
+// Block-uniform.
 template <typename T>
-__device__ bool queue_select(WideShared& s, const uint8_t* row, int V, int nvec, int S, uint32_t thr,
-                             bool& nonfinite) {
+__device__ int queue_collect(WideShared& s, const uint8_t* row, int V, int nvec, int v0, int v1, bool tail,
+                             uint32_t thr, bool& nonfinite) {
   constexpr int VEC = Elem<T>::VEC, U = 8;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt = (1u << lane) - 1u;
   int nq = 0;  // this warp's queued vectors (warp-uniform)
   bool nan = false;
-  for (int vb = 0; vb < nvec; vb += U * SW_THREADS) {  // warp-uniform trip count
+  for (int vb = v0; vb < v1; vb += U * SW_THREADS) {  // warp-uniform trip count
     uint4 v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int vi = vb + u * SW_THREADS + tid;
-      if (vi < nvec) v[u] = ldg_stream(row + static_cast<int64_t>(vi) * 16);
+      if (vi < v1) v[u] = ldg_stream(row + static_cast<int64_t>(vi) * 16);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int vi = vb + u * SW_THREADS + tid;
-      const bool pass = vi < nvec && vec_max_key16<T>(v[u], nan) >= thr;
+      const bool pass = vi < v1 && vec_max_key16<T>(v[u], nan) >= thr;
       const unsigned bal = __ballot_sync(FULL, pass);
       if (bal != 0u) {
         const int slot = nq + __popc(bal & lt);
@@ -616,16 +623,16 @@ __device__ bool queue_select(WideShared& s, const uint8_t* row, int V, int nvec,
       }
     }
   }
-  if (__syncthreads_or(nan || nq > SW_QW)) return false;
+  if (__syncthreads_or(nan || nq > SW_QW)) return -1;
   // the queued elements that reach the threshold: counted per lane (lane l
   // takes its warp's queued vectors l, l + 32, ...; thread t also the element
   // past the last whole vector, if any), placed by a block scan of the counts
   // and written in order, so no shared counter is contended
   const int id = nvec * VEC + tid;  // elements past the last whole vector
   uint32_t tail_key = 0u;
-  if (id < V) tail_key = scalar_key<T>(row, id, nonfinite);
-  const bool tail = id < V && tail_key >= thr;
-  int cnt = tail ? 1 : 0;
+  if (tail && id < V) tail_key = scalar_key<T>(row, id, nonfinite);
+  const bool take_tail = tail && id < V && tail_key >= thr;
+  int cnt = take_tail ? 1 : 0;
   for (int i = lane; i < nq; i += 32) {
     const uint4 v = s.qvec[warp][i];
 #pragma unroll
@@ -633,7 +640,7 @@ __device__ bool queue_select(WideShared& s, const uint8_t* row, int V, int nvec,
   }
   int n;
   int pos = block_excl_scan(s, cnt, &n);
-  if (n < S || n > SW_CAP) return false;  // block-uniform
+  if (n > SW_CAP) return -1;  // block-uniform
   for (int i = lane; i < nq; i += 32) {
     const uint4 v = s.qvec[warp][i];
     const uint32_t id0 = static_cast<uint32_t>(s.qvid[warp][i]) * VEC;
@@ -643,8 +650,16 @@ __device__ bool queue_select(WideShared& s, const uint8_t* row, int V, int nvec,
       if (key >= thr) s.cand[pos++] = make_comp(key, id0 + j);
     }
   }
-  if (tail) s.cand[pos] = make_comp(tail_key, static_cast<uint32_t>(id));
-  if (tid == 0) s.n_cand = n;
+  if (take_tail) s.cand[pos] = make_comp(tail_key, static_cast<uint32_t>(id));
+  return n;
+}
+
+template <typename T>
+__device__ bool queue_select(WideShared& s, const uint8_t* row, int V, int nvec, int S, uint32_t thr,
+                             bool& nonfinite) {
+  const int n = queue_collect<T>(s, row, V, nvec, 0, nvec, true, thr, nonfinite);
+  if (n < S) return false;  // block-uniform (n = -1: declined)
+  if (threadIdx.x == 0) s.n_cand = n;
   __syncthreads();
   return sort_cand_desc(s, n);
 }
@@ -745,27 +760,14 @@ __device__ void wide_epilogue(WideShared& s, const SelLaunch& a, int64_t out_row
   }
 }
 
+// The rest of a row once `done` says whether its exact top-|S| is sorted in
+// s.cand: otherwise the table path (rows of 2048 to SW_TBL vectors) and, when
+// that declines, the exact radix select; then the row's cut as the next
+// rows' hint and the epilogue.
 template <typename T>
-__global__ void __launch_bounds__(SW_THREADS, 2) select_wide_kernel(SelLaunch a, int64_t row_bytes) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  WideShared& s = *reinterpret_cast<WideShared*>(smem_raw);
-  const int64_t g = blockIdx.x;
-  const int64_t b = g / a.rows_used, e = g % a.rows_used;
-  const int64_t out_row = b * a.n_rows + a.sup_row0 + e;
-  const int64_t in_row = b * a.in_rows + e;
-  grid_dependency_wait();
-  grid_dependents_launch();
-  const uint8_t* row = static_cast<const uint8_t*>(a.logits) + in_row * row_bytes;
-  const int nvec = static_cast<int>((static_cast<int64_t>(a.V) * Elem<T>::ES) / 16);
-  bool nonfinite = false;
-  // rows of 2048 to SW_TBL vectors: the queue path when a recent row's cut is
-  // known (bf16), else or when it declines the table path; otherwise, or when
-  // that declines, the exact radix select
+__device__ void finish_row(WideShared& s, const SelLaunch& a, const uint8_t* row, int nvec, int64_t out_row,
+                           int64_t in_row, uint32_t* hint, bool done, bool& nonfinite) {
   const bool tabled = nvec >= 2 * SW_THREADS && nvec <= SW_TBL;
-  uint32_t* hint = a.sched != nullptr ? reinterpret_cast<uint32_t*>(a.sched) + 2 : nullptr;
-  const uint32_t h = hint != nullptr && sizeof(T) == 2 && tabled ? *reinterpret_cast<volatile uint32_t*>(hint) : 0u;
-  const uint32_t margin = wide_queue_margin(a.S);
-  bool done = h > margin && queue_select<T>(s, row, a.V, nvec, a.S, h - margin, nonfinite);
   if (!done && tabled) {
     __syncthreads();  // the queue shares its storage with the table
     done = table_select<T>(s, row, a.V, nvec, a.S, nonfinite);
@@ -784,8 +786,171 @@ __global__ void __launch_bounds__(SW_THREADS, 2) select_wide_kernel(SelLaunch a,
   // plain store, read by CTAs that start later and by the next launch)
   if (threadIdx.x == 0 && hint != nullptr && sizeof(T) == 2 && n == a.S)
     *reinterpret_cast<volatile uint32_t*>(hint) = static_cast<uint32_t>(s.cand[n - 1] >> 32);
-  wide_epilogue<T>(s, a, out_row, in_row, n);
+  if (a.S <= 128) {
+    // the streaming kernel's epilogue, by warp 0: the same supports bit for bit
+    if (threadIdx.x < 32) {
+      uint64_t val[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = j * 32 + static_cast<int>(threadIdx.x);
+        val[j] = r < n ? s.cand[r] : 0ull;
+      }
+      expand_epilogue<T>(val, a, out_row, in_row, n);
+    }
+  } else {
+    wide_epilogue<T>(s, a, out_row, in_row, n);
+  }
   if (nonfinite) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
+}
+
+// A recent row's cut from the row schedule (bf16 rows the queue path can
+// take), else 0.
+template <typename T>
+__device__ __forceinline__ uint32_t read_hint(const uint32_t* hint, int nvec) {
+  const bool tabled = nvec >= 2 * SW_THREADS && nvec <= SW_TBL;
+  return hint != nullptr && sizeof(T) == 2 && tabled ? *reinterpret_cast<const volatile uint32_t*>(hint) : 0u;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(SW_THREADS, 2) select_wide_kernel(SelLaunch a, int64_t row_bytes) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  WideShared& s = *reinterpret_cast<WideShared*>(smem_raw);
+  const int64_t g = blockIdx.x;
+  const int64_t b = g / a.rows_used, e = g % a.rows_used;
+  const int64_t out_row = b * a.n_rows + a.sup_row0 + e;
+  const int64_t in_row = b * a.in_rows + e;
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const uint8_t* row = static_cast<const uint8_t*>(a.logits) + in_row * row_bytes;
+  const int nvec = static_cast<int>((static_cast<int64_t>(a.V) * Elem<T>::ES) / 16);
+  bool nonfinite = false;
+  // the queue path when a recent row's cut is known, else or when it
+  // declines the table path, else the radix select
+  uint32_t* hint = a.sched != nullptr ? reinterpret_cast<uint32_t*>(a.sched) + 2 : nullptr;
+  const uint32_t h = read_hint<T>(hint, nvec);
+  const uint32_t margin = wide_queue_margin(a.S);
+  const bool done = h > margin && queue_select<T>(s, row, a.V, nvec, a.S, h - margin, nonfinite);
+  finish_row<T>(s, a, row, nvec, out_row, in_row, hint, done, nonfinite);
+}
+
+// ------------------------------------------------------------- split rows ---
+// Batches with fewer rows than CTA slots: each row is split over a cluster
+// of P CTAs.  Every CTA streams its 1/P of the row on the queue path (the
+// last one also the elements past the last whole vector) and counts its
+// candidates; the counts meet in the leader CTA's shared memory, each CTA
+// copies its candidates there behind the others' (distributed shared memory),
+// and the leader sorts them and runs the epilogue.  Exact by the queue path's
+// argument over the whole row: every element that reaches the threshold is a
+// candidate of its part.  When any part declines (no hint, NaN, a full
+// queue) or fewer than |S| or more than SW_CAP elements reach the threshold,
+// the leader takes the whole row on the table or radix path.
+__device__ __forceinline__ uint32_t sw_cluster_addr(const void* local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  return r;
+}
+
+template <typename T, int P>
+__global__ void __launch_bounds__(SW_THREADS, 2) select_split_kernel(SelLaunch a, int64_t row_bytes) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  WideShared& s = *reinterpret_cast<WideShared*>(smem_raw);
+  uint32_t part;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(part));
+  const int tid = threadIdx.x;
+  const int64_t g = blockIdx.x / P;
+  const int64_t b = g / a.rows_used, e = g % a.rows_used;
+  const int64_t out_row = b * a.n_rows + a.sup_row0 + e;
+  const int64_t in_row = b * a.in_rows + e;
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const uint8_t* row = static_cast<const uint8_t*>(a.logits) + in_row * row_bytes;
+  const int nvec = static_cast<int>((static_cast<int64_t>(a.V) * Elem<T>::ES) / 16);
+  bool nonfinite = false;
+  uint32_t* hint = a.sched != nullptr ? reinterpret_cast<uint32_t*>(a.sched) + 2 : nullptr;
+  const uint32_t h = read_hint<T>(hint, nvec);
+  const uint32_t margin = wide_queue_margin(a.S);
+  int np = -1;  // this part's candidates (-1: declined)
+  if (h > margin) {
+    const int per = (nvec + P - 1) / P;
+    const int v0 = min(static_cast<int>(part) * per, nvec), v1 = min(v0 + per, nvec);
+    np = queue_collect<T>(s, row, a.V, nvec, v0, v1, part == P - 1, h - margin, nonfinite);
+  }
+  if (tid == 0) {
+    const uint32_t dst = sw_cluster_addr(&s.part_n[part], 0);
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(dst), "r"(np) : "memory");
+  }
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  int off = 0, total = 0;
+  bool ok = true;
+#pragma unroll
+  for (int q = 0; q < P; ++q) {
+    int nq;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(nq) : "r"(sw_cluster_addr(&s.part_n[q], 0)) : "memory");
+    ok = ok && nq >= 0;
+    if (q < static_cast<int>(part)) off += nq;
+    total += nq;
+  }
+  ok = ok && total >= a.S && total <= SW_CAP;
+  if (ok && part != 0)
+    for (int i = tid; i < np; i += SW_THREADS) {
+      const uint32_t dst = sw_cluster_addr(&s.cand[off + i], 0);
+      asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(dst), "l"(s.cand[i]) : "memory");
+    }
+  // the candidates are in place, and no CTA writes into another after this
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (part != 0) {
+    if (nonfinite) set_status(a.status, SPEC_TREE_S_NONFINITE_DRAFT);
+    return;
+  }
+  bool done = false;
+  if (ok) {
+    if (tid == 0) s.n_cand = total;
+    __syncthreads();
+    done = sort_cand_desc(s, total);
+  }
+  finish_row<T>(s, a, row, nvec, out_row, in_row, hint, done, nonfinite);
+}
+
+template <typename T, int P>
+cudaError_t launch_split_p(const SelLaunch& L, int64_t row_bytes, cudaStream_t stream) {
+  const int smem = static_cast<int>(sizeof(WideShared));
+  cudaError_t err = cudaFuncSetAttribute(select_split_kernel<T, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(L.B) * L.rows_used * P));
+  cfg.blockDim = dim3(SW_THREADS);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = P;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, select_split_kernel<T, P>, L, row_bytes);
+}
+
+int select_split_parts(const SelLaunch& L) {
+  // the most parts (<= 8) that keep every row's parts in one wave of two
+  // CTAs per SM; 1: no split
+  const int64_t rows = static_cast<int64_t>(L.B) * L.rows_used;
+  const int64_t slots = static_cast<int64_t>(L.num_sms) * 2;
+  int p = 8;
+  while (p > 1 && rows * p > slots) p /= 2;
+  return rows == 0 ? 1 : p;
+}
+
+cudaError_t launch_select_split(int dtype, const SelLaunch& L, cudaStream_t stream) {
+  // bf16 rows only: the queue path is bf16's
+  if (dtype != SPEC_TREE_BF16) return cudaErrorInvalidValue;
+  const int P = select_split_parts(L);
+  const int64_t rb = L.row_stride * 2;
+  if (P >= 8) return launch_split_p<__nv_bfloat16, 8>(L, rb, stream);
+  if (P == 4) return launch_split_p<__nv_bfloat16, 4>(L, rb, stream);
+  return launch_split_p<__nv_bfloat16, 2>(L, rb, stream);
 }
 
 // ------------------------------------------------------------ dense support ---

@@ -71,6 +71,10 @@ size_t select_expand_smem_bytes();
 cudaError_t launch_select_expand(int dtype, const SelLaunch& L, cudaStream_t stream);
 // supports of 129 to 1024 tokens
 cudaError_t launch_select_wide(int dtype, const SelLaunch& L, cudaStream_t stream);
+// batches with fewer rows than CTA slots: each row split over a cluster of
+// select_split_parts(L) CTAs (1: no split, use the other kernels)
+int select_split_parts(const SelLaunch& L);
+cudaError_t launch_select_split(int dtype, const SelLaunch& L, cudaStream_t stream);
 // the dense support of a vocabulary above SPEC_TREE_MAX_SUPPORT tokens
 cudaError_t launch_select_dense(int dtype, const SelLaunch& L, cudaStream_t stream);
 cudaError_t launch_rank_topr(const RankLaunch& L, cudaStream_t stream);
