@@ -161,12 +161,13 @@ typedef struct spec_tree_params {
  *                on demand from this counter (a CTA that runs ahead takes
  *                more rows, so they finish together) and leaves both words at
  *                zero again when it ends.  [2]: the top-|S| cut key of a
- *                recent row (of the latest call for |S| <= 128; of the latest
- *                row finished for larger supports, which rows starting later
- *                in the same call read too), taken as the predicted queue
- *                threshold of the next rows (a hint only: a wrong value costs
- *                time, never a different result; any value is valid).  NULL:
- *                rows are dealt to the CTAs in a fixed order, no hint is kept.
+ *                recent row (of the latest call, or of the latest row finished
+ *                when rows are selected one CTA or one cluster per row, which
+ *                rows starting later in the same call read too), taken as the
+ *                predicted queue threshold of the next rows (a hint only: a
+ *                wrong value costs time, never a different result; any value
+ *                is valid).  NULL: rows are dealt to the CTAs in a fixed
+ *                order, no hint is kept.
  *                Calls that overlap on the GPU must not share one counter.
  */
 typedef struct spec_tree_t {
