@@ -752,16 +752,18 @@ cudaError_t launch_verify_n(const VerifyLaunch& L, int C, cudaStream_t stream) {
 
 template <typename T>
 cudaError_t launch_verify_t(const VerifyLaunch& L, cudaStream_t stream) {
-  // Threads per tree: the most (<= 8 x 1024) that keep the batch in one wave
-  // (an SM runs 1024 threads at 64 registers), spread over the largest
-  // cluster (<= 8 CTAs) whose CTAs keep >= 256 threads and one thread per
-  // support token.  More CTAs per tree put more SMs, and their exp2 units, on
-  // the row of the slowest tree; the slices (warps x CTAs) stay as many.
-  // A cluster shape the device cannot place is refused at launch, and the
-  // next smaller one is tried.
+  // Threads per tree: the most that keep the batch in one wave (an SM runs
+  // 1024 threads at 64 registers), up to 8 CTAs of the smallest size that
+  // gives one thread per support token (256 for |S| <= 256), spread over the
+  // largest cluster (<= 8 CTAs).  More CTAs per tree put more SMs, and their
+  // exp2 units, on the row of the slowest tree; small CTAs keep the leader's
+  // per-level barriers cheap (at 1-16 trees, clusters of 8 CTAs of 256
+  // threads beat clusters of 8 of 1024 by 5-11 us a step).  A cluster shape
+  // the device cannot place is refused at launch, and the next smaller one is
+  // tried.
   const int nt_min = L.S <= 256 ? 256 : L.S <= 512 ? 512 : VER_MAX_THREADS;
   const int64_t budget = static_cast<int64_t>(L.num_sms) * VER_MAX_THREADS / L.B;
-  int per_tree = VER_MAX_CLUSTER * VER_MAX_THREADS;
+  int per_tree = VER_MAX_CLUSTER * nt_min;
   while (per_tree > nt_min && per_tree > budget) per_tree /= 2;
   cudaError_t err = cudaErrorInvalidValue;
   for (int C = min(VER_MAX_CLUSTER, per_tree / nt_min); C >= 1; C /= 2) {
