@@ -44,7 +44,7 @@
 
 namespace st {
 
-constexpr int RANK_THREADS = 256;
+constexpr int RANK_THREADS = 512;
 constexpr int RK_PER_THREAD = (SPEC_TREE_MAX_CAND + RANK_THREADS - 1) / RANK_THREADS;
 constexpr int RK_MAX_LAYERS = 256;  // depth <= 255
 
