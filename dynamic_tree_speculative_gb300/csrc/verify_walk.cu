@@ -43,7 +43,9 @@ namespace st {
 
 constexpr int VER_MAX_THREADS = 1024;  // threads of a CTA: 256, 512 or 1024 (an SM runs 1024 at 64 registers)
 constexpr int VER_WARPS = VER_MAX_THREADS / 32;
-constexpr int VER_MAX_CLUSTER = 8;
+constexpr int VER_MAX_CLUSTER = 8;    // portable cluster size
+constexpr int VER_WIDE_CLUSTER = 16;  // batches of <= num_sms / 16 trees with long rows: non-portable clusters
+constexpr int VER_WIDE_MIN_V = 65536; //   of 16 CTAs, for rows of at least this many tokens
 constexpr int VER_MAX_SLICES = VER_WARPS * VER_MAX_CLUSTER;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr double MASS_MARGIN = 1e-6;
@@ -309,11 +311,12 @@ __device__ __forceinline__ int rank_of_slot(int slot, int m, int pp) {
 }
 
 template <typename T, int C, int NT>
-__global__ void __launch_bounds__(NT, VER_MAX_THREADS / NT) __cluster_dims__(C, 1, 1) verify_kernel(VerifyLaunch L) {
+__global__ void __launch_bounds__(NT, VER_MAX_THREADS / NT) verify_kernel(VerifyLaunch L) {  // clusters of C CTAs
   using E = VElem<T>;
   constexpr int VEC = E::VEC;
   constexpr int NW = NT / 32;   // warps of a CTA
   constexpr int NS = NW * C;    // slices per row
+  static_assert(NS <= VER_MAX_SLICES, "the slice statistics must fit the leader's arrays");
   extern __shared__ __align__(16) uint8_t smem_raw[];
   VerShared& s = *reinterpret_cast<VerShared*>(smem_raw);
   cg::cluster_group cluster = cg::this_cluster();
@@ -728,12 +731,53 @@ __global__ void __launch_bounds__(NT, VER_MAX_THREADS / NT) __cluster_dims__(C, 
   cluster.sync();
 }
 
+// Launch configuration of verify_kernel<T, C, NT>: the batch's clusters of
+// C CTAs (a runtime cluster shape; above 8 CTAs a non-portable one),
+// programmatic dependent launch on the stream.
 template <typename T, int C, int NT>
-cudaError_t launch_verify_c(const VerifyLaunch& L, cudaStream_t stream) {
+cudaError_t verify_config(const VerifyLaunch& L, cudaStream_t stream, cudaLaunchConfig_t& cfg,
+                          cudaLaunchAttribute (&attr)[2]) {
   const int smem = static_cast<int>(sizeof(VerShared));
   cudaError_t err = cudaFuncSetAttribute(verify_kernel<T, C, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err == cudaSuccess && C > VER_MAX_CLUSTER)
+    err = cudaFuncSetAttribute(verify_kernel<T, C, NT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cfg = cudaLaunchConfig_t{};
+  cfg.gridDim = dim3(static_cast<unsigned>(L.B * C));
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = C;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return err;
+}
+
+template <typename T, int C, int NT>
+cudaError_t launch_verify_c(const VerifyLaunch& L, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  cudaError_t err = verify_config<T, C, NT>(L, stream, cfg, attr);
   if (err != cudaSuccess) return err;
-  return launch_pdl(verify_kernel<T, C, NT>, dim3(L.B * C), dim3(NT), smem, stream, L);
+  return cudaLaunchKernelEx(&cfg, verify_kernel<T, C, NT>, L);
+}
+
+// Whether the device holds the batch's clusters of C CTAs in one wave.
+template <typename T, int C, int NT>
+bool verify_fits(const VerifyLaunch& L, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (verify_config<T, C, NT>(L, stream, cfg, attr) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, verify_kernel<T, C, NT>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();  // the query's own error, not a launch's
+    return false;
+  }
+  return n >= L.B;
 }
 
 template <typename T, int NT>
@@ -762,6 +806,12 @@ cudaError_t launch_verify_t(const VerifyLaunch& L, cudaStream_t stream) {
   // the device cannot place is refused at launch, and the next smaller one is
   // tried.
   const int nt_min = L.S <= 256 ? 256 : L.S <= 512 ? 512 : VER_MAX_THREADS;
+  // few trees with long rows: clusters of 16 CTAs of 256 threads (a level's
+  // row summed on 16 SMs), when the device holds them all at once; shorter
+  // rows leave too little work per CTA for the extra slices to pay
+  if (nt_min == 256 && L.V >= VER_WIDE_MIN_V && static_cast<int64_t>(L.B) * VER_WIDE_CLUSTER <= L.num_sms &&
+      verify_fits<T, VER_WIDE_CLUSTER, 256>(L, stream))
+    return launch_verify_c<T, VER_WIDE_CLUSTER, 256>(L, stream);
   const int64_t budget = static_cast<int64_t>(L.num_sms) * VER_MAX_THREADS / L.B;
   int per_tree = VER_MAX_CLUSTER * nt_min;
   while (per_tree > nt_min && per_tree > budget) per_tree /= 2;
