@@ -79,7 +79,8 @@ struct WideShared {
   unsigned long long red64[2][SW_WARPS];
   unsigned long long above_mass;
   int nth_id;
-  int part_n[8];  // split rows (leader): each part's candidate count, -1 if it declined
+  int part_n[8];        // split rows (leader): each part's candidate count, -1 if it declined
+  uint32_t part_h[8];   //   and the cut hint it read (the parts must have used one threshold)
 };
 
 // Calls f(key, id) for every element of the row that thread tid owns: the
@@ -876,17 +877,22 @@ __global__ void __launch_bounds__(SW_THREADS, 2) select_split_kernel(SelLaunch a
     np = queue_collect<T>(s, row, a.V, nvec, v0, v1, part == P - 1, h - margin, nonfinite);
   }
   if (tid == 0) {
-    const uint32_t dst = sw_cluster_addr(&s.part_n[part], 0);
-    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(dst), "r"(np) : "memory");
+    const uint32_t dn = sw_cluster_addr(&s.part_n[part], 0), dh = sw_cluster_addr(&s.part_h[part], 0);
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(dn), "r"(np) : "memory");
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(dh), "r"(h) : "memory");
   }
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  // a hint another row's leader rewrote between the parts' reads would give
+  // the parts different thresholds: then the leader takes the whole row
   int off = 0, total = 0;
   bool ok = true;
 #pragma unroll
   for (int q = 0; q < P; ++q) {
     int nq;
+    uint32_t hq;
     asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(nq) : "r"(sw_cluster_addr(&s.part_n[q], 0)) : "memory");
-    ok = ok && nq >= 0;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(hq) : "r"(sw_cluster_addr(&s.part_h[q], 0)) : "memory");
+    ok = ok && nq >= 0 && hq == h;
     if (q < static_cast<int>(part)) off += nq;
     total += nq;
   }
