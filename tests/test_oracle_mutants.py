@@ -13,7 +13,9 @@ The mistakes are the plausible ones for each part of the method:
   * expansion and verification (RheoSampling notes, Key designs 2 and 3): q~
     formed from the untempered q, the probe's proxy replaced by its true
     probability, the token id inside the ranking key, the residual without
-    max(0, .).
+    max(0, .), the target p left untempered, the bonus drawn from p instead
+    of the final residual;
+  * truncation (Key design 1): ties at the cut broken by descending id.
 """
 import pathlib
 import sys
@@ -46,6 +48,15 @@ def _smart_golden():
 def _lemma():
     for m in (1, 2):
         pins.test_local_ranking_preservation_lemma(m, 1.0)
+
+
+def _support_brute_force():
+    for V, size in [(300, 128), (3000, 256)]:
+        pins.test_support_is_brute_force_top_by_logit_then_id(V, size)
+
+
+def _chi_square():
+    pins.test_losslessness_chi_square_two_levels(0)
 
 
 def _lossless():
@@ -86,6 +97,18 @@ MUTANTS = {
         "        wn = np.maximum(0.0, w / Zr - qt)",
         "        wn = w / Zr - qt",
         [pins.test_hand_worked_verification_level, _lossless]),
+    "support_ties_by_id_descending": (
+        '    return np.argsort(-row, kind="stable")[:size]',
+        '    return (len(row) - 1 - np.argsort(-row[::-1], kind="stable"))[:size]',
+        [_support_brute_force]),
+    "target_p_untempered": (
+        "    e = np.exp((t - t.max()) / temperature)",
+        "    e = np.exp(t - t.max())",
+        [pins.test_target_probs_match_scipy]),
+    "bonus_from_p_not_the_residual": (
+        "        cum = np.cumsum(w)",
+        "        cum = np.cumsum(p_full) * Zr",
+        [_chi_square]),
 }
 
 

@@ -54,6 +54,16 @@ def test_support_treats_signed_zeros_equal_and_nan_last():
     assert O.support_of(row, 6)[-1] == 2
 
 
+def test_target_probs_match_scipy():
+    """p = softmax(t / T) over the whole vocabulary (RheoSampling, training strategy: verification at
+    temperature T), against scipy's softmax."""
+    rng = np.random.default_rng(3)
+    for T in (1.0, 0.7, 1.6):
+        row = _bf16_row(rng, 5000)
+        np.testing.assert_allclose(O.target_probs(row, T), scipy.special.softmax(row.astype(np.float64) / T),
+                                   rtol=1e-12, atol=1e-15)
+
+
 def test_truncated_softmax_matches_scipy():
     rng = np.random.default_rng(1)
     for T in (1.0, 0.7, 1.6):
