@@ -20,7 +20,10 @@
 //      w = max(0, a - c q~) on the tail has mass Zr - that sum;
 //   4. when every child is rejected, or the node has none, the bonus is the
 //      first token in id order whose cumulative w exceeds u_bonus * Zr: a scan
-//      in rounds of VD_THREADS consecutive vectors, each with a block scan.
+//      in rounds of VD_THREADS consecutive vectors, each with a block scan in
+//      float32 and the carry of the earlier rounds in float64 (the GPU's
+//      float64 rate is a small fraction of its float32 rate: with every
+//      partial sum in float64 the scan took most of the kernel).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -79,7 +82,6 @@ struct VDShared {
   int nzero;
   float red_m[VD_WARPS];
   float red_s[VD_WARPS];
-  double redd[VD_WARPS];
   int flag;
   // broadcast state of the level
   float M, invZp, c;  // target normaliser; c = log2(e) / T
@@ -117,18 +119,6 @@ __device__ __forceinline__ bool in_list(const int* list, int n, int v) {
   for (int k = 0; k < n; ++k)
     if (list[k] == v) return true;
   return false;
-}
-
-__device__ __forceinline__ double block_sum_d(VDShared& s, double x) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(FULL, x, o);
-  if (lane == 0) s.redd[warp] = x;
-  __syncthreads();
-  double t = 0.0;
-  for (int w = 0; w < VD_WARPS; ++w) t += s.redd[w];
-  __syncthreads();
-  return t;
 }
 
 template <typename T>
@@ -279,8 +269,16 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_dense_kernel(VerifyLaunc
           comp = (tt - acc) - y;
           acc = tt;
         });
-        const double tot = block_sum_d(s, static_cast<double>(acc));
+        // warp sums in float, the 32 of them added in double by thread 0 (the
+        // SM's float64 rate is a small fraction of its float32 rate)
+        float part = acc - comp;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(FULL, part, o);
+        if (lane == 0) s.red_s[warp] = part;
+        __syncthreads();
         if (tid == 0) {
+          double tot = 0.0;
+          for (int w = 0; w < VD_WARPS; ++w) tot += static_cast<double>(s.red_s[w]);
           s.Zr = static_cast<float>(static_cast<double>(s.Zr) - tot);
           s.need_pass = 0;
         }
@@ -358,7 +356,7 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_dense_kernel(VerifyLaunc
     }
     __syncthreads();
     const double target = s.bonus_target;
-    const double tie = static_cast<double>(VD_MARGIN) * Zr;
+    const float tie = VD_MARGIN * Zr;
     double carry = 0.0;
     const int rounds = (nvec + VD_THREADS - 1) / VD_THREADS + 1;  // the last round: the scalar tail
     for (int r = 0; r < rounds; ++r) {
@@ -371,11 +369,23 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_dense_kernel(VerifyLaunc
           const uint4 tv = ldg_stream(trow + static_cast<int64_t>(vi) * 16);
           uint4 dv = make_uint4(0, 0, 0, 0);
           if (residual) dv = ldg_stream(drow + static_cast<int64_t>(vi) * 16);
+          // which of the vector's tokens are zeroed or deterministic: the short
+          // lists are read once per vector, not once per token
+          unsigned zmask = 0u, dmask = 0u;
+          for (int k = 0; k < nz; ++k) {
+            const unsigned o = static_cast<unsigned>(s.zero[k] - id0);
+            if (o < static_cast<unsigned>(E::VEC)) zmask |= 1u << o;
+          }
+          if (residual)
+            for (int k = 0; k < m; ++k) {
+              const unsigned o = static_cast<unsigned>(s.det[k] - id0);
+              if (o < static_cast<unsigned>(E::VEC)) dmask |= 1u << o;
+            }
 #pragma unroll
           for (int q = 0; q < E::VEC; ++q) {
-            const int id = id0 + q;
-            float a = in_list(s.zero, nz, id) ? 0.0f : exp2f((E::get(tv, q) - M) * c) * invZp;
-            if (residual && !in_list(s.det, m, id)) a = fmaxf(0.0f, a - cres * exp2f((E::get(dv, q) - dmax) * c) * qscale);
+            float a = (zmask >> q) & 1u ? 0.0f : exp2f((E::get(tv, q) - M) * c) * invZp;
+            if (residual && !((dmask >> q) & 1u))
+              a = fmaxf(0.0f, a - cres * exp2f((E::get(dv, q) - dmax) * c) * qscale);
             w[q] = a;
           }
           nel = E::VEC;
@@ -391,7 +401,9 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_dense_kernel(VerifyLaunc
           nel = 1;
         }
       }
-      double ts = 0.0;
+      // the round's masses in float (a round is a small part of the row), the
+      // carry of the rounds before in double: the target relative to it
+      float ts = 0.0f;
       int lastp = -1;
 #pragma unroll
       for (int q = 0; q < E::VEC; ++q)
@@ -401,35 +413,36 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_dense_kernel(VerifyLaunc
         }
       if (lastp >= 0) atomicMax(&s.bonus_last, lastp);
       // block exclusive scan of ts
-      double incl = ts;
+      float incl = ts;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(FULL, incl, o);
+        const float y = __shfl_up_sync(FULL, incl, o);
         if (lane >= o) incl += y;
       }
-      if (lane == 31) s.redd[warp] = incl;
+      if (lane == 31) s.red_s[warp] = incl;
       __syncthreads();
-      double before = carry, total = 0.0;
+      float before = 0.0f, total = 0.0f;
       for (int k = 0; k < VD_WARPS; ++k) {
-        const double y = s.redd[k];
+        const float y = s.red_s[k];
         if (k < warp) before += y;
         total += y;
       }
       before += incl - ts;
-      if (ts > 0.0 && before <= target && target < before + ts) {
-        double run = before;
+      const float rel = static_cast<float>(target - carry);
+      if (ts > 0.0f && before <= rel && rel < before + ts) {
+        float run = before;
         int pick = -1;
         for (int q = 0; q < nel && pick < 0; ++q) {
-          const double nx = run + w[q];
-          if (target < nx) {
+          const float nx = run + w[q];
+          if (rel < nx) {
             pick = id0 + q;
-            if (L.margins && (target - run < tie || nx - target < tie)) atomicAdd(L.margins + 1, 1u);
+            if (L.margins && (rel - run < tie || nx - rel < tie)) atomicAdd(L.margins + 1, 1u);
           }
           run = nx;
         }
         if (pick >= 0) atomicMin(reinterpret_cast<unsigned int*>(&s.bonus), static_cast<unsigned int>(pick));
       }
-      carry += total;
+      carry += static_cast<double>(total);
       __syncthreads();
       if (s.bonus >= 0) break;
     }
