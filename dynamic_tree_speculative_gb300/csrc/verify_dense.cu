@@ -115,6 +115,15 @@ __device__ __forceinline__ void for_rows(const uint8_t* trow, const uint8_t* dro
   if (id < V) f(id, E::load(trow, id), with_draft ? E::load(drow, id) : 0.0f);
 }
 
+// 2^x on the special-function unit (PTX ex2.approx.ftz: a few ulp; results
+// below 2^-126 flush to zero).  Every exponential of the kernel uses it, so
+// the children's p and q~ and the row passes agree.
+__device__ __forceinline__ float vd_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ bool in_list(const int* list, int n, int v) {
   for (int k = 0; k < n; ++k)
     if (list[k] == v) return true;
@@ -181,17 +190,17 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_dense_kernel(VerifyLaunc
     for_rows<T>(trow, trow, V, nvec, false, [&](int, float x, float) {
       if (!(x < INFINITY) && !(x == -INFINITY)) nonfinite = true;  // NaN or +inf
       if (x > mx) {
-        sm = sm * exp2f((mx - x) * c) + 1.0f;
+        sm = sm * vd_ex2((mx - x) * c) + 1.0f;
         mx = x;
       } else if (x > -INFINITY) {
-        sm += exp2f((x - mx) * c);
+        sm += vd_ex2((x - mx) * c);
       }
     });
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float om = __shfl_xor_sync(FULL, mx, o), os = __shfl_xor_sync(FULL, sm, o);
       const float nm = fmaxf(mx, om);
-      sm = (mx > -INFINITY ? sm * exp2f((mx - nm) * c) : 0.0f) + (om > -INFINITY ? os * exp2f((om - nm) * c) : 0.0f);
+      sm = (mx > -INFINITY ? sm * vd_ex2((mx - nm) * c) : 0.0f) + (om > -INFINITY ? os * vd_ex2((om - nm) * c) : 0.0f);
       mx = nm;
     }
     if (lane == 0) {
@@ -204,7 +213,7 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_dense_kernel(VerifyLaunc
       for (int w = 0; w < VD_WARPS; ++w) M = fmaxf(M, s.red_m[w]);
       double Z = 0.0;
       for (int w = 0; w < VD_WARPS; ++w)
-        if (s.red_m[w] > -INFINITY) Z += static_cast<double>(s.red_s[w]) * exp2f((s.red_m[w] - M) * c);
+        if (s.red_m[w] > -INFINITY) Z += static_cast<double>(s.red_s[w]) * vd_ex2((s.red_m[w] - M) * c);
       s.M = M;
       s.invZp = static_cast<float>(1.0 / Z);
     }
@@ -231,8 +240,8 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_dense_kernel(VerifyLaunc
         s.ktok[tid] = tok;
         s.kkind[tid] = kind;
         const bool ok = tok >= 0 && tok < V;
-        s.kp[tid] = ok ? exp2f((E::load(trow, tok) - M) * c) * invZp : 0.0f;
-        s.kq[tid] = (ok && kind != SPEC_TREE_DET) ? exp2f((E::load(drow, tok) - s.dmax) * c) * s.qscale : 0.0f;
+        s.kp[tid] = ok ? vd_ex2((E::load(trow, tok) - M) * c) * invZp : 0.0f;
+        s.kq[tid] = (ok && kind != SPEC_TREE_DET) ? vd_ex2((E::load(drow, tok) - s.dmax) * c) * s.qscale : 0.0f;
       }
     }
     __syncthreads();
@@ -262,8 +271,8 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_dense_kernel(VerifyLaunc
         float acc = 0.0f, comp = 0.0f;
         for_rows<T>(trow, drow, V, nvec, true, [&](int id, float x, float dl) {
           if (in_list(s.det, m, id)) return;
-          const float a = in_list(s.zero, nz, id) ? 0.0f : exp2f((x - M) * c) * invZp;
-          const float q = exp2f((dl - dmax) * c) * qscale;
+          const float a = in_list(s.zero, nz, id) ? 0.0f : vd_ex2((x - M) * c) * invZp;
+          const float q = vd_ex2((dl - dmax) * c) * qscale;
           const float y = fminf(a, cres * q) - comp;
           const float tt = acc + y;
           comp = (tt - acc) - y;
@@ -383,9 +392,9 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_dense_kernel(VerifyLaunc
             }
 #pragma unroll
           for (int q = 0; q < E::VEC; ++q) {
-            float a = (zmask >> q) & 1u ? 0.0f : exp2f((E::get(tv, q) - M) * c) * invZp;
+            float a = (zmask >> q) & 1u ? 0.0f : vd_ex2((E::get(tv, q) - M) * c) * invZp;
             if (residual && !((dmask >> q) & 1u))
-              a = fmaxf(0.0f, a - cres * exp2f((E::get(dv, q) - dmax) * c) * qscale);
+              a = fmaxf(0.0f, a - cres * vd_ex2((E::get(dv, q) - dmax) * c) * qscale);
             w[q] = a;
           }
           nel = E::VEC;
@@ -394,9 +403,9 @@ __global__ void __launch_bounds__(VD_THREADS, 1) verify_dense_kernel(VerifyLaunc
         const int id = nvec * E::VEC + tid;
         id0 = id;
         if (id < V) {
-          float a = in_list(s.zero, nz, id) ? 0.0f : exp2f((E::load(trow, id) - M) * c) * invZp;
+          float a = in_list(s.zero, nz, id) ? 0.0f : vd_ex2((E::load(trow, id) - M) * c) * invZp;
           if (residual && !in_list(s.det, m, id))
-            a = fmaxf(0.0f, a - cres * exp2f((E::load(drow, id) - dmax) * c) * qscale);
+            a = fmaxf(0.0f, a - cres * vd_ex2((E::load(drow, id) - dmax) * c) * qscale);
           w[0] = a;
           nel = 1;
         }
